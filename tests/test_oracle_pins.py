@@ -1,0 +1,301 @@
+"""Pins for the float64 oracle against facts fixed outside it.
+
+Each test checks the oracle against something other than itself: values the
+pages state, closed forms, a library routine (torch's float64 scaled dot-product
+attention), definitional invariants, or brute-force loops on tiny inputs. The
+set is chosen so that a dropped term, a wrong sign, a wrong scale, a swapped
+operand pair or a wrong mask fails at least one of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import diffattn_oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _sdpa_causal(q, k, v):
+    """Library routine: torch's float64 CPU causal scaled dot-product attention."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), is_causal=True)[0, 0].numpy()
+
+
+# ----------------------------------------------------------------- lambda ---
+
+def test_lambda_init_matches_page_values():
+    g = json.load(open(os.path.join(GOLDEN, "lambda_init_pages.json")))
+    assert orc.lambda_init_schedule(1) == pytest.approx(g["lambda_init_first_layer"], abs=1e-15)
+    assert orc.lambda_init_schedule(400) == pytest.approx(g["lambda_init_deep_limit"], abs=1e-15)
+    vals = [orc.lambda_init_schedule(l) for l in range(1, 40)]
+    assert all(b > a for a, b in zip(vals, vals[1:])), "lower in early layers, higher in deep ones"
+    assert all(v < g["lambda_init_deep_limit"] for v in vals)
+    lam, lam_init = orc.reparam_lambda(np.zeros(8), np.zeros(8), np.zeros(8), np.zeros(8), layer=5,
+                                       lambda_init_override=g["lambda_init_constant_ablation"])
+    assert lam_init == 0.8 and lam == pytest.approx(0.8, abs=1e-15)
+    with pytest.raises(ValueError):
+        orc.lambda_init_schedule(0)
+
+
+def test_lambda_reparam_closed_forms():
+    z = np.zeros(16)
+    for l in (1, 3, 6, 12, 24):
+        lam, lam_init = orc.reparam_lambda(z, z, z, z, layer=l)
+        assert lam == pytest.approx(lam_init, abs=1e-15), "exp(0) - exp(0) cancels"
+    # lq1.lk1 = ln 3 and lq2.lk2 = ln 2 give 3 - 2 + lambda_init: fixes both exponentials' signs.
+    e0 = np.zeros(4)
+    e0[0] = 1.0
+    lam, lam_init = orc.reparam_lambda(e0 * math.log(3.0), e0, e0 * 0.5, e0 * 2 * math.log(2.0), layer=1)
+    assert lam_init == pytest.approx(0.2, abs=1e-15)
+    assert lam == pytest.approx(1.2, abs=1e-13)
+    # The dot product runs over the whole vectors: spread ln 3 over 4 entries.
+    lam, _ = orc.reparam_lambda(np.full(4, 0.5), np.full(4, math.log(3.0) / 2), z[:4], z[:4], layer=1)
+    assert lam == pytest.approx(3.0 - 1.0 + 0.2, abs=1e-13)
+
+
+# ------------------------------------------------------- mask and softmax ---
+
+def test_masked_softmax_rows_sum_to_one_and_mask_future():
+    rng = _rng(0)
+    n = 37
+    s = rng.normal(size=(n, n)) * 3
+    p = orc.masked_softmax_rows(s, orc.causal_allowed(np.arange(n), n))
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-12)
+    assert np.all(p[np.triu_indices(n, 1)] == 0.0)
+    assert np.all(p[np.tril_indices(n)] > 0.0)
+    assert p[0, 0] == 1.0
+
+
+def test_two_token_closed_form_fixes_sqrt_d_scale():
+    # d = 4, q = 1s, k0 = 0, k1 = (ln 3 / 2) * 1s: q.k1 / sqrt(4) = ln 3, so row 1 weights are (1/4, 3/4).
+    d = 4
+    q = np.ones((2, d))
+    k = np.zeros((2, d))
+    k[1] = math.log(3.0) / 2
+    v = np.array([[1.0, 0.0, 2.0], [0.0, 1.0, -2.0]])
+    o = orc.diffattn_head(q, q, k, k, v, lam=0.0)
+    np.testing.assert_allclose(o[0], v[0], atol=1e-15)
+    np.testing.assert_allclose(o[1], 0.25 * v[0] + 0.75 * v[1], atol=1e-14)
+
+
+# --------------------------------------------- structure against library ---
+
+@pytest.mark.parametrize("n,d,dv,lam", [(1, 8, 16, 0.3), (33, 16, 32, 0.0), (70, 32, 64, 0.7), (130, 8, 16, -0.4)])
+def test_head_is_difference_of_two_library_attentions(n, d, dv, lam):
+    """(P1 - lam P2) V = SDPA(q1,k1,v) - lam SDPA(q2,k2,v): pins pairing, scale, mask and sign."""
+    rng = _rng(n)
+    q1, q2, k1, k2 = (rng.normal(size=(n, d)) for _ in range(4))
+    v = rng.normal(size=(n, dv))
+    got = orc.diffattn_head(q1, q2, k1, k2, v, lam)
+    want = _sdpa_causal(q1, k1, v) - lam * _sdpa_causal(q2, k2, v)
+    np.testing.assert_allclose(got, want, atol=1e-12, rtol=1e-12)
+
+
+def test_lambda_zero_is_standard_causal_attention():
+    rng = _rng(5)
+    q1, q2, k1, k2 = (rng.normal(size=(50, 16)) for _ in range(4))
+    v = rng.normal(size=(50, 24))
+    got = orc.diffattn_head(q1, q2, k1, k2, v, 0.0)
+    np.testing.assert_allclose(got, _sdpa_causal(q1, k1, v), atol=1e-13)
+    # the second map has no influence at lambda = 0
+    got2 = orc.diffattn_head(q1, rng.normal(size=(50, 16)), k1, rng.normal(size=(50, 16)), v, 0.0)
+    np.testing.assert_array_equal(got, got2)
+
+
+def test_identical_maps_scale_standard_attention_by_one_minus_lambda():
+    rng = _rng(6)
+    q, k = rng.normal(size=(40, 8)), rng.normal(size=(40, 8))
+    v = rng.normal(size=(40, 12))
+    for lam in (0.2, 0.8, 1.0, 1.7):
+        got = orc.diffattn_head(q, q, k, k, v, lam)
+        np.testing.assert_allclose(got, (1 - lam) * _sdpa_causal(q, k, v), atol=1e-13)
+
+
+def test_non_causal_option_matches_library():
+    rng = _rng(7)
+    q1, q2, k1, k2 = (rng.normal(size=(20, 8)) for _ in range(4))
+    v = rng.normal(size=(20, 8))
+    t = lambda a: torch.from_numpy(a)[None, None]
+    sd = lambda q, k: torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v))[0, 0].numpy()
+    got = orc.diffattn_head(q1, q2, k1, k2, v, 0.5, causal=False)
+    np.testing.assert_allclose(got, sd(q1, k1) - 0.5 * sd(q2, k2), atol=1e-13)
+
+
+def test_row_chunking_is_exact():
+    rng = _rng(8)
+    q1, q2, k1, k2 = (rng.normal(size=(90, 8)) for _ in range(4))
+    v = rng.normal(size=(90, 8))
+    a = orc.diffattn_head(q1, q2, k1, k2, v, 0.6, row_chunk=512)
+    b = orc.diffattn_head(q1, q2, k1, k2, v, 0.6, row_chunk=7)
+    np.testing.assert_allclose(a, b, atol=1e-14)
+
+
+# ------------------------------------------------------ norm and scale ---
+
+def test_rmsnorm_row_rms_and_weight():
+    rng = _rng(9)
+    o = rng.normal(size=(25, 64)) * rng.uniform(0.01, 5, size=(25, 1))
+    eps = 1e-5
+    for lam_init in (0.2, 0.666, 0.8):
+        y = orc.head_rmsnorm_scale(o, lam_init, eps)
+        ms = np.mean(o * o, axis=1)
+        np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=1)),
+                                   abs(1 - lam_init) * np.sqrt(ms / (ms + eps)), rtol=1e-12)
+        # direction of each row is preserved
+        cos = np.sum(y * o, axis=1) / np.linalg.norm(y, axis=1) / np.linalg.norm(o, axis=1)
+        np.testing.assert_allclose(cos, 1.0, atol=1e-12)
+    w = rng.uniform(0.5, 2.0, size=64)
+    np.testing.assert_allclose(orc.head_rmsnorm_scale(o, 0.3, eps, w), orc.head_rmsnorm_scale(o, 0.3, eps) * w,
+                               rtol=1e-13)
+    assert np.all(orc.head_rmsnorm_scale(np.zeros((2, 8)), 0.3, eps) == 0.0)
+
+
+def test_first_row_closed_form():
+    """Token 0 sees only itself, so O_hat_0 = (1 - lam) V_0 and y_0 has a closed form."""
+    rng = _rng(10)
+    B, H, N, d, Dv = 2, 3, 9, 8, 16
+    q1, q2, k1, k2 = (rng.normal(size=(B, H, N, d)) for _ in range(4))
+    v = rng.normal(size=(B, H, N, Dv))
+    lam, lam_init, eps = 0.45, 0.3, 1e-5
+    out = orc.diffattn_fwd(q1, q2, k1, k2, v, lam, lam_init, eps)
+    o0 = (1 - lam) * v[:, :, 0, :]
+    y0 = o0 / np.sqrt(np.mean(o0 ** 2, axis=-1, keepdims=True) + eps) * (1 - lam_init)
+    np.testing.assert_allclose(out[:, 0, :, :], y0, atol=1e-13)
+
+
+def test_identical_maps_with_lambda_one_give_zero_output():
+    rng = _rng(11)
+    q, k = rng.normal(size=(1, 1, 12, 8)), rng.normal(size=(1, 1, 12, 8))
+    v = rng.normal(size=(1, 1, 12, 8))
+    out = orc.diffattn_fwd(q, q, k, k, v, 1.0, 0.5)
+    assert np.max(np.abs(out)) < 1e-10
+
+
+# --------------------------------------------------- causality, layout ---
+
+def test_causality_later_tokens_do_not_change_earlier_rows():
+    rng = _rng(12)
+    B, H, N, d, Dv = 1, 2, 40, 8, 8
+    t = [rng.normal(size=(B, H, N, d)) for _ in range(4)] + [rng.normal(size=(B, H, N, Dv))]
+    base = orc.diffattn_fwd(*t, 0.6, 0.4)
+    cut = 23
+    t2 = [a.copy() for a in t]
+    for a in t2:
+        a[:, :, cut:] = rng.normal(size=a[:, :, cut:].shape) * 10
+    pert = orc.diffattn_fwd(*t2, 0.6, 0.4)
+    np.testing.assert_array_equal(base[:, :cut], pert[:, :cut])
+    assert np.max(np.abs(base[:, cut:] - pert[:, cut:])) > 1e-3
+
+
+def test_output_layout_is_tokens_then_heads():
+    rng = _rng(13)
+    B, H, N, d, Dv = 2, 3, 5, 4, 6
+    t = [rng.normal(size=(B, H, N, d)) for _ in range(4)] + [rng.normal(size=(B, H, N, Dv))]
+    out = orc.diffattn_fwd(*t, 0.3, 0.2)
+    assert out.shape == (B, N, H, Dv)
+    b, h = 1, 2
+    one = orc.head_rmsnorm_scale(orc.diffattn_head(*(a[b, h] for a in t), 0.3), 0.2)
+    np.testing.assert_array_equal(out[b, :, h, :], one)
+
+
+# ---------------------------------------------------------- brute force ---
+
+def _brute_force_fwd(q1, q2, k1, k2, v, lam, lam_init, eps):
+    """Scalar loops with math.exp: the definition entry by entry."""
+    B, H, N, d = q1.shape
+    Dv = v.shape[-1]
+    out = np.zeros((B, N, H, Dv))
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                w = []
+                for q, k in ((q1, k1), (q2, k2)):
+                    s = [sum(q[b, h, i, c] * k[b, h, j, c] for c in range(d)) / math.sqrt(d) for j in range(i + 1)]
+                    mx = max(s)
+                    e = [math.exp(x - mx) for x in s]
+                    tot = sum(e)
+                    w.append([x / tot for x in e])
+                o = [sum((w[0][j] - lam * w[1][j]) * v[b, h, j, c] for j in range(i + 1)) for c in range(Dv)]
+                rms = math.sqrt(sum(x * x for x in o) / Dv + eps)
+                for c in range(Dv):
+                    out[b, i, h, c] = o[c] / rms * (1 - lam_init)
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_brute_force_tiny(seed):
+    rng = _rng(100 + seed)
+    B, H, N, d, Dv = 1, 2, 11, 3, 5
+    t = [rng.normal(size=(B, H, N, d)) for _ in range(4)] + [rng.normal(size=(B, H, N, Dv))]
+    lam, lam_init = orc.reparam_lambda(*(rng.normal(size=3) * 0.3 for _ in range(4)), layer=3)
+    got = orc.diffattn_fwd(*t, lam, lam_init, 1e-5)
+    np.testing.assert_allclose(got, _brute_force_fwd(*t, lam, lam_init, 1e-5), atol=1e-12)
+
+
+# --------------------------------------------------------------- decode ---
+
+def test_decode_equals_last_prefill_row_and_respects_seq_lens():
+    rng = _rng(14)
+    B, H, L, d, Dv = 3, 2, 30, 8, 16
+    k1, k2 = rng.normal(size=(B, H, L, d)), rng.normal(size=(B, H, L, d))
+    v = rng.normal(size=(B, H, L, Dv))
+    q1, q2 = rng.normal(size=(B, H, L, d)), rng.normal(size=(B, H, L, d))
+    lens = [30, 1, 17]
+    k1n, k2n, vn = k1.copy(), k2.copy(), v.copy()
+    for b, Lb in enumerate(lens):  # entries past each length must be ignored
+        k1n[b, :, Lb:] = np.nan
+        k2n[b, :, Lb:] = np.nan
+        vn[b, :, Lb:] = np.nan
+    qd1 = np.stack([q1[b, :, lens[b] - 1] for b in range(B)])
+    qd2 = np.stack([q2[b, :, lens[b] - 1] for b in range(B)])
+    got = orc.diffattn_decode(qd1, qd2, k1n, k2n, vn, lens, 0.55, 0.47)
+    assert np.all(np.isfinite(got))
+    for b, Lb in enumerate(lens):
+        pre = orc.diffattn_fwd(q1[b:b + 1, :, :Lb], q2[b:b + 1, :, :Lb], k1[b:b + 1, :, :Lb],
+                               k2[b:b + 1, :, :Lb], v[b:b + 1, :, :Lb], 0.55, 0.47)
+        np.testing.assert_allclose(got[b], pre[0, Lb - 1], atol=1e-12)
+
+
+# --------------------------------------------------------------- module ---
+
+def test_module_with_identity_projections_reduces_to_heads():
+    rng = _rng(15)
+    B, N, h, d = 1, 10, 2, 4
+    dm = 2 * d * h
+    Dv = dm // h
+    x = rng.normal(size=(B, N, dm))
+    eye = np.eye(dm)
+    y = orc.module_fwd(x, eye, eye, eye, eye, h, 0.4, 0.3)
+    for i in range(h):
+        xs = x[0, :, 2 * d * i: 2 * d * (i + 1)]
+        o = orc.diffattn_head(xs[:, :d], xs[:, d:], xs[:, :d], xs[:, d:], x[0, :, Dv * i: Dv * (i + 1)], 0.4)
+        np.testing.assert_allclose(y[0, :, Dv * i: Dv * (i + 1)], orc.head_rmsnorm_scale(o, 0.3), atol=1e-13)
+
+
+def test_module_projection_orientation_and_output_linearity():
+    rng = _rng(16)
+    B, N, h, d, Dv, dm = 2, 7, 2, 4, 8, 12
+    x = rng.normal(size=(B, N, dm))
+    wq, wk = rng.normal(size=(dm, 2 * d * h)), rng.normal(size=(dm, 2 * d * h))
+    wv, wo = rng.normal(size=(dm, Dv * h)), rng.normal(size=(Dv * h, dm))
+    y = orc.module_fwd(x, wq, wk, wv, wo, h, 0.5, 0.2)
+    y_cat = orc.module_fwd(x, wq, wk, wv, np.eye(Dv * h), h, 0.5, 0.2)
+    np.testing.assert_allclose(y, y_cat @ wo, atol=1e-12)
+    # Projections are x @ W: feeding pre-projected x with identity weights gives the same result.
+    xq, xk, xv = x @ wq, x @ wk, x @ wv
+    for b in range(B):
+        for i in range(h):
+            o = orc.diffattn_head(xq[b, :, 2 * d * i: 2 * d * i + d], xq[b, :, 2 * d * i + d: 2 * d * (i + 1)],
+                                  xk[b, :, 2 * d * i: 2 * d * i + d], xk[b, :, 2 * d * i + d: 2 * d * (i + 1)],
+                                  xv[b, :, Dv * i: Dv * (i + 1)], 0.5)
+            np.testing.assert_allclose(y_cat[b, :, Dv * i: Dv * (i + 1)], orc.head_rmsnorm_scale(o, 0.2),
+                                       atol=1e-12)
