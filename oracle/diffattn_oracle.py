@@ -119,21 +119,24 @@ def masked_softmax_rows(scores: np.ndarray, allowed: np.ndarray) -> np.ndarray:
 # One head of DiffAttn ("Como a atenção diferencial funciona")
 # --------------------------------------------------------------------------
 
-def diffattn_head(q1, q2, k1, k2, v, lam: float, causal: bool = True, row_chunk: int = 512) -> np.ndarray:
+def diffattn_head(q1, q2, k1, k2, v, lam: float, causal: bool = True, row_chunk: int = 512,
+                  positions=None) -> np.ndarray:
     """O_hat = (softmax(Q1 K1^T/sqrt(d) + M) - lam * softmax(Q2 K2^T/sqrt(d) + M)) V.
 
-    q1, q2: [N, d]; k1, k2: [Nk, d]; v: [Nk, Dv]. Query row i sits at position i
-    and, when causal, sees keys 0..i. Returns the pre-norm head output [N, Dv].
-    Query rows are processed ``row_chunk`` at a time.
+    q1, q2: [n, d]; k1, k2: [Nk, d]; v: [Nk, Dv]. Query row r sits at position
+    ``positions[r]`` (default r) and, when causal, sees keys 0..positions[r].
+    Returns the pre-norm head output [n, Dv]. Query rows are processed
+    ``row_chunk`` at a time.
     """
     q1, q2, k1, k2, v = (_f64(a) for a in (q1, q2, k1, k2, v))
     n, d = q1.shape
     nk = k1.shape[0]
+    pos = np.arange(n) if positions is None else np.asarray(positions)
     scale = 1.0 / math.sqrt(d)
     out = np.empty((n, v.shape[1]), dtype=np.float64)
     for r0 in range(0, n, row_chunk):
         rows = np.arange(r0, min(n, r0 + row_chunk))
-        allowed = causal_allowed(rows, nk) if causal else np.ones((len(rows), nk), dtype=bool)
+        allowed = causal_allowed(pos[rows], nk) if causal else np.ones((len(rows), nk), dtype=bool)
         p1 = masked_softmax_rows((q1[rows] @ k1.T) * scale, allowed)
         p2 = masked_softmax_rows((q2[rows] @ k2.T) * scale, allowed)
         out[rows] = (p1 - lam * p2) @ v

@@ -139,6 +139,16 @@ def test_row_chunking_is_exact():
     np.testing.assert_allclose(a, b, atol=1e-14)
 
 
+def test_row_positions_select_exact_rows():
+    rng = _rng(18)
+    q1, q2, k1, k2 = (rng.normal(size=(60, 8)) for _ in range(4))
+    v = rng.normal(size=(60, 8))
+    full = orc.diffattn_head(q1, q2, k1, k2, v, 0.4)
+    rows = np.array([0, 7, 31, 59])
+    part = orc.diffattn_head(q1[rows], q2[rows], k1, k2, v, 0.4, positions=rows)
+    np.testing.assert_array_equal(part, full[rows])
+
+
 # ------------------------------------------------------ norm and scale ---
 
 def test_rmsnorm_row_rms_and_weight():
