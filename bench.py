@@ -1,0 +1,355 @@
+"""Benchmark of the differential-attention hot path on one GB300 (per rank).
+
+A step is one pass of the prefill path over the B=4, H=16, N=2048, d=64,
+Dv=128 bf16 workload (layer 6): lambda on the host, then the fused tcgen05
+prefill kernel (both maps, combination, per-head RMSNorm, (1 - lambda_init)),
+bf16 output. The headline value is algorithmic TFLOP/s: per (b, h),
+4*Np*d + 2*Np*Dv with Np = N(N+1)/2 causal pairs. The decode path (64
+sequences x 16 heads x 8192 cached tokens) is timed in the same run and
+reported in the "decode" object as HBM GB/s over the KV-cache bytes.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun each rank runs an independent replica (the path needs no
+collective); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "DiffAttn fwd TFLOP/s & % GB300 BF16 peak; decode HBM GB/s & % peak"
+PREFILL = "prefill_bf16"
+DECODE = "decode_bf16"
+NAMES = ("q1", "q2", "k1", "k2", "v")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def prefill_def_flops(w) -> float:
+    n_pairs = w.N * (w.N + 1) / 2
+    return w.B * w.H * (4 * n_pairs * w.d + 2 * n_pairs * w.Dv)
+
+
+def prefill_exec_flops(w) -> float:
+    n_pairs = w.N * (w.N + 1) / 2
+    return w.B * w.H * (4 * n_pairs * w.d + 4 * n_pairs * w.Dv)
+
+
+def decode_kv_bytes(w) -> int:
+    return w.B * w.H * w.N * (2 * w.d + w.Dv) * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"diffattn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags) if fl == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- reference arm (oracle)
+def cpu_oracle_sample(budget_s: float):
+    """Times the float64 oracle on whole heads of the prefill workload until budget_s is used."""
+    from differential_attention_02_gb300 import inputs as gi
+    from oracle import diffattn_oracle as orc
+
+    w = gi.WORKLOADS[PREFILL]
+    t = gi.prefill_inputs(w, B=1)  # batch row 0 of the workload
+    lv = gi.lambda_vectors(w)
+    lam, lam_init = orc.reparam_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+    per_head = prefill_def_flops(w) / (w.B * w.H)
+    heads, t0 = 0, time.perf_counter()
+    while True:
+        h = heads % w.H
+        o = orc.diffattn_head(*(t[k][0, h] for k in NAMES), lam)
+        orc.head_rmsnorm_scale(o, lam_init, w.eps)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return heads, el, heads * per_head / el / 1e12
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_oracle_sample(0.0)
+    vals, total_heads, total_t = [], 0, 0.0
+    for _ in range(args.steps):
+        heads, el, tf = cpu_oracle_sample(args.ref_step_s)
+        vals.append(tf)
+        total_heads += heads
+        total_t += el
+    value = total_heads * prefill_def_flops_unit() / total_t / 1e12
+    cores = cpu_threads()
+    sample = (f"float64 NumPy oracle on whole heads (N=2048, d=64, Dv=128, causal) of the prefill workload, "
+              f"{total_heads} heads in {args.steps} steps of >= {args.ref_step_s:.0f} s")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill B4 H16 N2048 d64 Dv128 causal, layer 6 (sampled heads)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def prefill_def_flops_unit():
+    from differential_attention_02_gb300 import inputs as gi
+    w = gi.WORKLOADS[PREFILL]
+    return prefill_def_flops(w) / (w.B * w.H)
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import differential_attention_02_gb300 as da
+    from differential_attention_02_gb300 import build as dab
+    from differential_attention_02_gb300 import inputs as gi
+
+    dab.build()
+    da.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    peaks, peak_kind = load_peaks()
+
+    # -------- inputs resident in HBM
+    w = gi.WORKLOADS[PREFILL]
+    host = gi.prefill_inputs(w)
+    lv = gi.lambda_vectors(w)
+    x = {k: host[k].to(dev) for k in NAMES}
+    out = torch.empty((w.B, w.N, w.H, w.Dv), dtype=torch.bfloat16, device=dev)
+    ws = da.workspace(256, dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
+
+    def step():
+        lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+        da.diffattn_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam, lam_init, w.eps,
+                        out_dtype=torch.bfloat16, out=out, ws=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert da.read_error(ws) == 0
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # evict L2 between timed steps (not timed)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    clocks = clk.summary()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    ms_step = sum(ms) / len(ms)
+    if world > 1:
+        tt = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    flops = prefill_def_flops(w)
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    achieved = flops / (ms_step * 1e-3) / 1e12  # the prefill kernel is the whole step on the GPU
+    assert da.read_error(ws) == 0
+
+    # -------- end to end from pinned host buffers through the public API
+    pin = {k: host[k].pin_memory() for k in NAMES}
+    out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
+    for _ in range(2):
+        da.diffattn_fwd_host(*(pin[k] for k in NAMES), 0.5, 0.3, w.eps, out_dtype=torch.bfloat16,
+                             device=dev, out_host=out_host)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+        da.diffattn_fwd_host(*(pin[k] for k in NAMES), lam, lam_init, w.eps, out_dtype=torch.bfloat16,
+                             device=dev, out_host=out_host)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in NAMES)
+    d2h = out_host.numel() * out_host.element_size()
+    del x, out, pin, out_host
+
+    # -------- decode workload (HBM bound; 4.3 GB of KV cache, larger than L2)
+    dec = None
+    if not args.skip_decode:
+        wd = gi.WORKLOADS[DECODE]
+        hd = gi.decode_inputs(wd)
+        lvd = gi.lambda_vectors(wd)
+        y = {k: hd[k].to(dev) for k in NAMES}
+        del hd
+        dout = torch.empty((wd.B, wd.H, wd.Dv), dtype=torch.bfloat16, device=dev)
+        dws = da.workspace(da.decode_workspace_bytes(wd.B, wd.H, wd.N, wd.d, wd.Dv), dev)
+        lam, lam_init = da.diffattn_lambda(lvd["lq1"], lvd["lk1"], lvd["lq2"], lvd["lk2"], wd.layer)
+
+        def dstep():
+            da.diffattn_decode(y["q1"], y["q2"], y["k1"], y["k2"], y["v"], lam, lam_init, eps=wd.eps,
+                               out_dtype=torch.bfloat16, out=dout, ws=dws, stream=stream)
+
+        for _ in range(max(3, args.warmup)):
+            dstep()
+        torch.cuda.synchronize()
+        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+        for i in range(args.steps):
+            dev_ev[i][0].record(stream)
+            dstep()
+            dev_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert da.read_error(dws) == 0
+        dms = sum(a.elapsed_time(b) for a, b in dev_ev) / args.steps
+        kvb = decode_kv_bytes(wd)
+        gbs = kvb / (dms * 1e-3) / 1e9
+        dec = {"workload": "decode 64 seqs x 1 token, H16, L8192, d64, Dv128, layer 3", "ms_per_step": dms,
+               "value": gbs, "unit": "GB/s", "kv_bytes_per_step": kvb,
+               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
+                            "frac_of_spec_8tbs": gbs / 8000.0},
+               "gpu_launches_per_step": 2}
+        del y
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.skip_cpu_baseline and world == 1:
+        heads, el, tf = cpu_oracle_sample(args.cpu_budget_s)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{heads} whole heads (N=2048, d=64, Dv=128, causal) of the prefill workload, "
+                         f"float64 NumPy, {el:.1f} s"}
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill B4 H16 N2048 d64 Dv128 causal, layer 6, bf16 in/out, fp32 accumulate",
+                   "l2": "flushed between timed steps (256 MB write, untimed)",
+                   "flops": "algorithmic: 4*Np*d + 2*Np*Dv per (b,h), Np = N(N+1)/2",
+                   "exec_tflops": world * prefill_exec_flops(w) / (ms_step * 1e-3) / 1e12,
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": f"{peak_kind} bf16 burst"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "decode": dec,
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-step-s", type=float, default=8.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

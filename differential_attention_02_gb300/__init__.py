@@ -1,0 +1,250 @@
+"""Python binding of libdiffattn.so (causal multi-head differential attention, GB300).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels. PyTorch supplies device memory and the current CUDA stream. The
+library must have been built (``differential_attention_02_gb300.build.build()``);
+if it is missing, every call raises instead of computing anything elsewhere.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdiffattn.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
+F32, BF16 = 0, 1
+
+EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_workspace_size",
+            "diffattn_decode", "diffattn_decode_workspace_size", "diffattn_gemm_bf16",
+            "diffattn_gemm_workspace_size", "diffattn_read_error")
+
+
+class DiffAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class Tensor4(ctypes.Structure):
+    """diffattn_tensor: pointer plus (b, h, n) strides in elements."""
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64),
+                ("stride_n", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libdiffattn.so and declares its signatures (raises if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with differential_attention_02_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.diffattn_status_string.restype = ctypes.c_char_p
+    lib.diffattn_status_string.argtypes = [i32]
+    lib.diffattn_lambda.restype = i32
+    lib.diffattn_lambda.argtypes = [fp, fp, fp, fp, i32, i32, f32, fp, fp]
+    lib.diffattn_fwd.restype = i32
+    lib.diffattn_fwd.argtypes = [Tensor4] * 5 + [vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, f32, i32, i32,
+                                                 vp, sz, vp]
+    lib.diffattn_fwd_workspace_size.restype = i32
+    lib.diffattn_fwd_workspace_size.argtypes = [i32] * 5 + [ctypes.POINTER(sz)]
+    lib.diffattn_decode.restype = i32
+    lib.diffattn_decode.argtypes = [vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, vp, vp, i32, i32, i32, i32, f32,
+                                    f32, f32, i32, i32, vp, sz, vp]
+    lib.diffattn_decode_workspace_size.restype = i32
+    lib.diffattn_decode_workspace_size.argtypes = [i32] * 6 + [ctypes.POINTER(sz)]
+    lib.diffattn_gemm_bf16.restype = i32
+    lib.diffattn_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i64, i32, vp, sz, vp]
+    lib.diffattn_gemm_workspace_size.restype = i32
+    lib.diffattn_gemm_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+    lib.diffattn_read_error.restype = i32
+    lib.diffattn_read_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().diffattn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise DiffAttnError(status, what)
+
+
+def _stream_ptr(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt) -> int:
+    if dt == torch.float32:
+        return F32
+    if dt == torch.bfloat16:
+        return BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _t4(t: torch.Tensor) -> Tensor4:
+    """[B, H, rows, width] view with a contiguous last dim -> diffattn_tensor."""
+    if t.dim() != 4 or t.stride(-1) != 1:
+        raise ValueError("operand must be 4-D [B, H, rows, width] with a contiguous last dimension")
+    return Tensor4(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+# ------------------------------------------------------------------ workspace
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-initialised, 256-byte-aligned device buffer of at least nbytes (cached per device)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    key = dev.index
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(int(nbytes), 256) + 256, dtype=torch.uint8, device=dev)
+        _ws_cache[key] = buf
+    off = (-buf.data_ptr()) % 256
+    return buf[off:]
+
+
+def read_error(ws: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word of a workspace."""
+    code = ctypes.c_int32(0)
+    st = load_library().diffattn_read_error(ctypes.c_void_p(ws.data_ptr()), _stream_ptr(stream), ctypes.byref(code))
+    if st not in (OK, ERR_TIMEOUT):
+        _check(st, "diffattn_read_error")
+    return code.value
+
+
+# ------------------------------------------------------------------ entry points
+def diffattn_lambda(lq1, lk1, lq2, lk2, layer: int, lambda_init_override: float | None = None):
+    """lambda and lambda_init (host computation in double, returned as floats)."""
+    vs = [torch.as_tensor(v, dtype=torch.float32).contiguous().reshape(-1) for v in (lq1, lk1, lq2, lk2)]
+    d = vs[0].numel()
+    if any(v.numel() != d for v in vs):
+        raise ValueError("lambda vectors must have one common length")
+    lam, lam_init = ctypes.c_float(), ctypes.c_float()
+    fp = ctypes.POINTER(ctypes.c_float)
+    ptrs = [ctypes.cast(v.data_ptr(), fp) for v in vs]
+    ov = -1.0 if lambda_init_override is None else float(lambda_init_override)
+    _check(load_library().diffattn_lambda(*ptrs, d, int(layer), ov, ctypes.byref(lam), ctypes.byref(lam_init)),
+           "diffattn_lambda")
+    return lam.value, lam_init.value
+
+
+def diffattn_fwd(q1, q2, k1, k2, v, lam: float, lam_init: float, eps: float = 1e-5, norm_weight=None,
+                 causal: bool = True, out_dtype=torch.float32, out=None, ws=None, stream=None) -> torch.Tensor:
+    """Fused prefill. q1,q2,k1,k2: [B,H,N,d]; v: [B,H,N,Dv] (CUDA, fp32 or bf16). Returns [B,N,H,Dv]."""
+    B, H, N, d = q1.shape
+    Dv = v.shape[-1]
+    for t in (q1, q2, k1, k2, v):
+        if not t.is_cuda or t.dtype != q1.dtype:
+            raise ValueError("all operands must be CUDA tensors of one dtype")
+    if out is None:
+        out = torch.empty((B, N, H, Dv), dtype=out_dtype, device=q1.device)
+    lib = load_library()
+    nbytes = ctypes.c_size_t()
+    _check(lib.diffattn_fwd_workspace_size(B, H, N, d, Dv, ctypes.byref(nbytes)), "diffattn_fwd_workspace_size")
+    ws = workspace(nbytes.value, q1.device) if ws is None else ws
+    w = None if norm_weight is None else ctypes.c_void_p(norm_weight.data_ptr())
+    _check(lib.diffattn_fwd(_t4(q1), _t4(q2), _t4(k1), _t4(k2), _t4(v), ctypes.c_void_p(out.data_ptr()), w,
+                            B, H, N, d, Dv, int(bool(causal)), float(lam), float(lam_init), float(eps),
+                            _dtype_code(q1.dtype), _dtype_code(out.dtype), ctypes.c_void_p(ws.data_ptr()),
+                            ws.numel(), _stream_ptr(stream)), "diffattn_fwd")
+    return out
+
+
+def decode_workspace_bytes(B, H, L, d, Dv, num_splits=0) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().diffattn_decode_workspace_size(B, H, L, d, Dv, num_splits, ctypes.byref(n)),
+           "diffattn_decode_workspace_size")
+    return n.value
+
+
+def diffattn_decode(q1, q2, k1_cache, k2_cache, v_cache, lam: float, lam_init: float, seq_lens=None, L=None,
+                    eps: float = 1e-5, norm_weight=None, num_splits: int = 0, out_dtype=torch.float32, out=None,
+                    ws=None, stream=None) -> torch.Tensor:
+    """Split-KV decode. q: [B,H,d]; caches [B,H,Lmax,*] bf16; seq_lens int32 [B] (CUDA) or None. -> [B,H,Dv]."""
+    B, H, d = q1.shape
+    Dv = v_cache.shape[-1]
+    L = k1_cache.shape[2] if L is None else int(L)
+    if out is None:
+        out = torch.empty((B, H, Dv), dtype=out_dtype, device=q1.device)
+    nbytes = decode_workspace_bytes(B, H, L, d, Dv, num_splits)
+    ws = workspace(nbytes, q1.device) if ws is None else ws
+    sl = None
+    if seq_lens is not None:
+        if seq_lens.dtype != torch.int32 or not seq_lens.is_cuda:
+            raise ValueError("seq_lens must be a CUDA int32 tensor")
+        sl = ctypes.c_void_p(seq_lens.data_ptr())
+    w = None if norm_weight is None else ctypes.c_void_p(norm_weight.data_ptr())
+    _check(load_library().diffattn_decode(
+        ctypes.c_void_p(q1.data_ptr()), ctypes.c_void_p(q2.data_ptr()), _t4(k1_cache), _t4(k2_cache), _t4(v_cache),
+        sl, L, ctypes.c_void_p(out.data_ptr()), w, B, H, d, Dv, float(lam), float(lam_init), float(eps),
+        int(num_splits), _dtype_code(out.dtype), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream)),
+        "diffattn_decode")
+    return out
+
+
+def gemm_bf16(a: torch.Tensor, w: torch.Tensor, out_dtype=torch.bfloat16, out=None, ws=None, stream=None):
+    """C = a @ w with a [M,K] and w [K,N] bf16 row-major (unit last stride); tcgen05 kernel."""
+    M, K = a.shape
+    K2, N = w.shape
+    if K2 != K or a.stride(1) != 1 or w.stride(1) != 1:
+        raise ValueError("a [M,K] and w [K,N] with contiguous rows")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    ws = workspace(256, a.device) if ws is None else ws
+    _check(load_library().diffattn_gemm_bf16(
+        ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(out.data_ptr()), M, N, K,
+        a.stride(0), w.stride(0), out.stride(0), _dtype_code(out.dtype), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+        _stream_ptr(stream)), "diffattn_gemm_bf16")
+    return out
+
+
+def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float, eps: float = 1e-5,
+               norm_weight=None, ws=None, stream=None):
+    """Multi-head differential attention module, bf16: three projection GEMMs, the fused
+    attention reading Q/K/V in place through strided views, and the W_O GEMM.
+
+    x [B,N,d_model]; w_q, w_k [d_model, h*2d]; w_v [d_model, h*Dv]; w_o [h*Dv, d_model].
+    Head i uses Q[..., 2di:2di+d] as Q1 and Q[..., 2di+d:2d(i+1)] as Q2 (K likewise).
+    """
+    B, N, dm = x.shape
+    h = n_heads
+    d = w_q.shape[1] // (2 * h)
+    Dv = w_v.shape[1] // h
+    x2 = x.reshape(B * N, dm)
+    q = gemm_bf16(x2, w_q, ws=ws, stream=stream)
+    k = gemm_bf16(x2, w_k, ws=ws, stream=stream)
+    v = gemm_bf16(x2, w_v, ws=ws, stream=stream)
+    # [B*N, h*2d] -> [B, h, N, 2d] views (no copies): strides (N*h*2d, 2d, h*2d, 1)
+    q4 = q.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
+    k4 = k.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
+    v4 = v.view(B, N, h, Dv).permute(0, 2, 1, 3)
+    att = diffattn_fwd(q4[..., :d], q4[..., d:], k4[..., :d], k4[..., d:], v4, lam, lam_init, eps, norm_weight,
+                       out_dtype=torch.bfloat16, ws=ws, stream=stream)
+    y = gemm_bf16(att.view(B * N, h * Dv), w_o, ws=ws, stream=stream)
+    return y.view(B, N, dm)
+
+
+def diffattn_fwd_host(q1, q2, k1, k2, v, lam, lam_init, eps=1e-5, out_dtype=torch.float32, device="cuda",
+                      stream=None, out_host=None):
+    """End-to-end call from pinned HOST tensors: copy in, run the fused prefill, copy the result out."""
+    dev = [t.to(device, non_blocking=True) for t in (q1, q2, k1, k2, v)]
+    out = diffattn_fwd(*dev, lam, lam_init, eps, out_dtype=out_dtype, stream=stream)
+    if out_host is None:
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    out_host.copy_(out, non_blocking=True)
+    return out_host

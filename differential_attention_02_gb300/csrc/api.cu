@@ -1,0 +1,313 @@
+// Host side of the C ABI declared in include/diffattn.h: argument checks,
+// TMA descriptor encoding, kernel dispatch. No device memory is allocated
+// here and nothing synchronises except diffattn_read_error.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/diffattn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace da;
+
+namespace {
+
+// ---------------------------------------------------------------- helpers
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// 4-D bf16 map over a [B, H, rows, width] operand (strides in elements).
+// Size-1 dimensions get a harmless stride, since their stride is never used.
+bool encode_4d(CUtensorMap* m, const diffattn_tensor& t, int width, int rows, int H, int B, int box_w, int box_rows,
+               CUtensorMapSwizzle sw) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int64_t sn = t.stride_n, sh = (H > 1) ? t.stride_h : (int64_t)rows * sn,
+                  sb = (B > 1) ? t.stride_b : (int64_t)H * sh;
+    cuuint64_t dims[4] = {(cuuint64_t)width, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)(sn * 2), (cuuint64_t)(sh * 2), (cuuint64_t)(sb * 2)};
+    cuuint32_t box[4] = {(cuuint32_t)box_w, (cuuint32_t)box_rows, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(t.ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_2d(CUtensorMap* m, const void* ptr, int inner, int outer, int64_t ld, int box_inner, int box_outer) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand [B, H, rows, width], last dim contiguous; strides in elements; every
+// byte stride a multiple of 16 and the row stride at least the width.
+bool check_operand(const diffattn_tensor& t, int width, int elem_bytes) {
+    if (t.ptr == nullptr || !aligned16(t.ptr)) return false;
+    const int64_t q = 16 / elem_bytes;
+    if (t.stride_n < width || t.stride_n % q) return false;
+    if (t.stride_h < 0 || t.stride_h % q || t.stride_b < 0 || t.stride_b % q) return false;
+    return true;
+}
+
+diffattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA; }
+
+int32_t* err_word(void* ws) { return reinterpret_cast<int32_t*>(ws); }
+
+// Decode split count: the smallest split count whose CTA waves are at least 90%
+// full on this GPU, capped so that every split keeps at least 256 keys.
+int decode_auto_splits(int B, int H, int L, int d) {
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
+    const int per_sm = (d == 64) ? 2 : 1;  // resident split CTAs per SM (shared-memory bound)
+    const double slots = (double)sms * per_sm;
+    const int smax = std::max(1, std::min(256, L / 256));
+    for (int s = 1; s <= smax; ++s) {
+        const double waves = (double)B * H * s / slots;
+        if (waves >= 1.0 && waves / ceil(waves) >= 0.9) return s;
+        if (waves < 1.0 && s == smax) return s;
+    }
+    return smax;
+}
+
+void decode_geometry(int B, int H, int L, int d, int num_splits, int* S, int* kps) {
+    int s = num_splits > 0 ? num_splits : decode_auto_splits(B, H, L, d);
+    const int stage = decode_keys_per_stage(d);
+    int k = (L + s - 1) / s;
+    k = (k + stage - 1) / stage * stage;
+    s = (L + k - 1) / k;  // no split left without keys
+    *S = s;
+    *kps = k;
+}
+
+size_t decode_ws_bytes(int B, int H, int S, int Dv) {
+    return kControlBytes + (size_t)B * H * S * 4 * sizeof(float) + (size_t)B * H * S * 2 * Dv * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* diffattn_status_string(int s) {
+    switch (s) {
+        case DIFFATTN_OK: return "ok";
+        case DIFFATTN_ERR_INVALID_ARG: return "invalid argument";
+        case DIFFATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case DIFFATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case DIFFATTN_ERR_CUDA: return "CUDA error";
+        case DIFFATTN_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2, int d,
+                                int layer, float lambda_init_override, float* lambda_out, float* lambda_init_out) {
+    if (!lq1 || !lk1 || !lq2 || !lk2 || !lambda_out || !lambda_init_out || d < 1) return DIFFATTN_ERR_INVALID_ARG;
+    double lam_init;
+    if (lambda_init_override >= 0.f) {
+        lam_init = lambda_init_override;
+    } else {
+        if (layer < 1) return DIFFATTN_ERR_INVALID_ARG;
+        lam_init = 0.8 - 0.6 * exp(-0.3 * (double)(layer - 1));
+    }
+    double d1 = 0.0, d2 = 0.0;
+    for (int i = 0; i < d; ++i) {
+        d1 += (double)lq1[i] * (double)lk1[i];
+        d2 += (double)lq2[i] * (double)lk2[i];
+    }
+    const double lam = exp(d1) - exp(d2) + lam_init;
+    if (!isfinite(lam)) return DIFFATTN_ERR_INVALID_ARG;
+    *lambda_out = (float)lam;
+    *lambda_init_out = (float)lam_init;
+    return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_fwd_workspace_size(int B, int H, int N, int d, int Dv, size_t* bytes) {
+    if (!bytes || B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    *bytes = kControlBytes;
+    return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                             diffattn_tensor v, void* out, const float* norm_weight, int B, int H, int N, int d,
+                             int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype,
+                             int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if ((in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16) ||
+        (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (!isfinite(lambda) || !isfinite(lambda_init) || !(eps >= 0.f) || !isfinite(eps))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || N == 0) return DIFFATTN_OK;
+    const int eb = in_dtype == DIFFATTN_F32 ? 4 : 2;
+    if (!check_operand(q1, d, eb) || !check_operand(q2, d, eb) || !check_operand(k1, d, eb) ||
+        !check_operand(k2, d, eb) || !check_operand(v, Dv, eb))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (out == nullptr || !aligned16(out)) return DIFFATTN_ERR_INVALID_ARG;
+    if (norm_weight != nullptr && !aligned16(norm_weight)) return DIFFATTN_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < kControlBytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DIFFATTN_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (in_dtype == DIFFATTN_F32) {
+        if (d > 128 || d % 4 || Dv > 256 || Dv % 32) return DIFFATTN_ERR_UNSUPPORTED;
+        SimtF32Params p{};
+        p.q1 = static_cast<const float*>(q1.ptr);
+        p.q2 = static_cast<const float*>(q2.ptr);
+        p.k1 = static_cast<const float*>(k1.ptr);
+        p.k2 = static_cast<const float*>(k2.ptr);
+        p.v = static_cast<const float*>(v.ptr);
+        const diffattn_tensor* ts[5] = {&q1, &q2, &k1, &k2, &v};
+        int64_t* ss[5] = {p.sq1, p.sq2, p.sk1, p.sk2, p.sv};
+        for (int i = 0; i < 5; ++i) {
+            ss[i][0] = ts[i]->stride_b;
+            ss[i][1] = ts[i]->stride_h;
+            ss[i][2] = ts[i]->stride_n;
+        }
+        p.out = out;
+        p.out_bf16 = out_dtype == DIFFATTN_BF16;
+        p.norm_w = norm_weight;
+        p.B = B; p.H = H; p.N = N; p.d = d; p.Dv = Dv; p.causal = causal != 0;
+        p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
+        return cuda_status(launch_fwd_simt_f32(p, st));
+    }
+
+    if (!(d == 64 && Dv == 128)) return DIFFATTN_ERR_UNSUPPORTED;
+    FwdParams p{};
+    if (!encode_4d(&p.tm_q1, q1, d, N, H, B, 64, kFwdBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_4d(&p.tm_q2, q2, d, N, H, B, 64, kFwdBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_4d(&p.tm_k1, k1, d, N, H, B, 64, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_4d(&p.tm_k2, k2, d, N, H, B, 64, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_4d(&p.tm_v, v, Dv, N, H, B, 64, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return DIFFATTN_ERR_INVALID_ARG;
+    p.out = out;
+    p.out_bf16 = out_dtype == DIFFATTN_BF16;
+    p.norm_w = norm_weight;
+    p.B = B; p.H = H; p.N = N; p.d = d; p.Dv = Dv; p.causal = causal != 0;
+    p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
+    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+    p.err = err_word(workspace);
+    return cuda_status(launch_fwd_bf16(p, st));
+}
+
+diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int Dv, int num_splits, size_t* bytes) {
+    if (!bytes || B < 0 || H < 0 || L < 1 || d < 1 || Dv < 1 || num_splits < 0 || num_splits > 256)
+        return DIFFATTN_ERR_INVALID_ARG;
+    int S, kps;
+    decode_geometry(B, H, L, d, num_splits, &S, &kps);
+    *bytes = decode_ws_bytes(B, H, S, Dv);
+    return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor k1_cache, diffattn_tensor k2_cache,
+                                diffattn_tensor v_cache, const int32_t* seq_lens, int L, void* out,
+                                const float* norm_weight, int B, int H, int d, int Dv, float lambda,
+                                float lambda_init, float eps, int num_splits, int out_dtype, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    if (B < 0 || H < 0 || L < 1 || d < 1 || Dv < 1 || num_splits < 0 || num_splits > 256)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if (!isfinite(lambda) || !isfinite(lambda_init) || !(eps >= 0.f) || !isfinite(eps))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return DIFFATTN_OK;
+    if (!q1 || !q2 || !aligned16(q1) || !aligned16(q2) || !out || !aligned16(out)) return DIFFATTN_ERR_INVALID_ARG;
+    if (!check_operand(k1_cache, d, 2) || !check_operand(k2_cache, d, 2) || !check_operand(v_cache, Dv, 2))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (norm_weight != nullptr && !aligned16(norm_weight)) return DIFFATTN_ERR_INVALID_ARG;
+    if (!((d == 64 && Dv == 128) || (d == 128 && Dv == 256))) return DIFFATTN_ERR_UNSUPPORTED;
+    DecodeParams p{};
+    decode_geometry(B, H, L, d, num_splits, &p.num_splits, &p.keys_per_split);
+    const size_t need = decode_ws_bytes(B, H, p.num_splits, Dv);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DIFFATTN_ERR_WORKSPACE;
+    const int stage = decode_keys_per_stage(d);
+    if (!encode_4d(&p.tm_k1, k1_cache, d, L, H, B, 64, stage, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_4d(&p.tm_k2, k2_cache, d, L, H, B, 64, stage, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_4d(&p.tm_v, v_cache, Dv, L, H, B, Dv, stage, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return DIFFATTN_ERR_INVALID_ARG;
+    p.q1 = q1;
+    p.q2 = q2;
+    p.seq_lens = seq_lens;
+    p.L = L;
+    p.out = out;
+    p.out_bf16 = out_dtype == DIFFATTN_BF16;
+    p.norm_w = norm_weight;
+    p.B = B; p.H = H; p.d = d; p.Dv = Dv;
+    p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.err = err_word(workspace);
+    p.part_stats = reinterpret_cast<float*>(ws + kControlBytes);
+    p.part_o = p.part_stats + (size_t)B * H * p.num_splits * 4;
+    return cuda_status(launch_decode_bf16(p, static_cast<cudaStream_t>(stream)));
+}
+
+diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes) {
+    if (!bytes || M < 0 || N < 0 || K < 0) return DIFFATTN_ERR_INVALID_ARG;
+    *bytes = kControlBytes;
+    return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M, int N, int K, int64_t lda,
+                                   int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    if (M < 1 || N < 1 || K < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if (!A || !W || !C || !aligned16(A) || !aligned16(W) || !aligned16(C)) return DIFFATTN_ERR_INVALID_ARG;
+    const int cq = out_dtype == DIFFATTN_F32 ? 4 : 8;
+    if (lda < K || lda % 8 || ldw < N || ldw % 8 || ldc < N || ldc % cq || N % 8) return DIFFATTN_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < kControlBytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DIFFATTN_ERR_WORKSPACE;
+    GemmParams p{};
+    if (!encode_2d(&p.tm_a, A, K, M, lda, kGemmBK, kGemmBM) || !encode_2d(&p.tm_w, W, N, K, ldw, 64, kGemmBK))
+        return DIFFATTN_ERR_INVALID_ARG;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = M; p.N = N; p.K = K;
+    p.out_bf16 = out_dtype == DIFFATTN_BF16;
+    p.err = err_word(workspace);
+    return cuda_status(launch_gemm_bf16(p, static_cast<cudaStream_t>(stream)));
+}
+
+diffattn_status diffattn_read_error(void* workspace, void* stream, int32_t* device_code) {
+    if (!workspace || !device_code) return DIFFATTN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t code = 0;
+    if (cudaMemcpyAsync(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    *device_code = code;
+    if (code == 0) return DIFFATTN_OK;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    return DIFFATTN_ERR_TIMEOUT;
+}
+
+}  // extern "C"

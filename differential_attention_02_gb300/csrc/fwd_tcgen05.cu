@@ -1,0 +1,425 @@
+// Fused causal prefill of differential attention on the 5th-generation
+// tensor cores (tcgen05.mma with TMEM accumulators), fed by TMA.
+//
+// What it computes, per head: (softmax(Q1K1^T/sqrt d) - lambda
+// softmax(Q2K2^T/sqrt d)) V — the DiffAttn formula of "Differential
+// Transformer: Transformer que cancela ruído de atenção" (section "Como a
+// atenção diferencial funciona") under the causal mask of the intoai.pub page
+// ("A Deeper Dive Into Attention Calculations") — then each head's RMSNorm
+// and the (1 - lambda_init) scale (section "Estrutura multi-head e
+// arquitetura completa"). The output is written [B, N, H, Dv].
+//
+// The two maps only meet in the epilogue: map m keeps its own running max and
+// sum and its own accumulator O_m = sum_j exp(S_m - max_m) V_j, and the
+// epilogue forms O1/l1 - lambda O2/l2. (The pages' remark that FlashAttention
+// can be reused is prior art only; nothing of it is followed here.)
+//
+// CTA = one 128-row query tile of one (b, h); 12 warps:
+//   warp 0       TMA producer: Q1, Q2 once, then a 2-stage ring of (K1, K2, V)
+//                tiles of 128 keys, all 128-byte swizzled.
+//   warp 1       allocates 512 TMEM columns; one lane issues every MMA:
+//                S1 = Q1 K1^T, S2 = Q2 K2^T (fp32 in TMEM), O1 += P1 V,
+//                O2 += P2 V (P from shared memory, fp32 O in TMEM).
+//   warps 4..7   softmax of map 1; warps 8..11 softmax of map 2. Thread r of a
+//                group owns query row r (TMEM lane r): it reads its S row,
+//                updates max and sum, writes its P row as bf16 into shared
+//                memory, and rescales its O row in TMEM only when the running
+//                max grew by more than 2^8 (the stale max is exact because
+//                the final division uses the same max).
+//   epilogue     both softmax groups: O1/l1 - lambda O2/l2, row RMSNorm,
+//                (1 - lambda_init), norm weight, store.
+// The MMA order S1(j+1), PV2(j), S2(j+1), PV1(j+1) lets one group's softmax
+// run while the tensor core works for the other map.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace da {
+namespace {
+
+constexpr int BM = kFwdBM, BN = kFwdBN;
+constexpr int kThreads = 12 * 32;
+constexpr int kKvStages = 2;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D, int DV>
+struct FwdCfg {
+    static constexpr int kQBytes = BM * D * 2;       // one Q half tile
+    static constexpr int kKBytes = BN * D * 2;       // one K half tile
+    static constexpr int kVBytes = BN * DV * 2;
+    static constexpr int kBoxBytes = 128 * 128;      // one [128 rows][64 bf16] box
+    static constexpr int kStageBytes = 2 * kKBytes + kVBytes;
+    static constexpr int kPBytes = BM * BN * 2;      // one P tile (bf16)
+    static constexpr int kOffQ1 = 0;
+    static constexpr int kOffQ2 = kQBytes;
+    static constexpr int kOffStages = 2 * kQBytes;
+    static constexpr int kOffP = kOffStages + kKvStages * kStageBytes;
+    static constexpr int kOffBar = kOffP + 2 * kPBytes;
+    static constexpr int kBarBytes = 256;
+    // The epilogue's exchange buffer (4 x 128 floats) reuses the P tiles, which
+    // are idle once the last PV MMAs have completed.
+    static constexpr int kOffEpi = kOffP;
+    static constexpr size_t kSmem = 1024 + (size_t)kOffBar + kBarBytes;
+    static_assert(kSmem <= 232448, "shared memory budget");
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0;               // S1 at 0, S2 at BN
+    static constexpr uint32_t kColO = 2 * BN;          // O1 at 2BN, O2 at 2BN + DV
+    static_assert(2 * BN + 2 * DV <= 512, "TMEM budget");
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t kv_full[kKvStages];
+    uint64_t kv_empty[kKvStages];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_done[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr, uint32_t k_addr) {
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+        umma_ss(s_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
+                kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int DV>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_addr, uint32_t v_addr, bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, DV, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint64_t a = sdesc_sw128(p_addr + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
+        // V tile: boxes of [BN keys][64 columns]; next 64 columns = next box (leading
+        // offset), next 8 keys = +1024 bytes (stride offset); 16 keys = 2048 bytes.
+        const uint64_t b = sdesc_sw128(v_addr + kk * 16 * 128, BN * 128, 1024);
+        umma_ss(o_tmem, a, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <int D, int DV>
+__global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
+    using C = FwdCfg<D, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
+    float* epi = reinterpret_cast<float*>(smem + C::kOffEpi);  // [4][BM]: 1/l1, lambda/l2, ss1, ss2
+    volatile int* abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = (p.N + BM - 1) / BM;
+    const int BH = p.B * p.H;
+    const int qt = n_tiles - 1 - (int)(blockIdx.x / BH);  // heaviest causal tiles first
+    const int bh = blockIdx.x % BH;
+    const int b = bh / p.H, h = bh % p.H;
+    const int q0 = qt * BM;
+    const int nkv = p.causal ? min(qt + 1, n_tiles) : n_tiles;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        for (int s = 0; s < kKvStages; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&bars->s_full[g], 1);
+            mbar_init(&bars->p_full[g], 128);
+            mbar_init(&bars->o_done[g], 1);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    uint8_t* q1s = smem + C::kOffQ1;
+    uint8_t* q2s = smem + C::kOffQ2;
+    uint8_t* stages = smem + C::kOffStages;
+    uint8_t* ps = smem + C::kOffP;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tm_q1);
+            tma_prefetch_desc(&p.tm_q2);
+            tma_prefetch_desc(&p.tm_k1);
+            tma_prefetch_desc(&p.tm_k2);
+            tma_prefetch_desc(&p.tm_v);
+            mbar_arrive_expect_tx(&bars->q_full, 2 * C::kQBytes);
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) {
+                tma_load_4d(q1s + x * C::kBoxBytes, &p.tm_q1, &bars->q_full, x * 64, q0, h, b);
+                tma_load_4d(q2s + x * C::kBoxBytes, &p.tm_q2, &bars->q_full, x * 64, q0, h, b);
+            }
+            int j = 0;
+            for (; j < nkv; ++j) {
+                const int s = j % kKvStages;
+                if (!mbar_wait(&bars->kv_empty[s], ((j / kKvStages) & 1) ^ 1, abort_flag, p.err, 0x31)) break;
+                uint8_t* st = stages + s * C::kStageBytes;
+                mbar_arrive_expect_tx(&bars->kv_full[s], C::kStageBytes);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x) {
+                    tma_load_4d(st + x * C::kBoxBytes, &p.tm_k1, &bars->kv_full[s], x * 64, j * BN, h, b);
+                    tma_load_4d(st + C::kKBytes + x * C::kBoxBytes, &p.tm_k2, &bars->kv_full[s], x * 64, j * BN, h,
+                                b);
+                }
+#pragma unroll
+                for (int x = 0; x < DV / 64; ++x)
+                    tma_load_4d(st + 2 * C::kKBytes + x * C::kBoxBytes, &p.tm_v, &bars->kv_full[s], x * 64, j * BN,
+                                h, b);
+            }
+            // Drain: no copy may still be landing in shared memory when the CTA exits.
+            mbar_wait(&bars->q_full, 0, nullptr, p.err, 0x32);
+            for (int u = max(0, j - kKvStages); u < j; ++u)
+                mbar_wait(&bars->kv_full[u % kKvStages], (u / kKvStages) & 1, nullptr, p.err, 0x33);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + BN};
+            const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + DV};
+            const uint32_t aq[2] = {smem_u32(q1s), smem_u32(q2s)};
+            const uint32_t ap[2] = {smem_u32(ps), smem_u32(ps + C::kPBytes)};
+            const uint32_t ast = smem_u32(stages);
+            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, 0x34) &&
+                      mbar_wait(&bars->kv_full[0], 0, abort_flag, p.err, 0x35);
+            if (ok) {
+                tc_fence_after();
+                issue_qk<D>(tS[0], aq[0], ast);
+                umma_commit(&bars->s_full[0]);
+                issue_qk<D>(tS[1], aq[1], ast + C::kKBytes);
+                umma_commit(&bars->s_full[1]);
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int s = j % kKvStages;
+                const uint32_t st = ast + s * C::kStageBytes;
+                const bool more = j + 1 < nkv;
+                const int s1 = (j + 1) % kKvStages;
+                const uint32_t st1 = ast + s1 * C::kStageBytes;
+                // map 1: PV1(j), then S1(j+1)
+                if (!mbar_wait(&bars->p_full[0], j & 1, abort_flag, p.err, 0x36)) break;
+                tc_fence_after();
+                issue_pv<DV>(tO[0], ap[0], st + 2 * C::kKBytes, j > 0);
+                umma_commit(&bars->o_done[0]);
+                if (more) {
+                    if (!mbar_wait(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x37)) break;
+                    tc_fence_after();
+                    issue_qk<D>(tS[0], aq[0], st1);
+                    umma_commit(&bars->s_full[0]);
+                }
+                // map 2: PV2(j), release the stage, then S2(j+1)
+                if (!mbar_wait(&bars->p_full[1], j & 1, abort_flag, p.err, 0x38)) break;
+                tc_fence_after();
+                issue_pv<DV>(tO[1], ap[1], st + 2 * C::kKBytes, j > 0);
+                umma_commit(&bars->o_done[1]);
+                umma_commit(&bars->kv_empty[s]);
+                if (more) {
+                    issue_qk<D>(tS[1], aq[1], st1 + C::kKBytes);
+                    umma_commit(&bars->s_full[1]);
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax (map g)
+        const int g = (warp - 4) >> 2;
+        const int lg = warp & 3;
+        const int r = lg * 32 + lane;  // query row within the tile == TMEM lane
+        const int qrow = q0 + r;
+        const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
+        const uint32_t tS = lane_base + C::kColS + g * BN;
+        const uint32_t tO = lane_base + C::kColO + g * DV;
+        uint8_t* prow = ps + g * C::kPBytes + r * 128;
+        const float sl2 = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+
+        for (int j = 0; j < nkv; ++j) {
+            if (!mbar_wait_warp(&bars->s_full[g], j & 1, abort_flag, p.err, 0x40 + g)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
+            tmem_ld_wait();
+
+            const int kbase = j * BN;
+            const bool need_mask = (p.causal && kbase + BN - 1 > q0) || (kbase + BN > p.N);
+            if (need_mask) {
+                const int lim = p.causal ? min(qrow + 1, p.N) : p.N;  // visible keys: kbase + i < lim
+#pragma unroll
+                for (int i = 0; i < BN; ++i)
+                    if (kbase + i >= lim) sr[i] = __float_as_uint(-INFINITY);
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < BN; i += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(sr[i]));
+                mx1 = fmaxf(mx1, __uint_as_float(sr[i + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(sr[i + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(sr[i + 3]));
+            }
+            const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            float alpha = 1.f;
+            bool rescale = false;
+            if (j == 0) {
+                m_used = m_new;
+            } else if (m_new > m_used + kRescaleThreshold) {
+                alpha = fast_exp2(m_used - m_new);
+                m_used = m_new;
+                rescale = true;
+            }
+            // P = exp2(S * scale - max), row sum in fp32.
+            float rs0 = 0.f, rs1 = 0.f;
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int i = 0; i < BN; i += 2) {
+                const float e0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sl2, -m_used));
+                const float e1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sl2, -m_used));
+                rs0 += e0;
+                rs1 += e1;
+                pk[i / 2] = pack_bf16x2(e0, e1);
+            }
+            l = l * alpha + (rs0 + rs1);
+
+            if (j > 0) {
+                // PV(j-1) must be finished: it reads this group's P buffer and writes O.
+                if (!mbar_wait_warp(&bars->o_done[g], (j - 1) & 1, abort_flag, p.err, 0x42 + g)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                    for (int c = 0; c < DV / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + c * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            // P row -> shared memory, K-major with the 128-byte swizzle the MMA expects:
+            // keys [64a, 64a+64) form box a; 16-byte chunk c of row r sits at c ^ (r % 8).
+#pragma unroll
+            for (int c = 0; c < BN / 8; ++c) {
+                const int a = c >> 3, cc = c & 7;
+                uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                *reinterpret_cast<uint4*>(prow + a * (BM * 128) + ((cc ^ (r & 7)) << 4)) = v;
+            }
+            fence_proxy_async_shared();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[g]);
+        }
+
+        // ------------------------------------------------------------ epilogue
+        if (ok && nkv > 0) {
+            ok = mbar_wait_warp(&bars->o_done[0], (nkv - 1) & 1, abort_flag, p.err, 0x44) &&
+                 mbar_wait_warp(&bars->o_done[1], (nkv - 1) & 1, abort_flag, p.err, 0x45);
+        }
+        tc_fence_after();
+        named_bar_sync(1, 256);  // both groups past their last PV: the P tiles are free
+        epi[g * BM + r] = (g == 0) ? 1.0f / l : p.lambda / l;
+        named_bar_sync(1, 256);
+        const float inv1 = epi[r], inv2 = epi[BM + r];
+        constexpr int kHalf = DV / 2;  // columns handled by this group
+        float oh[kHalf];
+        float ss = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int c = 0; c < kHalf / 32; ++c) {
+                uint32_t o1[32], o2[32];
+                tmem_ld32(lane_base + C::kColO + g * kHalf + c * 32, o1);
+                tmem_ld32(lane_base + C::kColO + DV + g * kHalf + c * 32, o2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float x = __uint_as_float(o1[i]) * inv1 - __uint_as_float(o2[i]) * inv2;
+                    oh[c * 32 + i] = x;
+                    ss = fmaf(x, x, ss);
+                }
+            }
+        }
+        epi[(2 + g) * BM + r] = ss;
+        named_bar_sync(1, 256);
+        if (ok && !*abort_flag && qrow < p.N) {
+            const float tot = epi[2 * BM + r] + epi[3 * BM + r];
+            const float rsc = (1.0f - p.lambda_init) / sqrtf(tot / (float)DV + p.eps);
+            const int64_t obase = (((int64_t)b * p.N + qrow) * p.H + h) * DV + g * kHalf;
+            const float* w = p.norm_w ? p.norm_w + g * kHalf : nullptr;
+            if (p.out_bf16) {
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + obase;
+#pragma unroll
+                for (int i = 0; i < kHalf; i += 8) {
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = oh[i + e] * rsc * (w ? w[i + e] : 1.f);
+                    *reinterpret_cast<uint4*>(dst + i) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                                    pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                }
+            } else {
+                float* dst = reinterpret_cast<float*>(p.out) + obase;
+#pragma unroll
+                for (int i = 0; i < kHalf; i += 4) {
+                    float4 y;
+                    y.x = oh[i] * rsc * (w ? w[i] : 1.f);
+                    y.y = oh[i + 1] * rsc * (w ? w[i + 1] : 1.f);
+                    y.z = oh[i + 2] * rsc * (w ? w[i + 2] : 1.f);
+                    y.w = oh[i + 3] * rsc * (w ? w[i + 3] : 1.f);
+                    *reinterpret_cast<float4*>(dst + i) = y;
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    // Every MMA issued (also before an abort) must finish before TMEM is freed.
+    if (warp == 1 && lane == 0) {
+        umma_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, nullptr, p.err, 0x39);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, int DV>
+cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
+    using C = FwdCfg<D, DV>;
+    auto k = fwd_bf16_kernel<D, DV>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    const int n_tiles = (p.N + BM - 1) / BM;
+    k<<<n_tiles * p.B * p.H, kThreads, C::kSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream) {
+    if (p.d == 64 && p.Dv == 128) return launch_t<64, 128>(p, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace da

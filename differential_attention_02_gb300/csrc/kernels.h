@@ -1,0 +1,75 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the kernels.
+// Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace da {
+
+// fp32 SIMT prefill (any d <= 128 multiple of 4, Dv <= 256 multiple of 32).
+struct SimtF32Params {
+    const float* q1;
+    const float* q2;
+    const float* k1;
+    const float* k2;
+    const float* v;
+    int64_t sq1[3], sq2[3], sk1[3], sk2[3], sv[3];  // b, h, n strides in elements
+    void* out;                                      // [B, N, H, Dv]
+    int out_bf16;
+    const float* norm_w;  // [Dv] or null
+    int B, H, N, d, Dv, causal;
+    float lambda, lambda_init, eps;
+};
+cudaError_t launch_fwd_simt_f32(const SimtF32Params& p, cudaStream_t stream);
+
+// bf16 split-KV decode (+ merge).
+struct DecodeParams {
+    CUtensorMap tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H, L, width]
+    const void* q1;                  // [B, H, d] bf16
+    const void* q2;
+    const int32_t* seq_lens;  // [B] or null
+    int L;
+    void* out;  // [B, H, Dv]
+    int out_bf16;
+    const float* norm_w;
+    int B, H, d, Dv, num_splits, keys_per_split;
+    float lambda, lambda_init, eps;
+    float* part_stats;  // [B*H*S][4]
+    float* part_o;      // [B*H*S][2][Dv]
+    int32_t* err;
+};
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream);
+int decode_keys_per_stage(int d);
+
+// bf16 GEMM on tcgen05: C = A * W.
+struct GemmParams {
+    CUtensorMap tm_a;  // [M, K] K-major, box {64, 128}, 128B swizzle
+    CUtensorMap tm_w;  // [K, N] N-major, box {64, 64}, 128B swizzle
+    void* C;
+    int64_t ldc;
+    int M, N, K, out_bf16;
+    int32_t* err;
+};
+cudaError_t launch_gemm_bf16(const GemmParams& p, cudaStream_t stream);
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+constexpr int kGemmBK = 64;
+
+// bf16 fused prefill on tcgen05.
+struct FwdParams {
+    CUtensorMap tm_q1, tm_q2, tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H, N, width]
+    void* out;                                     // [B, N, H, Dv]
+    int out_bf16;
+    const float* norm_w;
+    int B, H, N, d, Dv, causal;
+    float lambda, lambda_init, eps;
+    float scale_log2;  // log2(e) / sqrt(d)
+    int32_t* err;
+};
+cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);
+constexpr int kFwdBM = 128;
+constexpr int kFwdBN = 128;
+
+}  // namespace da

@@ -1,0 +1,191 @@
+/*
+ * diffattn.h — C ABI of libdiffattn.so: causal multi-head differential
+ * attention on one GB300 (sm_103a).
+ *
+ * The operation, as the source pages define it:
+ *
+ *   DiffAttn(X) = (softmax(Q1 K1^T / sqrt(d)) - lambda * softmax(Q2 K2^T / sqrt(d))) V
+ *   lambda      = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init
+ *   lambda_init = 0.8 - 0.6 * exp(-0.3 * (l - 1))          (l = 1-based layer index)
+ *   y_head      = RMSNorm(DiffAttn_head) * (1 - lambda_init)
+ *
+ * "Differential Transformer: Transformer que cancela ruído de atenção"
+ * (pt.news.hada.io), sections "Como a atenção diferencial funciona" and
+ * "Estrutura multi-head e arquitetura completa"; the causal mask (M_ij = 0 for
+ * i >= j, -inf for i < j) from "A Simple Principle From Noise-Cancelling
+ * Headphones Supercharges Transformers Like Never Before" (intoai.pub),
+ * section "A Deeper Dive Into Attention Calculations".
+ *
+ * Conventions for every entry point:
+ *  - The caller owns every buffer; the library allocates no device memory and
+ *    never synchronises, except diffattn_read_error (documented there).
+ *  - All pointers are device pointers unless stated otherwise. Work is
+ *    enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *  - Every call returns a diffattn_status; nothing throws across the ABI.
+ *    Shapes, dtypes, alignment and strides are checked on the host before any
+ *    launch (DIFFATTN_ERR_INVALID_ARG); shape families without a kernel give
+ *    DIFFATTN_ERR_UNSUPPORTED; a failed launch gives DIFFATTN_ERR_CUDA.
+ *  - Kernels never spin without bound. A wait that exceeds its iteration cap
+ *    records a code in the workspace's error word and the kernel returns;
+ *    diffattn_read_error reports it as DIFFATTN_ERR_TIMEOUT.
+ *  - Softmax scale is 1/sqrt(d), d = the width of one query/key half.
+ *  - bf16 means IEEE bfloat16 stored in 2 bytes; f32 means IEEE binary32.
+ */
+#ifndef DIFFATTN_H
+#define DIFFATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DIFFATTN_OK = 0,
+    DIFFATTN_ERR_INVALID_ARG = 1,  /* bad pointer, shape, stride, alignment or dtype */
+    DIFFATTN_ERR_UNSUPPORTED = 2,  /* valid arguments, but no kernel for this (dtype, d, Dv) */
+    DIFFATTN_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than the size query returns */
+    DIFFATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    DIFFATTN_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up (see diffattn_read_error) */
+} diffattn_status;
+
+typedef enum { DIFFATTN_F32 = 0, DIFFATTN_BF16 = 1 } diffattn_dtype;
+
+/* A 4-D [B, H, rows, width] operand whose last dimension is contiguous.
+ * Strides are in ELEMENTS. ptr and every stride times the element size must be
+ * multiples of 16 bytes. */
+typedef struct {
+    const void* ptr;
+    int64_t stride_b;
+    int64_t stride_h;
+    int64_t stride_n;
+} diffattn_tensor;
+
+/* Human-readable name of a status code (static storage). */
+const char* diffattn_status_string(int status);
+
+/*
+ * diffattn_lambda — the lambda reparameterisation, on the host.
+ *   lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init
+ *   lambda_init = 0.8 - 0.6 * exp(-0.3 * (layer - 1))   if lambda_init_override < 0
+ *   lambda_init = lambda_init_override                   otherwise (the constant-0.8 ablation)
+ * Source: "Differential Transformer: Transformer que cancela ruído de atenção",
+ * section "Como a atenção diferencial funciona"; "Tag: Attention Mechanism"
+ * (priorstack.com), section "Cancelling Context Noise Through Attention Map
+ * Subtraction". One lambda serves every head of a layer (section "Estrutura
+ * multi-head e arquitetura completa").
+ *
+ * lq1, lk1, lq2, lk2: HOST pointers to d floats each. layer: 1-based.
+ * Computed in double, returned rounded to float in *lambda_out and
+ * *lambda_init_out (host pointers). INVALID_ARG on NULL pointers, d < 1,
+ * layer < 1 (when the schedule is used) or a non-finite result.
+ */
+diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                                int d, int layer, float lambda_init_override,
+                                float* lambda_out, float* lambda_init_out);
+
+/*
+ * diffattn_fwd — fused causal prefill: both softmax maps, their lambda-weighted
+ * difference times V, the per-head RMSNorm and the (1 - lambda_init) scale.
+ * Source: the DiffAttn formula ("Como a atenção diferencial funciona") and the
+ * per-head normalisation ("Estrutura multi-head e arquitetura completa") of
+ * "Differential Transformer: Transformer que cancela ruído de atenção"; causal
+ * mask from "A Deeper Dive Into Attention Calculations" (intoai.pub page).
+ *
+ * q1, q2, k1, k2: [B, H, N, d]; v: [B, H, N, Dv]; all of dtype in_dtype.
+ *   Query row i sits at position i and, when causal != 0, sees keys 0..i.
+ *   With causal == 0 every row sees all N keys.
+ * out: [B, N, H, Dv] contiguous, dtype out_dtype (tokens outermost, heads
+ *   concatenated on channels: the layout W_O multiplies).
+ * norm_weight: NULL (weight 1) or [Dv] f32, the RMSNorm gain.
+ * y = o / sqrt(mean_Dv(o^2) + eps) * norm_weight * (1 - lambda_init).
+ * Supported: in_dtype f32 with d <= 128 (multiple of 4) and Dv <= 256
+ * (multiple of 32), fp32 arithmetic throughout; in_dtype bf16 with
+ * (d, Dv) = (64, 128) or (128, 256), tcgen05 tensor-core kernels with fp32
+ * accumulation. out_dtype f32 or bf16 for either.
+ * B, H or N equal to 0: nothing to do, returns DIFFATTN_OK.
+ * workspace: at least diffattn_fwd_workspace_size() bytes, 256-byte aligned;
+ *   its first 4 bytes are the device error word, which must be zero before the
+ *   first call (diffattn_read_error re-zeroes it); the rest needs no
+ *   initialisation.
+ */
+diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                             diffattn_tensor v, void* out, const float* norm_weight,
+                             int B, int H, int N, int d, int Dv, int causal,
+                             float lambda, float lambda_init, float eps,
+                             int in_dtype, int out_dtype,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+diffattn_status diffattn_fwd_workspace_size(int B, int H, int N, int d, int Dv, size_t* bytes);
+
+/*
+ * diffattn_decode — one new query token per sequence against its KV cache,
+ * split over the cache length and merged (both softmax states are merged
+ * exactly, then combined, normalised and scaled as in diffattn_fwd).
+ * Source: as diffattn_fwd, applied to the last row of each sequence; the KV
+ * cache read at every decoding step is the cost "Tag: Attention Mechanism"
+ * (priorstack.com), article "Multi-Head Latent Attention: Scaling LLM Serving
+ * Throughput via Low-Rank KV Compression", describes.
+ *
+ * q1, q2: [B, H, d] contiguous bf16 (the new token's two query halves).
+ * k1_cache, k2_cache: [B, H, Lmax, d] bf16; v_cache: [B, H, Lmax, Dv] bf16.
+ * seq_lens: device int32 [B], 1 <= seq_lens[b] <= L, or NULL (every sequence has
+ *   length L). Values are clamped to [0, L] on the device; a length of 0 has
+ *   no keys and yields NaN for that sequence. The query is the last of its sequence's seq_lens[b] tokens (its
+ *   own K/V already appended) and sees cache entries 0..seq_lens[b]-1.
+ * L: the cache capacity used (<= the allocated Lmax; entries beyond are not read).
+ * out: [B, H, Dv] contiguous, out_dtype.
+ * num_splits: 0 = choose automatically; otherwise 1..256 key-range splits.
+ * Supported: bf16 with (d, Dv) = (64, 128) or (128, 256).
+ * workspace: at least diffattn_decode_workspace_size() bytes, 256-byte aligned,
+ *   for the error word (first 4 bytes, zero before the first call, as for
+ *   diffattn_fwd) and the split partial states (no initialisation needed).
+ * B or H equal to 0: returns DIFFATTN_OK without launching.
+ */
+diffattn_status diffattn_decode(const void* q1, const void* q2,
+                                diffattn_tensor k1_cache, diffattn_tensor k2_cache, diffattn_tensor v_cache,
+                                const int32_t* seq_lens, int L,
+                                void* out, const float* norm_weight,
+                                int B, int H, int d, int Dv, float lambda, float lambda_init, float eps,
+                                int num_splits, int out_dtype,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for diffattn_decode with these sizes; num_splits as above. */
+diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int Dv, int num_splits, size_t* bytes);
+
+/*
+ * diffattn_gemm_bf16 — C[M, N] = A[M, K] . W[K, N], bf16 operands, fp32
+ * accumulation, tcgen05 tensor cores. The module's projections: [Q|K|V] = X W
+ * and Y = concat(heads) W_O ("A Simple Principle From Noise-Cancelling
+ * Headphones...", sections "Moving On To The Differential Transformer" and
+ * "Differential Attention With Multiple Heads").
+ * A row-major with leading dimension lda (elements, K contiguous); W row-major
+ * with ldw (N contiguous); C row-major with ldc, dtype out_dtype.
+ * M, N, K >= 1; N a multiple of 8; pointers 16-byte aligned; lda, ldw
+ * multiples of 8; ldc a multiple of 8 (bf16 C) or 4 (f32 C). Ragged M, N and
+ * K tiles are handled (out-of-range operand elements read as zero).
+ * workspace: at least diffattn_gemm_workspace_size() bytes, 256-byte aligned
+ *   (the error word, zero before the first call).
+ */
+diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M, int N, int K,
+                                   int64_t lda, int64_t ldw, int64_t ldc, int out_dtype,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes);
+
+/*
+ * diffattn_read_error — reads and clears the device error word at the start of
+ * a workspace used by an earlier call. Synchronises `stream` (the one place the
+ * library blocks). *device_code (host pointer) receives the raw code: 0 = none;
+ * otherwise (site << 8) | kind, where kind 1 = a bounded wait gave up.
+ * Returns DIFFATTN_ERR_TIMEOUT when the code is non-zero, DIFFATTN_OK when it
+ * is zero, DIFFATTN_ERR_CUDA if the copy fails.
+ */
+diffattn_status diffattn_read_error(void* workspace, void* stream, int32_t* device_code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIFFATTN_H */

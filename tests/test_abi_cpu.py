@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function the header declares, computes lambda on the host like the
+oracle, and rejects bad arguments before launching anything."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import differential_attention_02_gb300 as da
+from differential_attention_02_gb300 import build as dab
+from oracle import diffattn_oracle as orc
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "diffattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dab.build()
+    return da.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(diffattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_library_agree(lib):
+    names = _declared_functions()
+    assert set(names) == set(da.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert da.status_string(da.OK) == "ok"
+    assert "timed out" in da.status_string(da.ERR_TIMEOUT)
+    assert da.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("layer", [1, 2, 6, 12, 24])
+def test_host_lambda_matches_oracle(lib, layer):
+    rng = np.random.default_rng(layer)
+    vs = [rng.normal(size=64).astype(np.float32) * 0.1 for _ in range(4)]
+    lam, lam_init = da.diffattn_lambda(*vs, layer)
+    lam64, lam_init64 = orc.reparam_lambda(*vs, layer)
+    assert lam == pytest.approx(lam64, abs=2e-7, rel=1e-6)
+    assert lam_init == pytest.approx(lam_init64, abs=1e-7)
+    lam, lam_init = da.diffattn_lambda(*vs, layer, lambda_init_override=0.8)
+    assert lam_init == pytest.approx(0.8, abs=1e-7)
+    assert lam == pytest.approx(orc.reparam_lambda(*vs, layer, 0.8)[0], abs=2e-7)
+
+
+def test_lambda_rejects_bad_arguments(lib):
+    z = np.zeros(4, np.float32)
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_lambda(z, z, z, z, 0)
+    assert e.value.status == da.ERR_INVALID_ARG
+    big = np.full(4, 100.0, np.float32)
+    with pytest.raises(da.DiffAttnError):
+        da.diffattn_lambda(big, big, z, z, 1)  # exp overflows
+
+
+def _tensor(ptr=0x10000, sb=4096, sh=1024, sn=64):
+    return da.Tensor4(ptr, sb, sh, sn)
+
+
+def _fwd(lib, **kw):
+    a = dict(q1=_tensor(), q2=_tensor(), k1=_tensor(), k2=_tensor(), v=_tensor(sn=128), out=0x20000, w=None,
+             B=1, H=2, N=16, d=64, Dv=128, causal=1, lam=0.5, lam_init=0.2, eps=1e-5, ind=da.BF16, outd=da.F32,
+             ws=0x40000, wsb=256, stream=None)
+    a.update(kw)
+    return lib.diffattn_fwd(a["q1"], a["q2"], a["k1"], a["k2"], a["v"], a["out"], a["w"], a["B"], a["H"], a["N"],
+                            a["d"], a["Dv"], a["causal"], a["lam"], a["lam_init"], a["eps"], a["ind"], a["outd"],
+                            a["ws"], a["wsb"], a["stream"])
+
+
+def test_fwd_argument_validation(lib):
+    assert _fwd(lib, B=-1) == da.ERR_INVALID_ARG
+    assert _fwd(lib, B=0) == da.OK and _fwd(lib, N=0) == da.OK  # nothing to do
+    assert _fwd(lib, q1=_tensor(ptr=0)) == da.ERR_INVALID_ARG
+    assert _fwd(lib, k2=_tensor(ptr=0x10008)) == da.ERR_INVALID_ARG      # misaligned
+    assert _fwd(lib, v=_tensor(sn=100)) == da.ERR_INVALID_ARG             # row stride < Dv
+    assert _fwd(lib, q1=_tensor(sh=1028)) == da.ERR_INVALID_ARG           # stride not 16-byte multiple
+    assert _fwd(lib, out=0x20004) == da.ERR_INVALID_ARG
+    assert _fwd(lib, ind=7) == da.ERR_INVALID_ARG
+    assert _fwd(lib, lam=float("nan")) == da.ERR_INVALID_ARG
+    assert _fwd(lib, eps=-1.0) == da.ERR_INVALID_ARG
+    assert _fwd(lib, ws=None) == da.ERR_WORKSPACE
+    assert _fwd(lib, wsb=8) == da.ERR_WORKSPACE
+    assert _fwd(lib, ws=0x40010) == da.ERR_WORKSPACE                      # not 256-byte aligned
+    assert _fwd(lib, d=32, Dv=64, q1=_tensor(sn=32), q2=_tensor(sn=32), k1=_tensor(sn=32),
+                k2=_tensor(sn=32), v=_tensor(sn=64)) == da.ERR_UNSUPPORTED  # bf16 needs (64,128)/(128,256)
+    assert _fwd(lib, ind=da.F32, d=130, Dv=128, q1=_tensor(sn=132), q2=_tensor(sn=132), k1=_tensor(sn=132),
+                k2=_tensor(sn=132)) == da.ERR_UNSUPPORTED
+
+
+def test_decode_and_gemm_argument_validation(lib):
+    t = _tensor()
+    vp = ctypes.c_void_p
+    call = lambda **kw: lib.diffattn_decode(
+        vp(kw.get("q1", 0x1000)), vp(0x1000), kw.get("k1", t), t, kw.get("v", _tensor(sn=128)), None,
+        kw.get("L", 64), vp(kw.get("out", 0x2000)), None, kw.get("B", 2), 2, kw.get("d", 64), 128, 0.5, 0.2, 1e-5,
+        kw.get("S", 0), da.F32, vp(kw.get("ws", 0x4000)), kw.get("wsb", 256), None)
+    assert call(B=0) == da.OK
+    assert call(L=0) == da.ERR_INVALID_ARG
+    assert call(q1=0) == da.ERR_INVALID_ARG
+    assert call(S=300) == da.ERR_INVALID_ARG
+    assert call(d=32, k1=_tensor(sn=32)) == da.ERR_UNSUPPORTED
+    assert call(wsb=256) == da.ERR_WORKSPACE  # partial states need more than the control block
+    n = ctypes.c_size_t()
+    assert lib.diffattn_decode_workspace_size(64, 16, 8192, 64, 128, 4, ctypes.byref(n)) == da.OK
+    assert n.value == 256 + 64 * 16 * 4 * 4 * 4 + 64 * 16 * 4 * 2 * 128 * 4
+    g = lambda **kw: lib.diffattn_gemm_bf16(vp(kw.get("A", 0x1000)), vp(0x2000), vp(0x3000), kw.get("M", 128),
+                                           kw.get("N", 256), 64, kw.get("lda", 64), 256, 256, da.BF16,
+                                           vp(0x4000), 256, None)
+    assert g(M=0) == da.ERR_INVALID_ARG
+    assert g(A=0x1008) == da.ERR_INVALID_ARG
+    assert g(lda=60) == da.ERR_INVALID_ARG
+    assert g(N=250) == da.ERR_INVALID_ARG
+
+
+def test_python_binding_refuses_without_library(tmp_path):
+    saved = da._lib
+    da._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            da.load_library(str(tmp_path / "nope.so"))
+    finally:
+        da._lib = saved

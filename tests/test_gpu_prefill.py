@@ -1,0 +1,147 @@
+"""GPU parity of diffattn_fwd against the float64 oracle (fp32 CUDA-core path
+and bf16 tensor-core path), on seeded inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+import differential_attention_02_gb300 as da
+from differential_attention_02_gb300 import inputs as gi
+from oracle import diffattn_oracle as orc
+from parity import assert_bf16_parity, assert_f32_parity
+
+pytestmark = pytest.mark.gpu
+NAMES = ("q1", "q2", "k1", "k2", "v")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from differential_attention_02_gb300 import build
+    build.build()
+    da.load_library()
+
+
+def _lam(w, override=None):
+    lv = gi.lambda_vectors(w)
+    return orc.reparam_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer, override)
+
+
+def _run(t, lam, lam_init, eps=1e-5, **kw):
+    ws = da.workspace(256)
+    out = da.diffattn_fwd(*(t[k].cuda() for k in NAMES), lam, lam_init, eps, ws=ws, **kw)
+    assert da.read_error(ws) == 0
+    return out
+
+
+# ------------------------------------------------------------------ fp32 path
+def test_tiny_fp32_workload_all_elements():
+    w = gi.WORKLOADS["tiny_fp32"]
+    t = gi.prefill_inputs(w)
+    lam, lam_init = _lam(w)
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, w.eps)
+    assert_f32_parity(_run(t, lam, lam_init, w.eps), ref, "tiny fp32")
+
+
+@pytest.mark.parametrize("N,d,Dv,causal", [(1, 32, 64, True), (45, 32, 64, True), (70, 64, 128, False),
+                                           (33, 128, 256, True), (20, 8, 32, True)])
+def test_fp32_shapes(N, d, Dv, causal):
+    w = gi.WORKLOADS["tiny_fp32"]
+    g = torch.Generator().manual_seed(N * 7 + d)
+    t = {k: torch.randn(2, 3, N, Dv if k == "v" else d, generator=g) for k in NAMES}
+    lam, lam_init = 0.37, 0.2
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, 1e-5, causal=causal)
+    assert_f32_parity(_run(t, lam, lam_init, causal=causal), ref, f"fp32 N={N} d={d}")
+
+
+def test_fp32_norm_weight_and_bf16_output():
+    w = gi.WORKLOADS["tiny_fp32"]
+    t = gi.prefill_inputs(w)
+    lam, lam_init = _lam(w)
+    nw = torch.linspace(0.5, 1.5, w.Dv)
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, w.eps, weight=nw.numpy())
+    assert_f32_parity(_run(t, lam, lam_init, w.eps, norm_weight=nw.cuda()), ref, "weight")
+    out = _run(t, lam, lam_init, w.eps, norm_weight=nw.cuda(), out_dtype=torch.bfloat16)
+    d = np.abs(out.float().cpu().numpy() - ref)
+    assert np.all(d <= 2.0 ** -8 * np.abs(ref) + 1e-6)  # bf16 rounding of the result only
+
+
+# ------------------------------------------------------------------ bf16 path
+@pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 2, 127), (1, 2, 128), (2, 1, 129), (1, 3, 300), (2, 2, 512)])
+def test_bf16_prefill_small_and_ragged(B, H, N):
+    w = gi.WORKLOADS["prefill_bf16"]
+    t = gi.prefill_inputs(w, B=B, H=H, N=N)
+    lam, lam_init = _lam(w)
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, w.eps)
+    assert_bf16_parity(_run(t, lam, lam_init, w.eps), ref, f"bf16 B{B} H{H} N{N}")
+
+
+@pytest.mark.parametrize("lam", [0.0, -0.7, 1.0, 2.5])
+def test_bf16_lambda_values(lam):
+    w = gi.WORKLOADS["prefill_bf16"]
+    t = gi.prefill_inputs(w, B=1, H=2, N=256)
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, 0.5, w.eps)
+    assert_bf16_parity(_run(t, lam, 0.5, w.eps), ref, f"lambda {lam}")
+
+
+def test_bf16_non_causal_weight_and_bf16_out():
+    w = gi.WORKLOADS["prefill_bf16"]
+    t = gi.prefill_inputs(w, B=1, H=2, N=200)
+    lam, lam_init = _lam(w)
+    nw = torch.linspace(0.5, 1.5, w.Dv)
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, w.eps, weight=nw.numpy(), causal=False)
+    assert_bf16_parity(_run(t, lam, lam_init, w.eps, norm_weight=nw.cuda(), causal=False), ref, "non-causal")
+    out = _run(t, lam, lam_init, w.eps, norm_weight=nw.cuda(), causal=False, out_dtype=torch.bfloat16)
+    assert_bf16_parity(out, ref, "bf16 out")
+
+
+def test_bf16_strided_views():
+    """Q1/Q2 and K1/K2 as halves of one [B, N, H, 2d] buffer (the module's layout)."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    B, H, N, d = 2, 3, 160, 64
+    g = torch.Generator().manual_seed(5)
+    qk = torch.randn(2, B, N, H, 2 * d, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, N, H, 128, generator=g).to(torch.bfloat16)
+    q4, k4, v4 = qk[0].permute(0, 2, 1, 3), qk[1].permute(0, 2, 1, 3), v.permute(0, 2, 1, 3)
+    t = {"q1": q4[..., :d], "q2": q4[..., d:], "k1": k4[..., :d], "k2": k4[..., d:], "v": v4}
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), 0.6, 0.3, w.eps)
+    dev = {k: x.cuda() for k, x in (("qk", qk), ("v", v))}
+    q4d, k4d = dev["qk"][0].permute(0, 2, 1, 3), dev["qk"][1].permute(0, 2, 1, 3)
+    out = da.diffattn_fwd(q4d[..., :d], q4d[..., d:], k4d[..., :d], k4d[..., d:], dev["v"].permute(0, 2, 1, 3),
+                          0.6, 0.3, w.eps)
+    assert_bf16_parity(out, ref, "strided")
+
+
+def test_bf16_prefill_workload_all_heads():
+    """The B=4, H=16, N=2048 prefill workload, every element."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    t = gi.prefill_inputs(w)
+    lam, lam_init = _lam(w)
+    out = _run(t, lam, lam_init, w.eps)
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, w.eps)
+    assert_bf16_parity(out, ref, "prefill workload")
+    outb = _run(t, lam, lam_init, w.eps, out_dtype=torch.bfloat16)
+    assert_bf16_parity(outb, ref, "prefill workload, bf16 out")
+
+
+def test_bf16_long_prefill_sampled_rows():
+    """The B=1, H=16, N=16384 workload: every head, 40 sampled rows each (incl. first/last)."""
+    w = gi.WORKLOADS["long_prefill_bf16"]
+    t = gi.prefill_inputs(w)
+    lam, lam_init = _lam(w)
+    out = _run(t, lam, lam_init, w.eps)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, w.N - 1], rng.integers(0, w.N, 35)]))
+    ref = np.full(out.shape, np.nan)
+    for h in range(w.H):
+        o = orc.diffattn_head(*(t[k][0, h, rows] if k in ("q1", "q2") else t[k][0, h] for k in NAMES), lam,
+                              positions=rows)
+        ref[0, rows, h, :] = orc.head_rmsnorm_scale(o, lam_init, w.eps)
+    assert_bf16_parity(out, ref, "long prefill")
+
+
+def test_repeat_calls_are_deterministic():
+    w = gi.WORKLOADS["prefill_bf16"]
+    t = gi.prefill_inputs(w, B=1, H=4, N=640)
+    a = _run(t, 0.5, 0.3)
+    b = _run(t, 0.5, 0.3)
+    assert torch.equal(a, b)
