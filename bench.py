@@ -62,51 +62,98 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi SM clock / throttle-reason sampling while the timed region runs."""
+    """Samples the SM clock and clock-event (throttle) reasons while the timed region runs.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads NVML through ctypes every ~1 ms on a background thread (reading only;
+    no GPU setting is changed). Falls back to `nvidia-smi -lms 200` when NVML
+    cannot be loaded.
+    """
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, gpu_index: int):
+        import threading
         self.gpu = gpu_index
+        self.samples = []
+        self.stop = threading.Event()
+        self.thread = None
+        self.max_mhz = None
+        self.nvml = None
         self.proc = None
-        self.path = os.path.join("/tmp", f"diffattn_clocks_{os.getpid()}.csv")
+
+    def _open_nvml(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        getr = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = mx.value
+        return nv, h, getr
+
+    def _loop(self):
+        import ctypes
+        nv, h, getr = self.nvml
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and getr(h, ctypes.byref(rs)) == 0:
+                self.samples.append((mhz.value, rs.value))
+            time.sleep(0.001)
 
     def __enter__(self):
+        import threading
         try:
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            self.nvml = self._open_nvml()
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+        except (OSError, AttributeError):
+            self.nvml = None
+            try:
+                self.path = os.path.join("/tmp", f"diffattn_clocks_{os.getpid()}.csv")
+                self.f = open(self.path, "w")
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+            except OSError:
+                self.proc = None
         return self
 
     def __exit__(self, *a):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             self.proc.wait(timeout=5)
             self.f.close()
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
+        if self.nvml is not None and self.samples:
+            reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+            return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(self.samples), "source": "nvml"}
+        if self.proc is not None:
+            rows = []
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
                 try:
-                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
-                except ValueError:
+                    rows.append((float(parts[0]), float(parts[1]), parts[2:6]))
+                except (ValueError, IndexError):
                     pass
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags) if fl == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            if rows:
+                return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                        "reasons": sorted({names[i] for _, _, f in rows for i, x in enumerate(f) if x == "Active"}),
+                        "samples": len(rows), "source": "nvidia-smi"}
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"], "samples": 0}
 
 
 # ----------------------------------------------------------------------------- reference arm (oracle)
@@ -175,6 +222,69 @@ def prefill_def_flops_unit():
 
 
 # ----------------------------------------------------------------------------- our arm
+def run_e2e(args, da, w, host, lv, out_shape, dev, stream, world):
+    """Same metric through the public API from pinned host buffers: H2D, prefill, D2H per step."""
+    pin = {k: host[k].pin_memory() for k in NAMES}
+    out_host = torch.empty(out_shape, dtype=torch.bfloat16, pin_memory=True)
+    for _ in range(2):
+        da.diffattn_fwd_host(*(pin[k] for k in NAMES), 0.5, 0.3, w.eps, out_dtype=torch.bfloat16,
+                             device=dev, out_host=out_host)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+        da.diffattn_fwd_host(*(pin[k] for k in NAMES), lam, lam_init, w.eps, out_dtype=torch.bfloat16,
+                             device=dev, out_host=out_host)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = sum(pin[k].numel() * pin[k].element_size() for k in NAMES)
+    d2h = out_host.numel() * out_host.element_size()
+    return {"value": world * prefill_def_flops(w) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_decode(args, da, gi, dev, stream, peaks, peak_kind):
+    """Times the split-KV decode (split kernel + merge kernel) on the decode workload."""
+    import dataclasses
+    wd = gi.WORKLOADS[DECODE]
+    if args.decode_batch:
+        wd = dataclasses.replace(wd, B=args.decode_batch)
+    hd = gi.decode_inputs(wd)
+    lvd = gi.lambda_vectors(wd)
+    y = {k: hd[k].to(dev) for k in NAMES}
+    del hd
+    dout = torch.empty((wd.B, wd.H, wd.Dv), dtype=torch.bfloat16, device=dev)
+    dws = da.workspace(da.decode_workspace_bytes(wd.B, wd.H, wd.N, wd.d, wd.Dv), dev)
+    lam, lam_init = da.diffattn_lambda(lvd["lq1"], lvd["lk1"], lvd["lq2"], lvd["lk2"], wd.layer)
+
+    def dstep():
+        da.diffattn_decode(y["q1"], y["q2"], y["k1"], y["k2"], y["v"], lam, lam_init, eps=wd.eps,
+                           out_dtype=torch.bfloat16, out=dout, ws=dws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        dstep()
+    torch.cuda.synchronize()
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        dev_ev[i][0].record(stream)
+        dstep()
+        dev_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert da.read_error(dws) == 0
+    dms = sum(a.elapsed_time(b) for a, b in dev_ev) / args.steps
+    kvb = decode_kv_bytes(wd)
+    gbs = kvb / (dms * 1e-3) / 1e9
+    return {"workload": f"decode {wd.B} seqs x 1 token, H{wd.H}, L{wd.N}, d{wd.d}, Dv{wd.Dv}, layer {wd.layer}",
+            "ms_per_step": dms, "value": gbs, "unit": "GB/s", "kv_bytes_per_step": kvb,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
+                         "frac_of_spec_8tbs": gbs / 8000.0},
+            "gpu_launches_per_step": 2}
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import differential_attention_02_gb300 as da
     from differential_attention_02_gb300 import build as dab
@@ -235,63 +345,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     assert da.read_error(ws) == 0
 
     # -------- end to end from pinned host buffers through the public API
-    pin = {k: host[k].pin_memory() for k in NAMES}
-    out_host = torch.empty(out.shape, dtype=torch.bfloat16, pin_memory=True)
-    for _ in range(2):
-        da.diffattn_fwd_host(*(pin[k] for k in NAMES), 0.5, 0.3, w.eps, out_dtype=torch.bfloat16,
-                             device=dev, out_host=out_host)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
-        da.diffattn_fwd_host(*(pin[k] for k in NAMES), lam, lam_init, w.eps, out_dtype=torch.bfloat16,
-                             device=dev, out_host=out_host)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    h2d = sum(pin[k].numel() * pin[k].element_size() for k in NAMES)
-    d2h = out_host.numel() * out_host.element_size()
-    del x, out, pin, out_host
+    e2e = None
+    if not args.skip_e2e:
+        e2e = run_e2e(args, da, w, host, lv, out.shape, dev, stream, world)
+    del x, out
 
     # -------- decode workload (HBM bound; 4.3 GB of KV cache, larger than L2)
     dec = None
     if not args.skip_decode:
-        wd = gi.WORKLOADS[DECODE]
-        hd = gi.decode_inputs(wd)
-        lvd = gi.lambda_vectors(wd)
-        y = {k: hd[k].to(dev) for k in NAMES}
-        del hd
-        dout = torch.empty((wd.B, wd.H, wd.Dv), dtype=torch.bfloat16, device=dev)
-        dws = da.workspace(da.decode_workspace_bytes(wd.B, wd.H, wd.N, wd.d, wd.Dv), dev)
-        lam, lam_init = da.diffattn_lambda(lvd["lq1"], lvd["lk1"], lvd["lq2"], lvd["lk2"], wd.layer)
-
-        def dstep():
-            da.diffattn_decode(y["q1"], y["q2"], y["k1"], y["k2"], y["v"], lam, lam_init, eps=wd.eps,
-                               out_dtype=torch.bfloat16, out=dout, ws=dws, stream=stream)
-
-        for _ in range(max(3, args.warmup)):
-            dstep()
-        torch.cuda.synchronize()
-        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
-        for i in range(args.steps):
-            dev_ev[i][0].record(stream)
-            dstep()
-            dev_ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        assert da.read_error(dws) == 0
-        dms = sum(a.elapsed_time(b) for a, b in dev_ev) / args.steps
-        kvb = decode_kv_bytes(wd)
-        gbs = kvb / (dms * 1e-3) / 1e9
-        dec = {"workload": "decode 64 seqs x 1 token, H16, L8192, d64, Dv128, layer 3", "ms_per_step": dms,
-               "value": gbs, "unit": "GB/s", "kv_bytes_per_step": kvb,
-               "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
-                            "frac_of_spec_8tbs": gbs / 8000.0},
-               "gpu_launches_per_step": 2}
-        del y
-
+        dec = run_decode(args, da, gi, dev, stream, peaks, peak_kind)
     if rank != 0:
         return
     cpu = None
@@ -313,8 +375,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None, "peak_kind": f"{peak_kind} bf16 burst"},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "decode": dec,
         "clocks": clocks,
         "gpu_launches": args.steps,
@@ -330,6 +391,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--decode-batch", type=int, default=0, help="override the decode workload's batch (profiling)")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
