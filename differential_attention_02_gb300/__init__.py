@@ -21,7 +21,7 @@ F32, BF16 = 0, 1
 
 EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_workspace_size",
             "diffattn_decode", "diffattn_decode_workspace_size", "diffattn_gemm_bf16",
-            "diffattn_gemm_workspace_size", "diffattn_read_error")
+            "diffattn_gemm_workspace_size", "diffattn_read_error", "diffattn_decode_noalloc")
 
 
 class DiffAttnError(RuntimeError):
@@ -67,6 +67,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i64, i32, vp, sz, vp]
     lib.diffattn_gemm_workspace_size.restype = i32
     lib.diffattn_gemm_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+    lib.diffattn_decode_noalloc.restype = i32
+    lib.diffattn_decode_noalloc.argtypes = [vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, vp, vp, i32, i32, i32, i32,
+                                            f32, f32, f32, i32, i32, vp]
     lib.diffattn_read_error.restype = i32
     lib.diffattn_read_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     _lib = lib

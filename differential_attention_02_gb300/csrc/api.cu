@@ -269,6 +269,50 @@ diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor 
     return cuda_status(launch_decode_bf16(p, static_cast<cudaStream_t>(stream)));
 }
 
+// ---------------------------------------------------------------- decode without caller workspace
+// Scratch for diffattn_decode_noalloc: error word, then the split partial
+// states, exactly as in a diffattn_decode workspace. Host code must not use the
+// symbol as an address; it looks the device address up per device.
+static __device__ __align__(256) uint8_t g_decode_scratch[DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device (looked up once per device).
+void* decode_scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) return nullptr;
+        g_scratch_addr[dev] = ptr;
+    }
+    return g_scratch_addr[dev];
+}
+}  // namespace
+
+diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2, diffattn_tensor k1_cache,
+                                        diffattn_tensor k2_cache, diffattn_tensor v_cache, const int32_t* seq_lens,
+                                        int L, void* out, const float* norm_weight, int B, int H, int d, int Dv,
+                                        float lambda, float lambda_init, float eps, int num_splits, int out_dtype,
+                                        void* stream) {
+    size_t need = 0;
+    const diffattn_status st = diffattn_decode_workspace_size(B, H, L, d, Dv, num_splits, &need);
+    if (st != DIFFATTN_OK) return st;
+    if (B == 0 || H == 0) return DIFFATTN_OK;
+    if (need > sizeof(g_decode_scratch)) return DIFFATTN_ERR_WORKSPACE;
+    void* scratch = decode_scratch_address();
+    if (scratch == nullptr) return DIFFATTN_ERR_CUDA;
+    // The error word must start at zero; the partial states are fully rewritten by the split kernel.
+    if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    return diffattn_decode(q1, q2, k1_cache, k2_cache, v_cache, seq_lens, L, out, norm_weight, B, H, d, Dv, lambda,
+                           lambda_init, eps, num_splits, out_dtype, scratch, sizeof(g_decode_scratch), stream);
+}
+
 diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes) {
     if (!bytes || M < 0 || N < 0 || K < 0) return DIFFATTN_ERR_INVALID_ARG;
     *bytes = kControlBytes;

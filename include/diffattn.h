@@ -155,6 +155,40 @@ diffattn_status diffattn_decode(const void* q1, const void* q2,
 diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int Dv, int num_splits, size_t* bytes);
 
 /*
+ * diffattn_decode_noalloc — diffattn_decode for callers that cannot allocate
+ * device memory: the same kernels and results, but the split partial states
+ * and the error word live in a scratch array inside the library instead of a
+ * caller-provided workspace. The pages have no counterpart to this entry
+ * point; it exists for hosts such as plugin or embedded runtimes that hand the
+ * code pre-allocated inputs and outputs but forbid cudaMalloc (and therefore
+ * cannot supply a workspace).
+ *
+ * Arguments are those of diffattn_decode without workspace/workspace_bytes.
+ * Scratch: a file-scope device array of DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES
+ * (8 MiB) that every GPU loading the library holds until process exit. Calls
+ * whose partial states need more (diffattn_decode_workspace_size() for the same
+ * arguments larger than the limit) are rejected with DIFFATTN_ERR_WORKSPACE
+ * before anything is launched.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current), so make that first call
+ * before any stream capture. No call allocates or frees device memory.
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents; the error word is cleared (cudaMemsetAsync on `stream`) at
+ * the start of each call. Calls that overlap on the GPU (different streams
+ * without ordering) race on the array and give undefined results. A device-side
+ * wait that gives up is recorded only in that private error word, which
+ * diffattn_read_error cannot reach; use diffattn_decode when that report is
+ * needed.
+ */
+#define DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2,
+                                        diffattn_tensor k1_cache, diffattn_tensor k2_cache, diffattn_tensor v_cache,
+                                        const int32_t* seq_lens, int L,
+                                        void* out, const float* norm_weight,
+                                        int B, int H, int d, int Dv, float lambda, float lambda_init, float eps,
+                                        int num_splits, int out_dtype, void* stream);
+
+/*
  * diffattn_gemm_bf16 — C[M, N] = A[M, K] . W[K, N], bf16 operands, fp32
  * accumulation, tcgen05 tensor cores. The module's projections: [Q|K|V] = X W
  * and Y = concat(heads) W_O ("A Simple Principle From Noise-Cancelling
