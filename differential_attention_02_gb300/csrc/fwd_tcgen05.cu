@@ -15,21 +15,26 @@
 // can be reused is prior art only; nothing of it is followed here.)
 //
 // CTA = one 128-row query tile of one (b, h); 12 warps:
-//   warp 0       TMA producer: Q1, Q2 once, then a 2-stage ring of (K1, K2, V)
+//   warp 0       TMA producer: Q1, Q2 once, then a 3-stage ring of (K1, K2, V)
 //                tiles of 128 keys, all 128-byte swizzled.
 //   warp 1       allocates 512 TMEM columns; one lane issues every MMA:
 //                S1 = Q1 K1^T, S2 = Q2 K2^T (fp32 in TMEM), O1 += P1 V,
-//                O2 += P2 V (P from shared memory, fp32 O in TMEM).
+//                O2 += P2 V (P read from TMEM, V from shared memory, fp32 O
+//                in TMEM).
 //   warps 4..7   softmax of map 1; warps 8..11 softmax of map 2. Thread r of a
 //                group owns query row r (TMEM lane r): it reads its S row,
-//                updates max and sum, writes its P row as bf16 into shared
-//                memory, and rescales its O row in TMEM only when the running
-//                max grew by more than 2^8 (the stale max is exact because
-//                the final division uses the same max).
+//                updates max and sum, writes its P row as bf16 back into the
+//                first half of its S columns, and rescales its O row in TMEM
+//                only when the running max grew by more than 2^8 (the stale
+//                max is exact because the final division uses the same max).
+// Keeping P in TMEM halves the shared-memory traffic of the PV products (only
+// V is read from shared memory), which otherwise bounds the tensor pipe.
 //   epilogue     both softmax groups: O1/l1 - lambda O2/l2, row RMSNorm,
 //                (1 - lambda_init), norm weight, store.
-// The MMA order S1(j+1), PV2(j), S2(j+1), PV1(j+1) lets one group's softmax
-// run while the tensor core works for the other map.
+// The MMA order PV1(j), S1(j+1), PV2(j), S2(j+1) lets one group's softmax run
+// while the tensor core works for the other map. S_m(j+1) overwrites the TMEM
+// columns PV_m(j) reads P from; tcgen05.mma operations issued by one thread
+// execute in issue order, so the read completes before the overwrite.
 #include <math.h>
 
 #include "common.cuh"
@@ -40,7 +45,7 @@ namespace {
 
 constexpr int BM = kFwdBM, BN = kFwdBN;
 constexpr int kThreads = 12 * 32;
-constexpr int kKvStages = 2;
+constexpr int kKvStages = 3;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D, int DV>
@@ -50,20 +55,19 @@ struct FwdCfg {
     static constexpr int kVBytes = BN * DV * 2;
     static constexpr int kBoxBytes = 128 * 128;      // one [128 rows][64 bf16] box
     static constexpr int kStageBytes = 2 * kKBytes + kVBytes;
-    static constexpr int kPBytes = BM * BN * 2;      // one P tile (bf16)
     static constexpr int kOffQ1 = 0;
     static constexpr int kOffQ2 = kQBytes;
     static constexpr int kOffStages = 2 * kQBytes;
-    static constexpr int kOffP = kOffStages + kKvStages * kStageBytes;
-    static constexpr int kOffBar = kOffP + 2 * kPBytes;
+    static constexpr int kOffBar = kOffStages + kKvStages * kStageBytes;
     static constexpr int kBarBytes = 256;
-    // The epilogue's exchange buffer (4 x 128 floats) reuses the P tiles, which
-    // are idle once the last PV MMAs have completed.
-    static constexpr int kOffEpi = kOffP;
+    // The epilogue's exchange buffer (4 x 128 floats) reuses the Q1 tile, which
+    // is idle once the last MMA has completed.
+    static constexpr int kOffEpi = kOffQ1;
+    static_assert(4 * BM * 4 <= kQBytes, "epilogue buffer fits in the Q1 tile");
     static constexpr size_t kSmem = 1024 + (size_t)kOffBar + kBarBytes;
     static_assert(kSmem <= 232448, "shared memory budget");
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kColS = 0;               // S1 at 0, S2 at BN
+    static constexpr uint32_t kColS = 0;               // S1 at 0, S2 at BN; P_m in the first BN/2 columns of S_m
     static constexpr uint32_t kColO = 2 * BN;          // O1 at 2BN, O2 at 2BN + DV
     static_assert(2 * BN + 2 * DV <= 512, "TMEM budget");
 };
@@ -91,16 +95,16 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr, uint3
     }
 }
 
+// O (+)= P V with P in TMEM: lane r holds row r, 16 keys (bf16 pairs) per 8 columns.
 template <int DV>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_addr, uint32_t v_addr, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate) {
     constexpr uint32_t idesc = idesc_bf16_f32(BM, DV, 0, 1);
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t a = sdesc_sw128(p_addr + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024);
         // V tile: boxes of [BN keys][64 columns]; next 64 columns = next box (leading
         // offset), next 8 keys = +1024 bytes (stride offset); 16 keys = 2048 bytes.
         const uint64_t b = sdesc_sw128(v_addr + kk * 16 * 128, BN * 128, 1024);
-        umma_ss(o_tmem, a, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        umma_ts(o_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -149,7 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     uint8_t* q1s = smem + C::kOffQ1;
     uint8_t* q2s = smem + C::kOffQ2;
     uint8_t* stages = smem + C::kOffStages;
-    uint8_t* ps = smem + C::kOffP;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -193,7 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
             const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + BN};
             const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + DV};
             const uint32_t aq[2] = {smem_u32(q1s), smem_u32(q2s)};
-            const uint32_t ap[2] = {smem_u32(ps), smem_u32(ps + C::kPBytes)};
             const uint32_t ast = smem_u32(stages);
             bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, 0x34) &&
                       mbar_wait(&bars->kv_full[0], 0, abort_flag, p.err, 0x35);
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 // map 1: PV1(j), then S1(j+1)
                 if (!mbar_wait(&bars->p_full[0], j & 1, abort_flag, p.err, 0x36)) break;
                 tc_fence_after();
-                issue_pv<DV>(tO[0], ap[0], st + 2 * C::kKBytes, j > 0);
+                issue_pv<DV>(tO[0], tS[0], st + 2 * C::kKBytes, j > 0);
                 umma_commit(&bars->o_done[0]);
                 if (more) {
                     if (!mbar_wait(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x37)) break;
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 // map 2: PV2(j), release the stage, then S2(j+1)
                 if (!mbar_wait(&bars->p_full[1], j & 1, abort_flag, p.err, 0x38)) break;
                 tc_fence_after();
-                issue_pv<DV>(tO[1], ap[1], st + 2 * C::kKBytes, j > 0);
+                issue_pv<DV>(tO[1], tS[1], st + 2 * C::kKBytes, j > 0);
                 umma_commit(&bars->o_done[1]);
                 umma_commit(&bars->kv_empty[s]);
                 if (more) {
@@ -242,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
         const uint32_t tS = lane_base + C::kColS + g * BN;
         const uint32_t tO = lane_base + C::kColO + g * DV;
-        uint8_t* prow = ps + g * C::kPBytes + r * 128;
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
@@ -268,13 +269,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
             }
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < BN; i += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(sr[i]));
-                mx1 = fmaxf(mx1, __uint_as_float(sr[i + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(sr[i + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(sr[i + 3]));
+            for (int i = 0; i < BN; i += 8) {
+                mx0 = fmax3(mx0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+                mx2 = fmax3(mx2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+                mx3 = fmax3(mx3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
             }
-            const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            const float m_new = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -285,20 +286,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 rescale = true;
             }
             // P = exp2(S * scale - max), row sum in fp32.
-            float rs0 = 0.f, rs1 = 0.f;
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[BN / 2];
 #pragma unroll
             for (int i = 0; i < BN; i += 2) {
                 const float e0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sl2, -m_used));
                 const float e1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sl2, -m_used));
-                rs0 += e0;
-                rs1 += e1;
+                rs[(i >> 1) & 3] += e0 + e1;
                 pk[i / 2] = pack_bf16x2(e0, e1);
             }
-            l = l * alpha + (rs0 + rs1);
+            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
 
             if (j > 0) {
-                // PV(j-1) must be finished: it reads this group's P buffer and writes O.
+                // PV(j-1) must be finished before O is rescaled (it already is once S(j)
+                // has landed, since MMAs complete in issue order).
                 if (!mbar_wait_warp(&bars->o_done[g], (j - 1) & 1, abort_flag, p.err, 0x42 + g)) {
                     ok = false;
                     break;
@@ -317,15 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                     tmem_st_wait();
                 }
             }
-            // P row -> shared memory, K-major with the 128-byte swizzle the MMA expects:
-            // keys [64a, 64a+64) form box a; 16-byte chunk c of row r sits at c ^ (r % 8).
+            // P row (bf16 pairs, lower key in the low half) -> the first BN/2 columns of S.
 #pragma unroll
-            for (int c = 0; c < BN / 8; ++c) {
-                const int a = c >> 3, cc = c & 7;
-                uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                *reinterpret_cast<uint4*>(prow + a * (BM * 128) + ((cc ^ (r & 7)) << 4)) = v;
-            }
-            fence_proxy_async_shared();
+            for (int c = 0; c < BN / 64; ++c) tmem_st32(tS + c * 32, pk + c * 32);
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->p_full[g]);
         }
@@ -336,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                  mbar_wait_warp(&bars->o_done[1], (nkv - 1) & 1, abort_flag, p.err, 0x45);
         }
         tc_fence_after();
-        named_bar_sync(1, 256);  // both groups past their last PV: the P tiles are free
+        named_bar_sync(1, 256);  // both groups past their last PV: the Q1 tile is free
         epi[g * BM + r] = (g == 0) ? 1.0f / l : p.lambda / l;
         named_bar_sync(1, 256);
         const float inv1 = epi[r], inv2 = epi[BM + r];
