@@ -245,6 +245,67 @@ def run_e2e(args, da, w, host, lv, out_shape, dev, stream, world):
             "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def time_device(fn, steps, warmup, stream, flush=None):
+    """Mean CUDA-event time (ms) of fn() over `steps` calls after `warmup` calls;
+    with `flush`, L2 is evicted (untimed) before each timed call."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        if flush is not None:
+            flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
+def run_long_prefill(args, da, gi, dev, stream, peaks, peak_kind):
+    """The B=1, H=16, N=16384 prefill workload (layer 12), bf16 in/out."""
+    w = gi.WORKLOADS["long_prefill_bf16"]
+    x = {k: v.to(dev) for k, v in gi.prefill_inputs(w).items()}
+    lv = gi.lambda_vectors(w)
+    lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+    out = torch.empty((w.B, w.N, w.H, w.Dv), dtype=torch.bfloat16, device=dev)
+    ws = da.workspace(256, dev)
+    fn = lambda: da.diffattn_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam, lam_init, w.eps,
+                                 out_dtype=torch.bfloat16, out=out, ws=ws, stream=stream)
+    ms = time_device(fn, max(3, args.steps // 4), args.warmup, stream)
+    assert da.read_error(ws) == 0
+    tf = prefill_def_flops(w) / (ms * 1e-3) / 1e12
+    return {"workload": "prefill B1 H16 N16384 d64 Dv128 causal, layer 12, bf16 in/out", "ms_per_step": ms,
+            "value": tf, "unit": "TFLOP/s", "exec_tflops": prefill_exec_flops(w) / (ms * 1e-3) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 burst"},
+            "gpu_launches_per_step": 1}
+
+
+def run_module(args, da, gi, dev, stream, peaks, peak_kind):
+    """Multi-head DiffAttn module: X [2,4096,2048] -> three projections, attention
+    (h=8, d=128, Dv=256), W_O; layer 1 (the layer changes only lambda/lambda_init)."""
+    w = gi.WORKLOADS["module_bf16"]
+    t = {k: v.to(dev) for k, v in gi.module_inputs(w).items()}
+    lv = gi.lambda_vectors(w)
+    lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], 1)
+    ws = da.workspace(256, dev)
+    fn = lambda: da.module_fwd(t["x"], t["w_q"], t["w_k"], t["w_v"], t["w_o"], w.H, lam, lam_init, w.eps, ws=ws,
+                               stream=stream)
+    ms = time_device(fn, max(3, args.steps // 4), args.warmup, stream)
+    assert da.read_error(ws) == 0
+    n_pairs = w.N * (w.N + 1) / 2
+    att = w.B * w.H * (4 * n_pairs * w.d + 2 * n_pairs * w.Dv)
+    M = w.B * w.N
+    gemm = 2.0 * M * w.d_model * (2 * w.H * 2 * w.d + w.H * w.Dv) + 2.0 * M * w.H * w.Dv * w.d_model
+    tf = (att + gemm) / (ms * 1e-3) / 1e12
+    return {"workload": "module X[2,4096,2048], h8 d128 Dv256, causal, layer 1; bf16 weights, fp16 Q/K/V",
+            "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "flops_per_step": att + gemm,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 burst"},
+            "gpu_launches_per_step": 5}
+
+
 def run_decode(args, da, gi, dev, stream, peaks, peak_kind):
     """Times the split-KV decode (split kernel + merge kernel) on the decode workload."""
     import dataclasses
@@ -354,6 +415,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dec = None
     if not args.skip_decode:
         dec = run_decode(args, da, gi, dev, stream, peaks, peak_kind)
+    # -------- the other workloads, reported beside the headline
+    extra = {}
+    if not args.skip_extra:
+        extra["long_prefill"] = run_long_prefill(args, da, gi, dev, stream, peaks, peak_kind)
+        extra["module"] = run_module(args, da, gi, dev, stream, peaks, peak_kind)
     if rank != 0:
         return
     cpu = None
@@ -377,6 +443,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "decode": dec,
+        **extra,
         "clocks": clocks,
         "gpu_launches": args.steps,
         "wall_s_timed_region": t_wall,
@@ -392,6 +459,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-extra", action="store_true", help="skip the long-prefill and module lines")
     ap.add_argument("--decode-batch", type=int, default=0, help="override the decode workload's batch (profiling)")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)

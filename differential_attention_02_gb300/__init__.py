@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdiffattn.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 
 EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_workspace_size",
             "diffattn_decode", "diffattn_decode_workspace_size", "diffattn_gemm_bf16",
@@ -95,6 +95,8 @@ def _dtype_code(dt) -> int:
         return F32
     if dt == torch.bfloat16:
         return BF16
+    if dt == torch.float16:
+        return F16
     raise ValueError(f"unsupported dtype {dt}")
 
 
@@ -148,7 +150,7 @@ def diffattn_lambda(lq1, lk1, lq2, lk2, layer: int, lambda_init_override: float 
 
 def diffattn_fwd(q1, q2, k1, k2, v, lam: float, lam_init: float, eps: float = 1e-5, norm_weight=None,
                  causal: bool = True, out_dtype=torch.float32, out=None, ws=None, stream=None) -> torch.Tensor:
-    """Fused prefill. q1,q2,k1,k2: [B,H,N,d]; v: [B,H,N,Dv] (CUDA, fp32 or bf16). Returns [B,N,H,Dv]."""
+    """Fused prefill. q1,q2,k1,k2: [B,H,N,d]; v: [B,H,N,Dv] (CUDA, fp32, bf16 or fp16). Returns [B,N,H,Dv]."""
     B, H, N, d = q1.shape
     Dv = v.shape[-1]
     for t in (q1, q2, k1, k2, v):
@@ -201,7 +203,7 @@ def diffattn_decode(q1, q2, k1_cache, k2_cache, v_cache, lam: float, lam_init: f
 
 
 def gemm_bf16(a: torch.Tensor, w: torch.Tensor, out_dtype=torch.bfloat16, out=None, ws=None, stream=None):
-    """C = a @ w with a [M,K] and w [K,N] bf16 row-major (unit last stride); tcgen05 kernel."""
+    """C = a @ w with a [M,K] and w [K,N] bf16 row-major (unit last stride); C fp32, bf16 or fp16."""
     M, K = a.shape
     K2, N = w.shape
     if K2 != K or a.stride(1) != 1 or w.stride(1) != 1:
@@ -217,28 +219,31 @@ def gemm_bf16(a: torch.Tensor, w: torch.Tensor, out_dtype=torch.bfloat16, out=No
 
 
 def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float, eps: float = 1e-5,
-               norm_weight=None, ws=None, stream=None):
-    """Multi-head differential attention module, bf16: three projection GEMMs, the fused
+               norm_weight=None, ws=None, stream=None, out_dtype=torch.bfloat16):
+    """Multi-head differential attention module: three projection GEMMs, the fused
     attention reading Q/K/V in place through strided views, and the W_O GEMM.
 
-    x [B,N,d_model]; w_q, w_k [d_model, h*2d]; w_v [d_model, h*Dv]; w_o [h*Dv, d_model].
-    Head i uses Q[..., 2di:2di+d] as Q1 and Q[..., 2di+d:2d(i+1)] as Q2 (K likewise).
+    x [B,N,d_model]; w_q, w_k [d_model, h*2d]; w_v [d_model, h*Dv]; w_o [h*Dv, d_model],
+    all bf16. Head i uses Q[..., 2di:2di+d] as Q1 and Q[..., 2di+d:2d(i+1)] as Q2
+    (K likewise). The projections are written in fp16 (bf16 rounding of Q, K and V
+    alone would cost about 3e-3 relative error at the output); the attention output
+    that W_O multiplies is bf16.
     """
     B, N, dm = x.shape
     h = n_heads
     d = w_q.shape[1] // (2 * h)
     Dv = w_v.shape[1] // h
     x2 = x.reshape(B * N, dm)
-    q = gemm_bf16(x2, w_q, ws=ws, stream=stream)
-    k = gemm_bf16(x2, w_k, ws=ws, stream=stream)
-    v = gemm_bf16(x2, w_v, ws=ws, stream=stream)
+    q = gemm_bf16(x2, w_q, out_dtype=torch.float16, ws=ws, stream=stream)
+    k = gemm_bf16(x2, w_k, out_dtype=torch.float16, ws=ws, stream=stream)
+    v = gemm_bf16(x2, w_v, out_dtype=torch.float16, ws=ws, stream=stream)
     # [B*N, h*2d] -> [B, h, N, 2d] views (no copies): strides (N*h*2d, 2d, h*2d, 1)
     q4 = q.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
     k4 = k.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
     v4 = v.view(B, N, h, Dv).permute(0, 2, 1, 3)
     att = diffattn_fwd(q4[..., :d], q4[..., d:], k4[..., :d], k4[..., d:], v4, lam, lam_init, eps, norm_weight,
                        out_dtype=torch.bfloat16, ws=ws, stream=stream)
-    y = gemm_bf16(att.view(B * N, h * Dv), w_o, ws=ws, stream=stream)
+    y = gemm_bf16(att.view(B * N, h * Dv), w_o, out_dtype=out_dtype, ws=ws, stream=stream)
     return y.view(B, N, dm)
 
 

@@ -43,7 +43,7 @@ int device_sm_count() {
 // 4-D bf16 map over a [B, H, rows, width] operand (strides in elements).
 // Size-1 dimensions get a harmless stride, since their stride is never used.
 bool encode_4d(CUtensorMap* m, const diffattn_tensor& t, int width, int rows, int H, int B, int box_w, int box_rows,
-               CUtensorMapSwizzle sw) {
+               CUtensorMapSwizzle sw, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const int64_t sn = t.stride_n, sh = (H > 1) ? t.stride_h : (int64_t)rows * sn,
@@ -52,7 +52,7 @@ bool encode_4d(CUtensorMap* m, const diffattn_tensor& t, int width, int rows, in
     cuuint64_t strides[3] = {(cuuint64_t)(sn * 2), (cuuint64_t)(sh * 2), (cuuint64_t)(sb * 2)};
     cuuint32_t box[4] = {(cuuint32_t)box_w, (cuuint32_t)box_rows, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(t.ptr), dims, strides, box, es,
+    return enc(m, dt, 4, const_cast<void*>(t.ptr), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -161,7 +161,7 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
                              int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype,
                              int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
     if (B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
-    if ((in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16) ||
+    if ((in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16 && in_dtype != DIFFATTN_F16) ||
         (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16))
         return DIFFATTN_ERR_INVALID_ARG;
     if (!isfinite(lambda) || !isfinite(lambda_init) || !(eps >= 0.f) || !isfinite(eps))
@@ -200,14 +200,16 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
         return cuda_status(launch_fwd_simt_f32(p, st));
     }
 
-    if (!(d == 64 && Dv == 128)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!((d == 64 && Dv == 128) || (d == 128 && Dv == 256))) return DIFFATTN_ERR_UNSUPPORTED;
     FwdParams p{};
-    if (!encode_4d(&p.tm_q1, q1, d, N, H, B, 64, kFwdBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_4d(&p.tm_q2, q2, d, N, H, B, 64, kFwdBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_4d(&p.tm_k1, k1, d, N, H, B, 64, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_4d(&p.tm_k2, k2, d, N, H, B, 64, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_4d(&p.tm_v, v, Dv, N, H, B, 64, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B))
+    const CUtensorMapDataType dt =
+        in_dtype == DIFFATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!encode_4d(&p.tm_q1, q1, d, N, H, B, 64, kFwdBM, sw, dt) || !encode_4d(&p.tm_q2, q2, d, N, H, B, 64, kFwdBM, sw, dt) ||
+        !encode_4d(&p.tm_k1, k1, d, N, H, B, 64, kFwdBN, sw, dt) || !encode_4d(&p.tm_k2, k2, d, N, H, B, 64, kFwdBN, sw, dt) ||
+        !encode_4d(&p.tm_v, v, Dv, N, H, B, 64, kFwdBN, sw, dt))
         return DIFFATTN_ERR_INVALID_ARG;
+    p.in_f16 = in_dtype == DIFFATTN_F16;
     p.out = out;
     p.out_bf16 = out_dtype == DIFFATTN_BF16;
     p.norm_w = norm_weight;
@@ -215,7 +217,9 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
     p.err = err_word(workspace);
-    return cuda_status(launch_fwd_bf16(p, st));
+    // (64, 128): both maps share one CTA; (128, 256): the accumulators of both
+    // maps do not fit one CTA's tensor memory, so a CTA pair splits the maps.
+    return cuda_status(d == 64 ? launch_fwd_bf16(p, st) : launch_fwd_pair_bf16(p, st));
 }
 
 diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int Dv, int num_splits, size_t* bytes) {
@@ -323,7 +327,8 @@ diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M,
                                    int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,
                                    void* stream) {
     if (M < 1 || N < 1 || K < 1) return DIFFATTN_ERR_INVALID_ARG;
-    if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16 && out_dtype != DIFFATTN_F16)
+        return DIFFATTN_ERR_INVALID_ARG;
     if (!A || !W || !C || !aligned16(A) || !aligned16(W) || !aligned16(C)) return DIFFATTN_ERR_INVALID_ARG;
     const int cq = out_dtype == DIFFATTN_F32 ? 4 : 8;
     if (lda < K || lda % 8 || ldw < N || ldw % 8 || ldc < N || ldc % cq || N % 8) return DIFFATTN_ERR_INVALID_ARG;
@@ -336,6 +341,7 @@ diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M,
     p.ldc = ldc;
     p.M = M; p.N = N; p.K = K;
     p.out_bf16 = out_dtype == DIFFATTN_BF16;
+    p.out_f16 = out_dtype == DIFFATTN_F16;
     p.err = err_word(workspace);
     return cuda_status(launch_gemm_bf16(p, static_cast<cudaStream_t>(stream)));
 }

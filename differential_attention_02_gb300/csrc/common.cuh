@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -73,6 +74,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` waiting for the
+// phase (it wakes as soon as the phase completes), so waiting threads stop
+// taking issue slots from the warps doing the work on the same sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSleepHintNs = 1000000;  // 1 ms per attempt; the total stays bounded below
+
 // Waits for the phase of `bar` with the given parity to complete.
 // Gives up when *abort becomes non-zero (another role of the CTA failed) or
 // after kWaitTimeoutNs; on a timeout it records `site` in the error word and
@@ -82,8 +100,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
         if (abort != nullptr && *abort) return false;
         if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
             report_error(err, site, kErrWaitTimeout);
@@ -139,13 +157,17 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
-// Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format
-// (1 = bf16), 15 A major (1 = MN-major), 16 B major, [17,23) N/8, [24,29) M/16.
+// Instruction descriptor for kind::f16 with an fp32 accumulator; A and B are
+// both bf16 (ab_f16 = 0) or both fp16 (ab_f16 = 1). Bits: [4,6) D format
+// (1 = f32), [7,10) A format, [10,13) B format (0 = f16, 1 = bf16), 15 A major
+// (1 = MN-major), 16 B major, [17,23) N/8, [24,29) M/16.
+__host__ __device__ constexpr uint32_t idesc_kind_f16(int M, int N, int a_mn_major, int b_mn_major, int ab_f16) {
+    return (1u << 4) | (static_cast<uint32_t>(ab_f16 ? 0 : 1) << 7) | (static_cast<uint32_t>(ab_f16 ? 0 : 1) << 10) |
+           (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
-           (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
+    return idesc_kind_f16(M, N, a_mn_major, b_mn_major, 0);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle. Fields: [0,14) start
@@ -255,6 +277,83 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
 }
 
 // ----------------------------------------------------------------------------
+// Thread-block clusters: rank, distributed shared memory, cluster barrier
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address (shared::cluster window) of the same offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t caddr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(caddr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t caddr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
+}
+// Hardware cluster barrier. It has no bounded form, so it is used only where
+// it depends on nothing but every CTA of the cluster having started (right
+// after barrier initialisation, before any other wait).
+__device__ __forceinline__ void cluster_sync_start() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster_local(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Arrive on the barrier at shared::cluster address `caddr` (another CTA's barrier).
+__device__ __forceinline__ void mbar_arrive_cluster_remote(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded two-CTA rendezvous. `bar` (count 2) receives, per phase, one arrival
+// from this CTA and one from the peer. Each thread's earlier shared-memory
+// writes are released at cluster scope, so after it returns true the peer's
+// writes before its matching call are visible. Returns false (error recorded,
+// *abort raised) if the peer does not arrive within kWaitTimeoutNs.
+__device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t peer, uint32_t phase, volatile int* abort,
+                                          int32_t* err, int32_t site) {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_arrive_cluster_local(bar);
+        mbar_arrive_cluster_remote(mapa_shared(smem_u32(bar), peer));
+    }
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_cluster(bar, phase & 1, kSleepHintNs)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            report_error(err, site, kErrWaitTimeout);
+            if (abort != nullptr) *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// ----------------------------------------------------------------------------
 // Numeric helpers
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t packed) { return __uint_as_float(packed << 16); }
@@ -264,6 +363,19 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) { return __uint_
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Packs two floats as fp16 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// P tile packing for an MMA operand of 16-bit type F16 ? fp16 : bf16.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+    if constexpr (F16) return pack_f16x2(lo, hi);
+    else return pack_bf16x2(lo, hi);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -84,31 +84,32 @@ struct Bars {
     int abort;
 };
 
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_addr, uint32_t k_addr) {
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+// The MMA issuer shares its SM sub-partition with two softmax warps, so each
+// MMA costs as few instructions as possible: descriptors are built once and
+// advanced by adding the (16-byte-unit) start-address offset to the low word.
+template <int D, bool F16>
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc, uint64_t k_desc) {
+    constexpr uint32_t idesc = idesc_kind_f16(BM, BN, 0, 0, F16);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-        umma_ss(s_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
-                kk > 0 ? 1u : 0u);
+        const uint64_t off = (uint64_t)(((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4);
+        umma_ss(s_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
 // O (+)= P V with P in TMEM: lane r holds row r, 16 keys (bf16 pairs) per 8 columns.
-template <int DV>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate) {
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, DV, 0, 1);
+// V tile descriptor: boxes of [BN keys][64 columns]; the next 64 columns are the
+// next box (leading offset), the next 8 keys +1024 bytes (stride offset), so one
+// K=16 step advances 2048 bytes (128 in 16-byte units).
+template <int DV, bool F16>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t accumulate) {
+    constexpr uint32_t idesc = idesc_kind_f16(BM, DV, 0, 1, F16);
+    umma_ts(o_tmem, p_tmem, v_desc, idesc, accumulate);
 #pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk) {
-        // V tile: boxes of [BN keys][64 columns]; next 64 columns = next box (leading
-        // offset), next 8 keys = +1024 bytes (stride offset); 16 keys = 2048 bytes.
-        const uint64_t b = sdesc_sw128(v_addr + kk * 16 * 128, BN * 128, 1024);
-        umma_ts(o_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 1; kk < BN / 16; ++kk) umma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)(kk * 128), idesc, 1u);
 }
 
-template <int D, int DV>
+template <int D, int DV, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D, DV>;
     extern __shared__ uint8_t smem_raw[];
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(&bars->s_full[g], 1);
-            mbar_init(&bars->p_full[g], 128);
+            mbar_init(&bars->p_full[g], 4);  // one arrival per softmax warp
             mbar_init(&bars->o_done[g], 1);
         }
         mbar_init(&bars->drain, 1);
@@ -195,42 +196,46 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         if (lane == 0) {
             const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + BN};
             const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + DV};
-            const uint32_t aq[2] = {smem_u32(q1s), smem_u32(q2s)};
-            const uint32_t ast = smem_u32(stages);
+            const uint64_t dq[2] = {sdesc_sw128(smem_u32(q1s), 16, 1024), sdesc_sw128(smem_u32(q2s), 16, 1024)};
+            // Stage s descriptors = stage-0 descriptors + s * kStageBytes (in 16-byte units).
+            const uint64_t dk0 = sdesc_sw128(smem_u32(stages), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(stages) + 2 * C::kKBytes, BN * 128, 1024);
+            constexpr uint64_t kStageStep = C::kStageBytes >> 4;
+            constexpr uint64_t kK2Step = C::kKBytes >> 4;
             bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, 0x34) &&
                       mbar_wait(&bars->kv_full[0], 0, abort_flag, p.err, 0x35);
             if (ok) {
                 tc_fence_after();
-                issue_qk<D>(tS[0], aq[0], ast);
+                issue_qk<D, F16>(tS[0], dq[0], dk0);
                 umma_commit(&bars->s_full[0]);
-                issue_qk<D>(tS[1], aq[1], ast + C::kKBytes);
+                issue_qk<D, F16>(tS[1], dq[1], dk0 + kK2Step);
                 umma_commit(&bars->s_full[1]);
             }
             for (int j = 0; ok && j < nkv; ++j) {
                 const int s = j % kKvStages;
-                const uint32_t st = ast + s * C::kStageBytes;
+                const uint64_t dv = dv0 + s * kStageStep;
                 const bool more = j + 1 < nkv;
                 const int s1 = (j + 1) % kKvStages;
-                const uint32_t st1 = ast + s1 * C::kStageBytes;
+                const uint64_t dk1 = dk0 + s1 * kStageStep;
                 // map 1: PV1(j), then S1(j+1)
                 if (!mbar_wait(&bars->p_full[0], j & 1, abort_flag, p.err, 0x36)) break;
                 tc_fence_after();
-                issue_pv<DV>(tO[0], tS[0], st + 2 * C::kKBytes, j > 0);
+                issue_pv<DV, F16>(tO[0], tS[0], dv, j > 0 ? 1u : 0u);
                 umma_commit(&bars->o_done[0]);
                 if (more) {
                     if (!mbar_wait(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x37)) break;
                     tc_fence_after();
-                    issue_qk<D>(tS[0], aq[0], st1);
+                    issue_qk<D, F16>(tS[0], dq[0], dk1);
                     umma_commit(&bars->s_full[0]);
                 }
                 // map 2: PV2(j), release the stage, then S2(j+1)
                 if (!mbar_wait(&bars->p_full[1], j & 1, abort_flag, p.err, 0x38)) break;
                 tc_fence_after();
-                issue_pv<DV>(tO[1], tS[1], st + 2 * C::kKBytes, j > 0);
+                issue_pv<DV, F16>(tO[1], tS[1], dv, j > 0 ? 1u : 0u);
                 umma_commit(&bars->o_done[1]);
                 umma_commit(&bars->kv_empty[s]);
                 if (more) {
-                    issue_qk<D>(tS[1], aq[1], st1 + C::kKBytes);
+                    issue_qk<D, F16>(tS[1], dq[1], dk1 + kK2Step);
                     umma_commit(&bars->s_full[1]);
                 }
             }
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 const float e0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sl2, -m_used));
                 const float e1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sl2, -m_used));
                 rs[(i >> 1) & 3] += e0 + e1;
-                pk[i / 2] = pack_bf16x2(e0, e1);
+                pk[i / 2] = pack_p<F16>(e0, e1);
             }
             l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
 
@@ -323,7 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
             for (int c = 0; c < BN / 64; ++c) tmem_st32(tS + c * 32, pk + c * 32);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&bars->p_full[g]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full[g]);
         }
 
         // ------------------------------------------------------------ epilogue
@@ -400,10 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     }
 }
 
-template <int D, int DV>
+template <int D, int DV, bool F16>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D, DV>;
-    auto k = fwd_bf16_kernel<D, DV>;
+    auto k = fwd_bf16_kernel<D, DV, F16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     const int n_tiles = (p.N + BM - 1) / BM;
@@ -414,7 +420,7 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream) {
-    if (p.d == 64 && p.Dv == 128) return launch_t<64, 128>(p, stream);
+    if (p.d == 64 && p.Dv == 128) return p.in_f16 ? launch_t<64, 128, true>(p, stream) : launch_t<64, 128, false>(p, stream);
     return cudaErrorInvalidValue;
 }
 

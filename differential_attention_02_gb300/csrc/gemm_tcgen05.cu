@@ -107,9 +107,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     } else {
         // Epilogue: TMEM -> registers -> global.
         const int lg = warp & 3;  // TMEM lane group this warp may access
-        const bool ok = mbar_wait(acc_full, 0, abort_flag, p.err, 0x26);
+        // tcgen05.ld is warp-collective: the decision to read TMEM is made per warp.
+        bool ok = mbar_wait_warp(acc_full, 0, abort_flag, p.err, 0x26);
         tc_fence_after();
-        if (ok && !*abort_flag) {
+        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+        if (ok) {
             const int row = m0 + lg * 32 + lane;
             const uint32_t t_row = tmem + ((uint32_t)(lg * 32) << 16);
 #pragma unroll 1
@@ -119,7 +121,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                 tmem_ld_wait();
                 const int col = n0 + c0;
                 if (row < p.M && col < p.N) {
-                    if (p.out_bf16) {
+                    if (p.out_f16) {
+                        __half* dst = reinterpret_cast<__half*>(p.C) + (int64_t)row * p.ldc + col;
+                        if (col + 32 <= p.N) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) {
+                                uint4 v;
+                                v.x = pack_f16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+                                v.y = pack_f16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                                v.z = pack_f16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+                                v.w = pack_f16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+                                *reinterpret_cast<uint4*>(dst + j) = v;
+                            }
+                        } else {
+                            for (int j = 0; j < p.N - col; ++j) dst[j] = __float2half_rn(__uint_as_float(r[j]));
+                        }
+                    } else if (p.out_bf16) {
                         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col;
                         if (col + 32 <= p.N) {
 #pragma unroll

@@ -49,7 +49,7 @@ struct GemmParams {
     CUtensorMap tm_w;  // [K, N] N-major, box {64, 64}, 128B swizzle
     void* C;
     int64_t ldc;
-    int M, N, K, out_bf16;
+    int M, N, K, out_bf16, out_f16;  // output bf16, fp16, or fp32 when both are 0
     int32_t* err;
 };
 cudaError_t launch_gemm_bf16(const GemmParams& p, cudaStream_t stream);
@@ -61,14 +61,16 @@ constexpr int kGemmBK = 64;
 struct FwdParams {
     CUtensorMap tm_q1, tm_q2, tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H, N, width]
     void* out;                                     // [B, N, H, Dv]
-    int out_bf16;
+    int out_bf16;                                  // output bf16 (1) or fp32 (0)
+    int in_f16;                                    // operands fp16 (1) or bf16 (0)
     const float* norm_w;
     int B, H, N, d, Dv, causal;
     float lambda, lambda_init, eps;
     float scale_log2;  // log2(e) / sqrt(d)
     int32_t* err;
 };
-cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);       // both maps in one CTA
+cudaError_t launch_fwd_pair_bf16(const FwdParams& p, cudaStream_t stream);  // one map per CTA of a pair
 constexpr int kFwdBM = 128;
 constexpr int kFwdBN = 128;
 

@@ -29,7 +29,8 @@
  *    records a code in the workspace's error word and the kernel returns;
  *    diffattn_read_error reports it as DIFFATTN_ERR_TIMEOUT.
  *  - Softmax scale is 1/sqrt(d), d = the width of one query/key half.
- *  - bf16 means IEEE bfloat16 stored in 2 bytes; f32 means IEEE binary32.
+ *  - bf16 means bfloat16 and f16 IEEE binary16, each stored in 2 bytes; f32
+ *    means IEEE binary32.
  */
 #ifndef DIFFATTN_H
 #define DIFFATTN_H
@@ -50,7 +51,7 @@ typedef enum {
     DIFFATTN_ERR_TIMEOUT = 5       /* a device-side bounded wait gave up (see diffattn_read_error) */
 } diffattn_status;
 
-typedef enum { DIFFATTN_F32 = 0, DIFFATTN_BF16 = 1 } diffattn_dtype;
+typedef enum { DIFFATTN_F32 = 0, DIFFATTN_BF16 = 1, DIFFATTN_F16 = 2 } diffattn_dtype;
 
 /* A 4-D [B, H, rows, width] operand whose last dimension is contiguous.
  * Strides are in ELEMENTS. ptr and every stride times the element size must be
@@ -93,7 +94,8 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
  * "Differential Transformer: Transformer que cancela ruído de atenção"; causal
  * mask from "A Deeper Dive Into Attention Calculations" (intoai.pub page).
  *
- * q1, q2, k1, k2: [B, H, N, d]; v: [B, H, N, Dv]; all of dtype in_dtype.
+ * q1, q2, k1, k2: [B, H, N, d]; v: [B, H, N, Dv]; all of dtype in_dtype
+ *   (f32, bf16 or f16).
  *   Query row i sits at position i and, when causal != 0, sees keys 0..i.
  *   With causal == 0 every row sees all N keys.
  * out: [B, N, H, Dv] contiguous, dtype out_dtype (tokens outermost, heads
@@ -101,9 +103,10 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
  * norm_weight: NULL (weight 1) or [Dv] f32, the RMSNorm gain.
  * y = o / sqrt(mean_Dv(o^2) + eps) * norm_weight * (1 - lambda_init).
  * Supported: in_dtype f32 with d <= 128 (multiple of 4) and Dv <= 256
- * (multiple of 32), fp32 arithmetic throughout; in_dtype bf16 with
+ * (multiple of 32), fp32 arithmetic throughout; in_dtype bf16 or f16 with
  * (d, Dv) = (64, 128) or (128, 256), tcgen05 tensor-core kernels with fp32
- * accumulation. out_dtype f32 or bf16 for either.
+ * accumulation (the probability tile P is rounded to the operand type for the
+ * P.V product). out_dtype f32 or bf16 for every in_dtype.
  * B, H or N equal to 0: nothing to do, returns DIFFATTN_OK.
  * workspace: at least diffattn_fwd_workspace_size() bytes, 256-byte aligned;
  *   its first 4 bytes are the device error word, which must be zero before the
@@ -195,9 +198,10 @@ diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2,
  * Headphones...", sections "Moving On To The Differential Transformer" and
  * "Differential Attention With Multiple Heads").
  * A row-major with leading dimension lda (elements, K contiguous); W row-major
- * with ldw (N contiguous); C row-major with ldc, dtype out_dtype.
+ * with ldw (N contiguous); C row-major with ldc, dtype out_dtype (f32, bf16 or
+ * f16).
  * M, N, K >= 1; N a multiple of 8; pointers 16-byte aligned; lda, ldw
- * multiples of 8; ldc a multiple of 8 (bf16 C) or 4 (f32 C). Ragged M, N and
+ * multiples of 8; ldc a multiple of 8 (bf16/f16 C) or 4 (f32 C). Ragged M, N and
  * K tiles are handled (out-of-range operand elements read as zero).
  * workspace: at least diffattn_gemm_workspace_size() bytes, 256-byte aligned
  *   (the error word, zero before the first call).

@@ -88,6 +88,7 @@ def test_fwd_argument_validation(lib):
     assert _fwd(lib, q1=_tensor(sh=1028)) == da.ERR_INVALID_ARG           # stride not 16-byte multiple
     assert _fwd(lib, out=0x20004) == da.ERR_INVALID_ARG
     assert _fwd(lib, ind=7) == da.ERR_INVALID_ARG
+    assert _fwd(lib, outd=da.F16) == da.ERR_INVALID_ARG  # outputs are f32 or bf16
     assert _fwd(lib, lam=float("nan")) == da.ERR_INVALID_ARG
     assert _fwd(lib, eps=-1.0) == da.ERR_INVALID_ARG
     assert _fwd(lib, ws=None) == da.ERR_WORKSPACE
@@ -95,6 +96,8 @@ def test_fwd_argument_validation(lib):
     assert _fwd(lib, ws=0x40010) == da.ERR_WORKSPACE                      # not 256-byte aligned
     assert _fwd(lib, d=32, Dv=64, q1=_tensor(sn=32), q2=_tensor(sn=32), k1=_tensor(sn=32),
                 k2=_tensor(sn=32), v=_tensor(sn=64)) == da.ERR_UNSUPPORTED  # bf16 needs (64,128)/(128,256)
+    assert _fwd(lib, ind=da.F16, d=32, Dv=64, q1=_tensor(sn=32), q2=_tensor(sn=32), k1=_tensor(sn=32),
+                k2=_tensor(sn=32), v=_tensor(sn=64)) == da.ERR_UNSUPPORTED
     assert _fwd(lib, ind=da.F32, d=130, Dv=128, q1=_tensor(sn=132), q2=_tensor(sn=132), k1=_tensor(sn=132),
                 k2=_tensor(sn=132)) == da.ERR_UNSUPPORTED
 

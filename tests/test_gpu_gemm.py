@@ -30,3 +30,14 @@ def test_gemm_against_float64(M, N, K):
     outb = da.gemm_bf16(a.cuda(), w.cuda(), out_dtype=torch.bfloat16, ws=ws)
     d = np.abs(outb.float().cpu().numpy() - ref)
     assert np.max(d - 2.0 ** -8 * np.abs(ref)) <= 1e-3
+
+
+def test_gemm_f16_output():
+    g = torch.Generator().manual_seed(3)
+    a = torch.randn(300, 512, generator=g).to(torch.bfloat16)
+    w = (torch.randn(512, 384, generator=g) / 512 ** 0.5).to(torch.bfloat16)
+    ref = a.double().numpy() @ w.double().numpy()
+    out = da.gemm_bf16(a.cuda(), w.cuda(), out_dtype=torch.float16)
+    assert out.dtype == torch.float16
+    d = np.abs(out.double().cpu().numpy() - ref)
+    assert np.max(d - 2.0 ** -11 * np.abs(ref)) <= 1e-3

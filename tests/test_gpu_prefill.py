@@ -8,7 +8,7 @@ import torch
 import differential_attention_02_gb300 as da
 from differential_attention_02_gb300 import inputs as gi
 from oracle import diffattn_oracle as orc
-from parity import assert_bf16_parity, assert_f32_parity
+from parity import assert_bf16_out_parity, assert_bf16_parity, assert_f32_parity
 
 pytestmark = pytest.mark.gpu
 NAMES = ("q1", "q2", "k1", "k2", "v")
@@ -91,7 +91,7 @@ def test_bf16_non_causal_weight_and_bf16_out():
     ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, w.eps, weight=nw.numpy(), causal=False)
     assert_bf16_parity(_run(t, lam, lam_init, w.eps, norm_weight=nw.cuda(), causal=False), ref, "non-causal")
     out = _run(t, lam, lam_init, w.eps, norm_weight=nw.cuda(), causal=False, out_dtype=torch.bfloat16)
-    assert_bf16_parity(out, ref, "bf16 out")
+    assert_bf16_out_parity(out, ref, "bf16 out")
 
 
 def test_bf16_strided_views():
@@ -120,7 +120,7 @@ def test_bf16_prefill_workload_all_heads():
     ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, w.eps)
     assert_bf16_parity(out, ref, "prefill workload")
     outb = _run(t, lam, lam_init, w.eps, out_dtype=torch.bfloat16)
-    assert_bf16_parity(outb, ref, "prefill workload, bf16 out")
+    assert_bf16_out_parity(outb, ref, "prefill workload, bf16 out")
 
 
 def test_bf16_long_prefill_sampled_rows():
@@ -145,3 +145,39 @@ def test_repeat_calls_are_deterministic():
     a = _run(t, 0.5, 0.3)
     b = _run(t, 0.5, 0.3)
     assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ wide heads (d=128, Dv=256), CTA-pair kernel
+@pytest.mark.parametrize("B,H,N,causal", [(1, 1, 1, True), (1, 2, 129, True), (2, 1, 256, True), (1, 2, 300, False),
+                                          (1, 1, 640, True)])
+def test_bf16_wide_heads(B, H, N, causal):
+    g = torch.Generator().manual_seed(N + 11)
+    t = {k: torch.randn(B, H, N, 256 if k == "v" else 128, generator=g).to(torch.bfloat16) for k in NAMES}
+    lam, lam_init = 0.63, 0.2
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, 1e-5, causal=causal)
+    assert_bf16_parity(_run(t, lam, lam_init, causal=causal), ref, f"wide B{B} H{H} N{N}")
+
+
+def test_bf16_wide_heads_weight_bf16_out_and_lambda():
+    """The absolute bound is stated for unit gain: with a gain vector it is
+    checked on the output divided by the gain (the error scales with it)."""
+    g = torch.Generator().manual_seed(77)
+    t = {k: torch.randn(1, 3, 200, 256 if k == "v" else 128, generator=g).to(torch.bfloat16) for k in NAMES}
+    nw = torch.linspace(0.5, 1.5, 256)
+    for lam in (-0.5, 0.0, 1.3):
+        ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, 0.4, 1e-5, weight=nw.numpy())
+        out = _run(t, lam, 0.4, norm_weight=nw.cuda())
+        assert_bf16_parity(out / nw.cuda(), ref / nw.numpy(), f"wide lam {lam}")
+        outb = _run(t, lam, 0.4, norm_weight=nw.cuda(), out_dtype=torch.bfloat16)
+        assert_bf16_out_parity(outb.float() / nw.cuda(), ref / nw.numpy(), "wide bf16 out")
+
+
+# ------------------------------------------------------------------ fp16 operands (both kernels)
+@pytest.mark.parametrize("d,Dv,N", [(64, 128, 1), (64, 128, 200), (64, 128, 513), (128, 256, 130), (128, 256, 384)])
+def test_f16_operands(d, Dv, N):
+    g = torch.Generator().manual_seed(d + N)
+    t = {k: torch.randn(2, 2, N, Dv if k == "v" else d, generator=g).to(torch.float16) for k in NAMES}
+    lam, lam_init = 0.55, 0.3
+    ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, 1e-5)
+    assert_bf16_parity(_run(t, lam, lam_init), ref, f"f16 d{d} N{N}")
+    assert_bf16_out_parity(_run(t, lam, lam_init, out_dtype=torch.bfloat16), ref, f"f16 d{d} N{N} bf16 out")
