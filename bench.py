@@ -48,8 +48,32 @@ def prefill_exec_flops(w) -> float:
     return w.B * w.H * (4 * n_pairs * w.d + 4 * n_pairs * w.Dv)
 
 
+def prefill_bytes(w) -> int:
+    """Inputs read once plus the bf16 output written once."""
+    return w.B * w.H * w.N * (4 * w.d + w.Dv) * 2 + w.B * w.N * w.H * w.Dv * 2
+
+
 def decode_kv_bytes(w) -> int:
     return w.B * w.H * w.N * (2 * w.d + w.Dv) * 2
+
+
+CSRC = os.path.join(ROOT, "differential_attention_02_gb300", "csrc")
+
+
+def profiled_traffic(key, files):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/traffic.json,
+    or None when the kernel sources have changed since that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[key]
+        h = hashlib.sha256()
+        for name in files:
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(f.read())
+    except (OSError, KeyError, ValueError):
+        return None
+    return rec["traffic_bytes"] if h.hexdigest()[:16] == rec["source_sha"] else None
 
 
 def load_peaks():
@@ -338,10 +362,12 @@ def run_decode(args, da, gi, dev, stream, peaks, peak_kind):
     dms = sum(a.elapsed_time(b) for a, b in dev_ev) / args.steps
     kvb = decode_kv_bytes(wd)
     gbs = kvb / (dms * 1e-3) / 1e9
+    per_seq = profiled_traffic("decode_split_per_sequence_H16L8192", ["decode_bf16.cu", "common.cuh", "kernels.h"])
+    traffic = per_seq * wd.B if (per_seq is not None and wd.H == 16 and wd.N == 8192) else None
     return {"workload": f"decode {wd.B} seqs x 1 token, H{wd.H}, L{wd.N}, d{wd.d}, Dv{wd.Dv}, layer {wd.layer}",
             "ms_per_step": dms, "value": gbs, "unit": "GB/s", "kv_bytes_per_step": kvb,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_kind": peak_kind,
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "peak_kind": peak_kind,
                          "frac_of_spec_8tbs": gbs / 8000.0},
             "gpu_launches_per_step": 2}
 
@@ -439,7 +465,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "exec_tflops": world * prefill_exec_flops(w) / (ms_step * 1e-3) / 1e12,
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": f"{peak_kind} bf16 burst"},
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} bf16 burst",
+                     "traffic": profiled_traffic("fwd_bf16_prefill_B4H16N2048",
+                                                 ["fwd_tcgen05.cu", "common.cuh", "kernels.h"]),
+                     "algorithmic_bytes": prefill_bytes(w)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "decode": dec,
