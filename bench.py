@@ -76,6 +76,22 @@ def profiled_traffic(key, files):
     return rec["traffic_bytes"] if h.hexdigest()[:16] == rec["source_sha"] else None
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The maximum of x over the ranks of the default process group (x itself
+    without one): the job's step time is its slowest replica's."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job rate: the units all ranks processed divided by the slowest rank's time (per second)."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -421,13 +437,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         t_wall = time.perf_counter() - t_wall
     clocks = clk.summary()
     ms = [a.elapsed_time(b) for a, b in ev]
-    ms_step = sum(ms) / len(ms)
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks(sum(ms) / len(ms), dev)
     flops = prefill_def_flops(w)
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops, ms_step, world) / 1e12
     achieved = flops / (ms_step * 1e-3) / 1e12  # the prefill kernel is the whole step on the GPU
     assert da.read_error(ws) == 0
 

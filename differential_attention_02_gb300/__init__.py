@@ -21,7 +21,8 @@ F32, BF16, F16 = 0, 1, 2
 
 EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_workspace_size",
             "diffattn_decode", "diffattn_decode_workspace_size", "diffattn_gemm_bf16",
-            "diffattn_gemm_workspace_size", "diffattn_read_error", "diffattn_decode_noalloc")
+            "diffattn_gemm_workspace_size", "diffattn_read_error", "diffattn_decode_noalloc",
+            "diffattn_selftest_timeout")
 
 
 class DiffAttnError(RuntimeError):
@@ -70,6 +71,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_decode_noalloc.restype = i32
     lib.diffattn_decode_noalloc.argtypes = [vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, vp, vp, i32, i32, i32, i32,
                                             f32, f32, f32, i32, i32, vp]
+    lib.diffattn_selftest_timeout.restype = i32
+    lib.diffattn_selftest_timeout.argtypes = [vp, sz, vp]
     lib.diffattn_read_error.restype = i32
     lib.diffattn_read_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     _lib = lib

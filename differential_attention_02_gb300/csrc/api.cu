@@ -346,6 +346,12 @@ diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M,
     return cuda_status(launch_gemm_bf16(p, static_cast<cudaStream_t>(stream)));
 }
 
+diffattn_status diffattn_selftest_timeout(void* workspace, size_t workspace_bytes, void* stream) {
+    if (workspace == nullptr || workspace_bytes < kControlBytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DIFFATTN_ERR_WORKSPACE;
+    return cuda_status(launch_selftest_timeout(err_word(workspace), static_cast<cudaStream_t>(stream)));
+}
+
 diffattn_status diffattn_read_error(void* workspace, void* stream, int32_t* device_code) {
     if (!workspace || !device_code) return DIFFATTN_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -22,6 +22,7 @@ constexpr int32_t kErrWaitTimeout = 1;
 // Upper bound for one barrier wait. No legitimate wait in these kernels comes
 // within orders of magnitude of it; reaching it means a lost arrival.
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
+constexpr uint32_t kWaitMaxIters = 1u << 16;         // outer polling rounds of one wait
 
 __device__ __forceinline__ void report_error(int32_t* err, int32_t site, int32_t kind) {
     if (err != nullptr) atomicCAS(err, 0, (site << 8) | kind);
@@ -99,11 +100,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           int32_t site) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    for (uint32_t it = 0;; ++it) {
         for (int i = 0; i < 8; ++i)
             if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
         if (abort != nullptr && *abort) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        // Time bound, with an iteration cap as a backstop should the timer not advance.
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs || it > kWaitMaxIters) {
             report_error(err, site, kErrWaitTimeout);
             if (abort != nullptr) *abort = 1;
             return false;
@@ -343,8 +345,8 @@ __device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t peer, uint32_t
         mbar_arrive_cluster_remote(mapa_shared(smem_u32(bar), peer));
     }
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait_cluster(bar, phase & 1, kSleepHintNs)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    for (uint32_t it = 0; !mbar_try_wait_cluster(bar, phase & 1, kSleepHintNs); ++it) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs || it > 8 * kWaitMaxIters) {
             report_error(err, site, kErrWaitTimeout);
             if (abort != nullptr) *abort = 1;
             return false;

@@ -74,4 +74,7 @@ cudaError_t launch_fwd_pair_bf16(const FwdParams& p, cudaStream_t stream);  // o
 constexpr int kFwdBM = 128;
 constexpr int kFwdBN = 128;
 
+// One CTA whose single wait can never complete (bounded-wait self-test).
+cudaError_t launch_selftest_timeout(int32_t* err, cudaStream_t stream);
+
 }  // namespace da

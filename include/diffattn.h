@@ -222,6 +222,16 @@ diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes)
  */
 diffattn_status diffattn_read_error(void* workspace, void* stream, int32_t* device_code);
 
+/*
+ * diffattn_selftest_timeout — exercises the bounded-wait path every kernel of
+ * the library relies on: launches one CTA whose single barrier wait can never
+ * complete. After about one second the wait gives up, records site 0x7F
+ * (device code 0x7F01) in the workspace error word and the kernel returns; a
+ * later diffattn_read_error on that workspace reports DIFFATTN_ERR_TIMEOUT.
+ * workspace: at least 256 bytes, 256-byte aligned, error word zero.
+ */
+diffattn_status diffattn_selftest_timeout(void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
