@@ -57,6 +57,20 @@ bool encode_4d(CUtensorMap* m, const diffattn_tensor& t, int width, int rows, in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a contiguous output [B, N, W] (W = H * Dv elements per token),
+// boxes of 128 bytes x `box_rows` rows, 128-byte swizzle (for TMA stores).
+bool encode_out_3d(CUtensorMap* m, void* ptr, int W, int N, int B, int elem_bytes, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)N, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)W * elem_bytes, (cuuint64_t)W * elem_bytes * N};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_2d(CUtensorMap* m, const void* ptr, int inner, int outer, int64_t ld, int box_inner, int box_outer) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
@@ -207,7 +221,8 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
     if (!encode_4d(&p.tm_q1, q1, d, N, H, B, 64, kFwdBM, sw, dt) || !encode_4d(&p.tm_q2, q2, d, N, H, B, 64, kFwdBM, sw, dt) ||
         !encode_4d(&p.tm_k1, k1, d, N, H, B, 64, kFwdBN, sw, dt) || !encode_4d(&p.tm_k2, k2, d, N, H, B, 64, kFwdBN, sw, dt) ||
-        !encode_4d(&p.tm_v, v, Dv, N, H, B, 64, kFwdBN, sw, dt))
+        !encode_4d(&p.tm_v, v, Dv, N, H, B, 64, kFwdBN, sw, dt) ||
+        !encode_out_3d(&p.tm_out, out, H * Dv, N, B, out_dtype == DIFFATTN_F32 ? 4 : 2, kFwdBM))
         return DIFFATTN_ERR_INVALID_ARG;
     p.in_f16 = in_dtype == DIFFATTN_F16;
     p.out = out;

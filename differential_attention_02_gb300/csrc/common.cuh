@@ -137,6 +137,29 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// TMA store of a shared-memory box to a 3-D / 2-D tensor (out-of-range rows are
+// clipped by the hardware). The generic-proxy writes that filled the box must
+// be fenced (fence_proxy_async_shared) and synchronised before the issuing
+// thread calls this.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed store of this thread has finished reading shared memory.
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Offset of 16-byte chunk c of row r in a 128-byte-swizzled [rows][128 B] box.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
 // ----------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation MMA
 // ----------------------------------------------------------------------------

@@ -362,33 +362,57 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         }
         epi[(2 + g) * BM + r] = ss;
         named_bar_sync(1, 256);
-        if (ok && !*abort_flag && qrow < p.N) {
+        // Stage this group's DV/2 output columns in shared memory as 128-byte-swizzled
+        // boxes of 128 rows (row-per-thread writes hit distinct banks) and write the
+        // tile with TMA stores, which clip the rows past N. Row-per-thread global
+        // stores would touch one 4 KB-strided row per lane and cost ~3.5K cycles a
+        // tile. The K/V ring is idle after the last PV.
+        uint8_t* stage = smem + C::kOffStages;
+        if (ok) {
             const float tot = epi[2 * BM + r] + epi[3 * BM + r];
             const float rsc = (1.0f - p.lambda_init) / sqrtf(tot / (float)DV + p.eps);
-            const int64_t obase = (((int64_t)b * p.N + qrow) * p.H + h) * DV + g * kHalf;
             const float* w = p.norm_w ? p.norm_w + g * kHalf : nullptr;
             if (p.out_bf16) {
-                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + obase;
 #pragma unroll
-                for (int i = 0; i < kHalf; i += 8) {
-                    float y[8];
+                for (int bx = 0; bx < kHalf / 64; ++bx) {
+                    uint8_t* box = stage + (g * (kHalf / 64) + bx) * (BM * 128);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = oh[i + e] * rsc * (w ? w[i + e] : 1.f);
-                    *reinterpret_cast<uint4*>(dst + i) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                                                    pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                    for (int c = 0; c < 8; ++c) {
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int i = bx * 64 + c * 8 + e;
+                            y[e] = oh[i] * rsc * (w ? w[i] : 1.f);
+                        }
+                        *reinterpret_cast<uint4*>(box + sw128_offset(r, c)) =
+                            make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                       pack_bf16x2(y[6], y[7]));
+                    }
                 }
             } else {
-                float* dst = reinterpret_cast<float*>(p.out) + obase;
 #pragma unroll
-                for (int i = 0; i < kHalf; i += 4) {
-                    float4 y;
-                    y.x = oh[i] * rsc * (w ? w[i] : 1.f);
-                    y.y = oh[i + 1] * rsc * (w ? w[i + 1] : 1.f);
-                    y.z = oh[i + 2] * rsc * (w ? w[i + 2] : 1.f);
-                    y.w = oh[i + 3] * rsc * (w ? w[i + 3] : 1.f);
-                    *reinterpret_cast<float4*>(dst + i) = y;
+                for (int bx = 0; bx < kHalf / 32; ++bx) {
+                    uint8_t* box = stage + (g * (kHalf / 32) + bx) * (BM * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float y[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = bx * 32 + c * 4 + e;
+                            y[e] = oh[i] * rsc * (w ? w[i] : 1.f);
+                        }
+                        *reinterpret_cast<float4*>(box + sw128_offset(r, c)) = make_float4(y[0], y[1], y[2], y[3]);
+                    }
                 }
             }
+        }
+        fence_proxy_async_shared();
+        named_bar_sync(1, 256);
+        if (threadIdx.x == 128 && !*abort_flag) {
+            const int bw = p.out_bf16 ? 64 : 32;  // elements per 128-byte box row
+            for (int i = 0; i < DV / bw; ++i) tma_store_3d(&p.tm_out, stage + i * (BM * 128), h * DV + i * bw, q0, b);
+            tma_store_commit();
+            tma_store_wait_read();
         }
     }
 

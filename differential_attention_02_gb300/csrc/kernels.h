@@ -60,6 +60,7 @@ constexpr int kGemmBK = 64;
 // bf16 fused prefill on tcgen05.
 struct FwdParams {
     CUtensorMap tm_q1, tm_q2, tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H, N, width]
+    CUtensorMap tm_out;                            // 3-D map over the output [B, N, H*Dv], 128-byte boxes
     void* out;                                     // [B, N, H, Dv]
     int out_bf16;                                  // output bf16 (1) or fp32 (0)
     int in_f16;                                    // operands fp16 (1) or bf16 (0)
