@@ -352,6 +352,22 @@ diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M,
     GemmParams p{};
     if (!encode_2d(&p.tm_a, A, K, M, lda, kGemmBK, kGemmBM) || !encode_2d(&p.tm_w, W, N, K, ldw, 64, kGemmBK))
         return DIFFATTN_ERR_INVALID_ARG;
+    {
+        // Output map for the epilogue's TMA stores: 128-byte x 32-row boxes.
+        auto enc = tensor_map_encoder();
+        const int eb = out_dtype == DIFFATTN_F32 ? 4 : 2;
+        const CUtensorMapDataType dt = out_dtype == DIFFATTN_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : out_dtype == DIFFATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+        cuuint64_t strides[1] = {(cuuint64_t)(ldc * eb)};
+        cuuint32_t box[2] = {(cuuint32_t)(128 / eb), 32};
+        cuuint32_t es[2] = {1, 1};
+        if (!enc || enc(&p.tm_c, dt, 2, C, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return DIFFATTN_ERR_INVALID_ARG;
+    }
     p.C = C;
     p.ldc = ldc;
     p.M = M; p.N = N; p.K = K;

@@ -7,11 +7,15 @@
 // (intoai.pub), sections "Moving On To The Differential Transformer" and
 // "Differential Attention With Multiple Heads".
 //
-// One CTA per 128 x 256 output tile. Warp roles: warp 0 = TMA producer (one
-// lane), warp 1 = MMA issuer (one lane) and TMEM owner, warps 2..5 = epilogue
-// (warp w reads TMEM lanes 32*(w%4) .. +31). A is K-major (128-byte swizzled
-// 128 x 64 boxes); W is N-major, so B is given to the MMA as MN-major (four
-// 64 x 64 boxes per stage, 128-byte swizzled).
+// Persistent: one CTA per SM walks the 128 x 256 output tiles (M-block-major,
+// so the CTAs running at once share W and each A row block through L2). Two
+// 256-column TMEM accumulators let the epilogue of one tile overlap the MMAs
+// of the next. Warp roles: warp 0 = TMA producer (one lane; A K-major
+// 128 x 64 boxes, W N-major 64 x 64 boxes, both 128-byte swizzled, 3-stage
+// ring), warp 1 = TMEM owner and MMA issuer (one lane; B given as MN-major),
+// warps 2..5 = epilogue: warp w owns TMEM lanes (tile rows) 32*(w%4)..+31 and
+// writes them through 128-byte-swizzled shared-memory boxes with TMA stores,
+// 128 columns per pass.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -19,153 +23,195 @@ namespace da {
 namespace {
 
 constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;           // 16 KB
-constexpr int kWBoxBytes = BK * 64 * 2;        // 8 KB: 64 K-rows x 64 N-columns
+constexpr int kStages = 3;
+constexpr int kABytes = BM * BK * 2;             // 16 KB
+constexpr int kWBoxBytes = BK * 64 * 2;          // 8 KB: 64 K-rows x 64 N-columns
 constexpr int kWBytes = (BN / 64) * kWBoxBytes;  // 32 KB
 constexpr int kStageBytes = kABytes + kWBytes;
+constexpr int kOutBoxBytes = 32 * 128;           // one [32 rows][128 bytes] output box
+constexpr int kOutWarpBytes = 4 * kOutBoxBytes;  // one epilogue warp's staging: 128 columns of fp32
+constexpr int kOffOut = kStages * kStageBytes;
+constexpr int kOffBar = kOffOut + 4 * kOutWarpBytes;
 constexpr int kThreads = 6 * 32;
-constexpr uint32_t kTmemCols = BN;  // fp32 accumulator, one column per output column
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+constexpr uint32_t kTmemCols = 2 * BN;           // two fp32 accumulators
+constexpr size_t kSmem = 1024 + (size_t)kOffBar + 256;
+static_assert(kSmem <= 232448, "shared memory budget");
+
+struct GemmBars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* acc_full = empty + kStages;
-    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_slot + 1);
+    GemmBars* bars = reinterpret_cast<GemmBars*>(smem + kOffBar);
+    volatile int* abort_flag = &bars->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int tiles_n = (p.N + BN - 1) / BN;
+    const int tiles = ((p.M + BM - 1) / BM) * tiles_n;
     const int kblocks = (p.K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
         }
-        mbar_init(acc_full, 1);
-        *abort_flag = 0;
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->acc_full[b], 1);
+            mbar_init(&bars->acc_empty[b], 4);  // one arrival per epilogue warp
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_base_slot, kTmemCols);
+        tmem_alloc(&bars->tmem_base, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_base_slot;
+    const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
+        // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&p.tm_a);
             tma_prefetch_desc(&p.tm_w);
-            int kb = 0;
-            for (; kb < kblocks; ++kb) {
-                const int s = kb % kStages;
-                if (!mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag, p.err, 0x21)) break;
-                uint8_t* st = smem + s * kStageBytes;
-                mbar_arrive_expect_tx(&full[s], kStageBytes);
-                tma_load_2d(st, &p.tm_a, &full[s], kb * BK, m0);
+            int it = 0;
+            bool go = true;
+            for (int t = blockIdx.x; go && t < tiles; t += gridDim.x) {
+                const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(&bars->empty[s], ((it / kStages) & 1) ^ 1, abort_flag, p.err, 0x21)) {
+                        go = false;
+                        break;
+                    }
+                    uint8_t* st = smem + s * kStageBytes;
+                    mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
+                    tma_load_2d(st, &p.tm_a, &bars->full[s], kb * BK, m0);
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c)
-                    tma_load_2d(st + kABytes + c * kWBoxBytes, &p.tm_w, &full[s], n0 + c * 64, kb * BK);
+                    for (int c = 0; c < BN / 64; ++c)
+                        tma_load_2d(st + kABytes + c * kWBoxBytes, &p.tm_w, &bars->full[s], n0 + c * 64, kb * BK);
+                }
             }
-            for (int u = max(0, kb - kStages); u < kb; ++u)
-                mbar_wait(&full[u % kStages], (u / kStages) & 1, nullptr, p.err, 0x22);
+            // Drain: no copy may still be landing in shared memory when the CTA exits.
+            for (int u = max(0, it - kStages); u < it; ++u)
+                mbar_wait(&bars->full[u % kStages], (u / kStages) & 1, nullptr, p.err, 0x22);
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
-            bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kStages;
-                if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag, p.err, 0x23)) {
-                    ok = false;
-                    break;
-                }
+            // A: K-major, 128-byte rows; one K=16 step is 32 bytes along the row.
+            // B: MN-major; 64-column boxes are kWBoxBytes apart (leading offset),
+            // 8-row K groups 1024 bytes apart (stride offset); K=16 is 16 rows.
+            const uint64_t da0 = sdesc_sw128(smem_u32(smem), 16, 1024);
+            const uint64_t dw0 = sdesc_sw128(smem_u32(smem) + kABytes, kWBoxBytes, 1024);
+            constexpr uint64_t kStep = kStageBytes >> 4;
+            int it = 0, local = 0;
+            bool go = true;
+            for (int t = blockIdx.x; go && t < tiles; t += gridDim.x, ++local) {
+                const int buf = local & 1;
+                // The epilogue must have read this accumulator's previous tile.
+                if (!mbar_wait(&bars->acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 0x23)) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + s * kStageBytes);
-                const uint32_t w_addr = a_addr + kABytes;
+                const uint32_t acc = tmem + buf * BN;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(&bars->full[s], (it / kStages) & 1, abort_flag, p.err, 0x24)) {
+                        go = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    // A: K-major, 128-byte rows; one K=16 step is 32 bytes along the row.
-                    const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
-                    // B: MN-major; 64-column boxes are kWBoxBytes apart (leading offset),
-                    // 8-row K groups are 1024 bytes apart (stride offset); K=16 is 16 rows.
-                    const uint64_t bd = sdesc_sw128(w_addr + k * 16 * 128, kWBoxBytes, 1024);
-                    umma_ss(tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_ss(acc, da0 + s * kStep + (uint64_t)(k * 2), dw0 + s * kStep + (uint64_t)(k * 128), idesc,
+                                (kb > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(&bars->empty[s]);
                 }
-                umma_commit(&empty[s]);
+                if (go) umma_commit(&bars->acc_full[buf]);
             }
-            umma_commit(acc_full);  // also drains the MMAs issued before an abort
-            mbar_wait(acc_full, 0, nullptr, p.err, ok ? 0x24 : 0x25);
+            // Every MMA issued (also before an abort) must finish before TMEM is freed.
+            umma_commit(&bars->drain);
+            mbar_wait(&bars->drain, 0, nullptr, p.err, 0x25);
         }
     } else {
-        // Epilogue: TMEM -> registers -> global.
-        const int lg = warp & 3;  // TMEM lane group this warp may access
-        // tcgen05.ld is warp-collective: the decision to read TMEM is made per warp.
-        bool ok = mbar_wait_warp(acc_full, 0, abort_flag, p.err, 0x26);
-        tc_fence_after();
-        ok = __all_sync(0xffffffffu, ok && !*abort_flag);
-        if (ok) {
-            const int row = m0 + lg * 32 + lane;
-            const uint32_t t_row = tmem + ((uint32_t)(lg * 32) << 16);
+        // ------------------------------------------------------------ epilogue
+        const int lg = warp & 3;  // TMEM lane group (tile rows) this warp may access
+        uint8_t* stage = smem + kOffOut + lg * kOutWarpBytes;
+        const int eb = p.out_bf16 || p.out_f16 ? 2 : 4;
+        const int bw = 128 / eb;  // elements per 128-byte box row
+        int local = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
+            const int buf = local & 1;
+            // tcgen05.ld is warp-collective: the decision to read TMEM is made per warp.
+            bool ok = mbar_wait_warp(&bars->acc_full[buf], (local >> 1) & 1, abort_flag, p.err, 0x26);
+            ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+            const uint32_t t_row = tmem + buf * BN + ((uint32_t)(lg * 32) << 16);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(t_row + c0, r);
-                tmem_ld_wait();
-                const int col = n0 + c0;
-                if (row < p.M && col < p.N) {
-                    if (p.out_f16) {
-                        __half* dst = reinterpret_cast<__half*>(p.C) + (int64_t)row * p.ldc + col;
-                        if (col + 32 <= p.N) {
+            for (int pass = 0; pass < BN / 128; ++pass) {
+                // The staging boxes of this warp must be free (its previous stores read them).
+                if (lane == 0) tma_store_wait_read();
+                __syncwarp();
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_row + pass * 128 + c * 32, r);
+                    tmem_ld_wait();
+                    if (eb == 2) {
+                        // 32 columns = half a box row: box c/2, 16-byte chunks (c%2)*4 .. +3.
+                        uint8_t* box = stage + (c >> 1) * kOutBoxBytes;
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                uint4 v;
-                                v.x = pack_f16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-                                v.y = pack_f16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                                v.z = pack_f16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-                                v.w = pack_f16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-                                *reinterpret_cast<uint4*>(dst + j) = v;
-                            }
-                        } else {
-                            for (int j = 0; j < p.N - col; ++j) dst[j] = __float2half_rn(__uint_as_float(r[j]));
-                        }
-                    } else if (p.out_bf16) {
-                        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col;
-                        if (col + 32 <= p.N) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                uint4 v;
-                                v.x = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-                                v.y = pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                                v.z = pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-                                v.w = pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-                                *reinterpret_cast<uint4*>(dst + j) = v;
-                            }
-                        } else {
-                            for (int j = 0; j < p.N - col; ++j) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                        for (int j = 0; j < 4; ++j) {
+                            const float* f = reinterpret_cast<const float*>(r + 8 * j);
+                            uint4 v;
+                            if (p.out_f16)
+                                v = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                                               pack_f16x2(f[6], f[7]));
+                            else
+                                v = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                               pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                            *reinterpret_cast<uint4*>(box + sw128_offset(lane, (c & 1) * 4 + j)) = v;
                         }
                     } else {
-                        float* dst = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + col;
-                        if (col + 32 <= p.N) {
+                        // 32 fp32 columns = one box row.
+                        uint8_t* box = stage + c * kOutBoxBytes;
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                *reinterpret_cast<float4*>(dst + j) =
-                                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                        } else {
-                            for (int j = 0; j < p.N - col; ++j) dst[j] = __uint_as_float(r[j]);
-                        }
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<uint4*>(box + sw128_offset(lane, j)) =
+                                make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
                     }
+                }
+                if (pass == BN / 128 - 1) {
+                    // Done reading this accumulator: the MMA warp may reuse it.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->acc_empty[buf]);
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    const int nbox = 128 / bw;
+                    for (int i = 0; i < nbox; ++i)
+                        tma_store_2d(&p.tm_c, stage + i * kOutBoxBytes, n0 + pass * 128 + i * bw, m0 + lg * 32);
+                    tma_store_commit();
                 }
             }
         }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -180,8 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
 cudaError_t launch_gemm_bf16(const GemmParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
-    gemm_bf16_kernel<<<grid, kThreads, kSmem, stream>>>(p);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    gemm_bf16_kernel<<<tiles < sms ? tiles : sms, kThreads, kSmem, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -47,6 +47,7 @@ int decode_keys_per_stage(int d);
 struct GemmParams {
     CUtensorMap tm_a;  // [M, K] K-major, box {64, 128}, 128B swizzle
     CUtensorMap tm_w;  // [K, N] N-major, box {64, 64}, 128B swizzle
+    CUtensorMap tm_c;  // [M, N] output, boxes of 128 bytes x 32 rows, 128B swizzle
     void* C;
     int64_t ldc;
     int M, N, K, out_bf16, out_f16;  // output bf16, fp16, or fp32 when both are 0
