@@ -54,6 +54,11 @@ struct PairCfg {
     static constexpr int kOffX = kOffStages;          // exchange buffer reuses the K/V rings
     static constexpr int kOffSS = kOffX + BM * kXStride * 4;
     static_assert(kOffSS + BM * 4 <= kOffBar, "epilogue buffers fit in the K/V rings");
+    // Output staging (128-byte-swizzled boxes of 128 rows, up to 64 KB) in the
+    // second half of the V ring, clear of the exchange buffers.
+    static constexpr int kOffOut = kOffV + kVStages * kVBytes / 2;
+    static_assert(kOffOut >= kOffSS + BM * 4 && kOffOut % 1024 == 0, "staging after the exchange buffers");
+    static_assert(kOffOut + BM * 128 * (kHalf / 32) <= kOffBar, "fp32 staging fits");
     static_assert(kSmem <= 232448, "shared memory budget");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 2 * BN;
@@ -376,9 +381,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // Phase C: normalise and store this CTA's half of the row.
         const float tot = ss + ld_dsmem_f32(mapa_shared(smem_u32(ssbuf + r), peer));
         const float rsc = (1.0f - p.lambda_init) / sqrtf(tot / (float)DV + p.eps);
-        const int qrow = q0 + r;
-        const bool store = qrow < p.N;
-        const int64_t obase = (((int64_t)b * p.N + (store ? qrow : 0)) * p.H + h) * DV + own0;
+        // Stage the half row in 128-byte-swizzled boxes of 128 rows; one TMA store per
+        // box writes the tile and clips the rows past N.
+        uint8_t* stage = smem + C::kOffOut;
 #pragma unroll 1
         for (int c = 0; c < H2 / 32; ++c) {
             uint32_t o[32];
@@ -393,22 +398,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 y[4 * i + 2] = fmaf(__uint_as_float(o[4 * i + 2]), coef, q.z) * rsc;
                 y[4 * i + 3] = fmaf(__uint_as_float(o[4 * i + 3]), coef, q.w) * rsc;
             }
-            if (!store) continue;
             if (p.norm_w) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) y[i] *= p.norm_w[own0 + c * 32 + i];
             }
             if (p.out_bf16) {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + obase + c * 32);
+                // 32 columns = half a box row: box c/2, 16-byte chunks (c%2)*4 .. +3.
+                uint8_t* box = stage + (c >> 1) * (BM * 128);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pack_bf16x2(y[8 * i], y[8 * i + 1]), pack_bf16x2(y[8 * i + 2], y[8 * i + 3]),
-                                        pack_bf16x2(y[8 * i + 4], y[8 * i + 5]), pack_bf16x2(y[8 * i + 6], y[8 * i + 7]));
+                    *reinterpret_cast<uint4*>(box + sw128_offset(r, (c & 1) * 4 + i)) =
+                        make_uint4(pack_bf16x2(y[8 * i], y[8 * i + 1]), pack_bf16x2(y[8 * i + 2], y[8 * i + 3]),
+                                   pack_bf16x2(y[8 * i + 4], y[8 * i + 5]), pack_bf16x2(y[8 * i + 6], y[8 * i + 7]));
             } else {
-                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + obase + c * 32);
+                uint8_t* box = stage + c * (BM * 128);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+                for (int i = 0; i < 8; ++i)
+                    *reinterpret_cast<float4*>(box + sw128_offset(r, i)) =
+                        make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
             }
+        }
+    }
+    if (epi) {
+        fence_proxy_async_shared();
+        named_bar_sync(1, 128);  // all four epilogue warps, on every path
+        if (warp == 2 && lane == 0 && !*abort_flag) {
+            const int bw = p.out_bf16 ? 64 : 32;  // elements per 128-byte box row
+            for (int i = 0; i < H2 / bw; ++i)
+                tma_store_3d(&p.tm_out, smem + C::kOffOut + i * (BM * 128), h * DV + own0 + i * bw, q0, b);
+            tma_store_commit();
+            tma_store_wait_read();
         }
     }
     // The peer must have finished reading this CTA's shared memory before it exits.
