@@ -14,14 +14,15 @@
 // epilogue forms O1/l1 - lambda O2/l2. (The pages' remark that FlashAttention
 // can be reused is prior art only; nothing of it is followed here.)
 //
-// CTA = one 128-row query tile of one (b, h); 12 warps:
+// CTA = one 128-row query tile of one (b, h); 10 warps:
 //   warp 0       TMA producer: Q1, Q2 once, then a 3-stage ring of (K1, K2, V)
 //                tiles of 128 keys, all 128-byte swizzled.
 //   warp 1       allocates 512 TMEM columns; one lane issues every MMA:
 //                S1 = Q1 K1^T, S2 = Q2 K2^T (fp32 in TMEM), O1 += P1 V,
 //                O2 += P2 V (P read from TMEM, V from shared memory, fp32 O
 //                in TMEM).
-//   warps 4..7   softmax of map 1; warps 8..11 softmax of map 2. Thread r of a
+//   warps 2..5   softmax of map 1; warps 6..9 softmax of map 2 (warp w reads
+//                TMEM lanes 32*(w%4)..+31). Thread r of a
 //                group owns query row r (TMEM lane r): it reads its S row,
 //                updates max and sum, writes its P row as bf16 back into the
 //                first half of its S columns, and rescales its O row in TMEM
@@ -44,7 +45,7 @@ namespace da {
 namespace {
 
 constexpr int BM = kFwdBM, BN = kFwdBN;
-constexpr int kThreads = 12 * 32;
+constexpr int kThreads = 10 * 32;
 constexpr int kKvStages = 3;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -240,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 }
             }
         }
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ softmax (map g)
-        const int g = (warp - 4) >> 2;
+        const int g = (warp - 2) >> 2;
         const int lg = warp & 3;
         const int r = lg * 32 + lane;  // query row within the tile == TMEM lane
         const int qrow = q0 + r;
