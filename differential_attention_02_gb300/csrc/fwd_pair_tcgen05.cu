@@ -200,41 +200,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t tS[2] = {tmem, tmem + BN};
-            const uint32_t tO = tmem + C::kColO;
-            const uint64_t dq = sdesc_sw128(smem_u32(qs), 16, 1024);
-            const uint64_t dk0 = sdesc_sw128(smem_u32(ks), 16, 1024);
-            const uint64_t dv0 = sdesc_sw128(smem_u32(vs), BN * 128, 1024);
-            constexpr uint64_t kKStep = C::kKBytes >> 4, kVStep = C::kVBytes >> 4;
-            // S(j) = Q K(j)^T into score buffer j % 2, then K(j) is released.
-            auto issue_s = [&](int j) -> bool {
-                const int sk = j % C::kKStages;
-                if (!mbar_wait(&bars->k_full[sk], (j / C::kKStages) & 1, abort_flag, p.err, 0x55)) return false;
-                tc_fence_after();
+        // The whole warp walks the loop and waits; one elected lane issues each
+        // group of MMAs together with the commits that track them.
+        const uint32_t tS[2] = {tmem, tmem + BN};
+        const uint32_t tO = tmem + C::kColO;
+        const uint64_t dq = sdesc_sw128(smem_u32(qs), 16, 1024);
+        const uint64_t dk0 = sdesc_sw128(smem_u32(ks), 16, 1024);
+        const uint64_t dv0 = sdesc_sw128(smem_u32(vs), BN * 128, 1024);
+        constexpr uint64_t kKStep = C::kKBytes >> 4, kVStep = C::kVBytes >> 4;
+        // S(j) = Q K(j)^T into score buffer j % 2, then K(j) is released.
+        auto issue_s = [&](int j) -> bool {
+            const int sk = j % C::kKStages;
+            if (!mbar_wait_warp(&bars->k_full[sk], (j / C::kKStages) & 1, abort_flag, p.err, 0x55)) return false;
+            tc_fence_after();
+            if (elect_one()) {
                 issue_qk<D, F16>(tS[j & 1], dq, dk0 + sk * kKStep);
                 umma_commit(&bars->s_full[j & 1]);
                 umma_commit(&bars->k_empty[sk]);
-                return true;
-            };
-            bool go = mbar_wait(&bars->q_full, 0, abort_flag, p.err, 0x54) && issue_s(0) && (nkv < 2 || issue_s(1));
-            for (int j = 0; go && j < nkv; ++j) {
-                const int bf = j & 1;
-                const int sv = j % C::kVStages;
-                if (!mbar_wait(&bars->p_full[bf], (j >> 1) & 1, abort_flag, p.err, 0x57)) break;
-                if (!mbar_wait(&bars->v_full[sv], (j / C::kVStages) & 1, abort_flag, p.err, 0x58)) break;
-                tc_fence_after();
+            }
+            __syncwarp();
+            return true;
+        };
+        bool go = mbar_wait_warp(&bars->q_full, 0, abort_flag, p.err, 0x54) && issue_s(0) && (nkv < 2 || issue_s(1));
+        for (int j = 0; go && j < nkv; ++j) {
+            const int bf = j & 1;
+            const int sv = j % C::kVStages;
+            if (!mbar_wait_warp(&bars->p_full[bf], (j >> 1) & 1, abort_flag, p.err, 0x57)) break;
+            if (!mbar_wait_warp(&bars->v_full[sv], (j / C::kVStages) & 1, abort_flag, p.err, 0x58)) break;
+            tc_fence_after();
+            if (elect_one()) {
                 issue_pv<DV, F16>(tO, tS[bf], dv0 + sv * kVStep, j > 0 ? 1u : 0u);
                 umma_commit(&bars->o_done);
                 umma_commit(&bars->v_empty[sv]);
-                // S(j+2) reuses buffer bf: it is issued after PV(j), which reads P(j)
-                // there, and tcgen05 MMAs of one thread execute in issue order.
-                if (j + 2 < nkv && !issue_s(j + 2)) break;
             }
-            // Every MMA issued (also before an abort) must finish before TMEM is freed.
-            umma_commit(&bars->drain);
-            mbar_wait(&bars->drain, 0, nullptr, p.err, 0x59);
+            __syncwarp();
+            // S(j+2) reuses buffer bf: it is issued after PV(j), which reads P(j)
+            // there, and tcgen05 MMAs of one thread execute in issue order.
+            if (j + 2 < nkv && !issue_s(j + 2)) break;
         }
+        // Every MMA issued (also before an abort) must finish before TMEM is freed.
+        if (elect_one()) umma_commit(&bars->drain);
+        __syncwarp();
+        mbar_wait(&bars->drain, 0, nullptr, p.err, 0x59);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax

@@ -17,7 +17,8 @@
 // CTA = one 128-row query tile of one (b, h); 10 warps:
 //   warp 0       TMA producer: Q1, Q2 once, then a 3-stage ring of (K1, K2, V)
 //                tiles of 128 keys, all 128-byte swizzled.
-//   warp 1       allocates 512 TMEM columns; one lane issues every MMA:
+//   warp 1       allocates 512 TMEM columns; the warp walks the MMA loop
+//                converged and one elected lane issues every MMA:
 //                S1 = Q1 K1^T, S2 = Q2 K2^T (fp32 in TMEM), O1 += P1 V,
 //                O2 += P2 V (P read from TMEM, V from shared memory, fp32 O
 //                in TMEM).
@@ -194,44 +195,51 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + BN};
-            const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + DV};
-            const uint64_t dq[2] = {sdesc_sw128(smem_u32(q1s), 16, 1024), sdesc_sw128(smem_u32(q2s), 16, 1024)};
-            // Stage s descriptors = stage-0 descriptors + s * kStageBytes (in 16-byte units).
-            const uint64_t dk0 = sdesc_sw128(smem_u32(stages), 16, 1024);
-            const uint64_t dv0 = sdesc_sw128(smem_u32(stages) + 2 * C::kKBytes, BN * 128, 1024);
-            constexpr uint64_t kStageStep = C::kStageBytes >> 4;
-            constexpr uint64_t kK2Step = C::kKBytes >> 4;
-            bool ok = mbar_wait(&bars->q_full, 0, abort_flag, p.err, 0x34) &&
-                      mbar_wait(&bars->kv_full[0], 0, abort_flag, p.err, 0x35);
-            if (ok) {
-                tc_fence_after();
+        // The whole warp walks the loop and waits; one elected lane issues each
+        // group of MMAs together with the commits that track them.
+        const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + BN};
+        const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + DV};
+        const uint64_t dq[2] = {sdesc_sw128(smem_u32(q1s), 16, 1024), sdesc_sw128(smem_u32(q2s), 16, 1024)};
+        // Stage s descriptors = stage-0 descriptors + s * kStageBytes (in 16-byte units).
+        const uint64_t dk0 = sdesc_sw128(smem_u32(stages), 16, 1024);
+        const uint64_t dv0 = sdesc_sw128(smem_u32(stages) + 2 * C::kKBytes, BN * 128, 1024);
+        constexpr uint64_t kStageStep = C::kStageBytes >> 4;
+        constexpr uint64_t kK2Step = C::kKBytes >> 4;
+        bool ok = mbar_wait_warp(&bars->q_full, 0, abort_flag, p.err, 0x34) &&
+                  mbar_wait_warp(&bars->kv_full[0], 0, abort_flag, p.err, 0x35);
+        if (ok) {
+            tc_fence_after();
+            if (elect_one()) {
                 issue_qk<D, F16>(tS[0], dq[0], dk0);
                 umma_commit(&bars->s_full[0]);
                 issue_qk<D, F16>(tS[1], dq[1], dk0 + kK2Step);
                 umma_commit(&bars->s_full[1]);
             }
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int s = j % kKvStages;
-                const uint64_t dv = dv0 + s * kStageStep;
-                const bool more = j + 1 < nkv;
-                const int s1 = (j + 1) % kKvStages;
-                const uint64_t dk1 = dk0 + s1 * kStageStep;
-                // map 1: PV1(j), then S1(j+1)
-                if (!mbar_wait(&bars->p_full[0], j & 1, abort_flag, p.err, 0x36)) break;
-                tc_fence_after();
+            __syncwarp();
+        }
+        for (int j = 0; ok && j < nkv; ++j) {
+            const int s = j % kKvStages;
+            const uint64_t dv = dv0 + s * kStageStep;
+            const bool more = j + 1 < nkv;
+            const int s1 = (j + 1) % kKvStages;
+            const uint64_t dk1 = dk0 + s1 * kStageStep;
+            // map 1: PV1(j), then S1(j+1)
+            if (!mbar_wait_warp(&bars->p_full[0], j & 1, abort_flag, p.err, 0x36)) break;
+            if (more && !mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x37)) break;
+            tc_fence_after();
+            if (elect_one()) {
                 issue_pv<DV, F16>(tO[0], tS[0], dv, j > 0 ? 1u : 0u);
                 umma_commit(&bars->o_done[0]);
                 if (more) {
-                    if (!mbar_wait(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x37)) break;
-                    tc_fence_after();
                     issue_qk<D, F16>(tS[0], dq[0], dk1);
                     umma_commit(&bars->s_full[0]);
                 }
-                // map 2: PV2(j), release the stage, then S2(j+1)
-                if (!mbar_wait(&bars->p_full[1], j & 1, abort_flag, p.err, 0x38)) break;
-                tc_fence_after();
+            }
+            __syncwarp();
+            // map 2: PV2(j), release the stage, then S2(j+1)
+            if (!mbar_wait_warp(&bars->p_full[1], j & 1, abort_flag, p.err, 0x38)) break;
+            tc_fence_after();
+            if (elect_one()) {
                 issue_pv<DV, F16>(tO[1], tS[1], dv, j > 0 ? 1u : 0u);
                 umma_commit(&bars->o_done[1]);
                 umma_commit(&bars->kv_empty[s]);
@@ -240,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                     umma_commit(&bars->s_full[1]);
                 }
             }
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------------------ softmax (map g)
@@ -419,8 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 
     // ---------------------------------------------------------------- teardown
     // Every MMA issued (also before an abort) must finish before TMEM is freed.
-    if (warp == 1 && lane == 0) {
-        umma_commit(&bars->drain);
+    if (warp == 1) {
+        if (elect_one()) umma_commit(&bars->drain);  // the lane that issued the MMAs
+        __syncwarp();
         mbar_wait(&bars->drain, 0, nullptr, p.err, 0x39);
     }
     tc_fence_before();

@@ -12,7 +12,7 @@
 // 256-column TMEM accumulators let the epilogue of one tile overlap the MMAs
 // of the next. Warp roles: warp 0 = TMA producer (one lane; A K-major
 // 128 x 64 boxes, W N-major 64 x 64 boxes, both 128-byte swizzled, 3-stage
-// ring), warp 1 = TMEM owner and MMA issuer (one lane; B given as MN-major),
+// ring), warp 1 = TMEM owner and MMA issuer (an elected lane of the converged warp; B given as MN-major),
 // warps 2..5 = epilogue: warp w owns TMEM lanes (tile rows) 32*(w%4)..+31 and
 // writes them through 128-byte-swizzled shared-memory boxes with TMA stores,
 // 128 columns per pass.
@@ -109,41 +109,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
-            // A: K-major, 128-byte rows; one K=16 step is 32 bytes along the row.
-            // B: MN-major; 64-column boxes are kWBoxBytes apart (leading offset),
-            // 8-row K groups 1024 bytes apart (stride offset); K=16 is 16 rows.
-            const uint64_t da0 = sdesc_sw128(smem_u32(smem), 16, 1024);
-            const uint64_t dw0 = sdesc_sw128(smem_u32(smem) + kABytes, kWBoxBytes, 1024);
-            constexpr uint64_t kStep = kStageBytes >> 4;
-            int it = 0, local = 0;
-            bool go = true;
-            for (int t = blockIdx.x; go && t < tiles; t += gridDim.x, ++local) {
-                const int buf = local & 1;
-                // The epilogue must have read this accumulator's previous tile.
-                if (!mbar_wait(&bars->acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 0x23)) break;
+        // The whole warp walks the loop and waits; one elected lane issues each
+        // k-block's MMAs together with the commit that tracks them.
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
+        // A: K-major, 128-byte rows; one K=16 step is 32 bytes along the row.
+        // B: MN-major; 64-column boxes are kWBoxBytes apart (leading offset),
+        // 8-row K groups 1024 bytes apart (stride offset); K=16 is 16 rows.
+        const uint64_t da0 = sdesc_sw128(smem_u32(smem), 16, 1024);
+        const uint64_t dw0 = sdesc_sw128(smem_u32(smem) + kABytes, kWBoxBytes, 1024);
+        constexpr uint64_t kStep = kStageBytes >> 4;
+        int it = 0, local = 0;
+        bool go = true;
+        for (int t = blockIdx.x; go && t < tiles; t += gridDim.x, ++local) {
+            const int buf = local & 1;
+            // The epilogue must have read this accumulator's previous tile.
+            if (!mbar_wait_warp(&bars->acc_empty[buf], ((local >> 1) & 1) ^ 1, abort_flag, p.err, 0x23)) break;
+            tc_fence_after();
+            const uint32_t acc = tmem + buf * BN;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % kStages;
+                if (!mbar_wait_warp(&bars->full[s], (it / kStages) & 1, abort_flag, p.err, 0x24)) {
+                    go = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t acc = tmem + buf * BN;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int s = it % kStages;
-                    if (!mbar_wait(&bars->full[s], (it / kStages) & 1, abort_flag, p.err, 0x24)) {
-                        go = false;
-                        break;
-                    }
-                    tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         umma_ss(acc, da0 + s * kStep + (uint64_t)(k * 2), dw0 + s * kStep + (uint64_t)(k * 128), idesc,
                                 (kb > 0 || k > 0) ? 1u : 0u);
                     umma_commit(&bars->empty[s]);
+                    if (kb == kblocks - 1) umma_commit(&bars->acc_full[buf]);
                 }
-                if (go) umma_commit(&bars->acc_full[buf]);
+                __syncwarp();
             }
-            // Every MMA issued (also before an abort) must finish before TMEM is freed.
-            umma_commit(&bars->drain);
-            mbar_wait(&bars->drain, 0, nullptr, p.err, 0x25);
         }
+        // Every MMA issued (also before an abort) must finish before TMEM is freed.
+        if (elect_one()) umma_commit(&bars->drain);
+        __syncwarp();
+        mbar_wait(&bars->drain, 0, nullptr, p.err, 0x25);
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         const int lg = warp & 3;  // TMEM lane group (tile rows) this warp may access
