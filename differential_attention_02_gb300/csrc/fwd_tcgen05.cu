@@ -79,6 +79,7 @@ struct Bars {
     uint64_t kv_full[kKvStages];
     uint64_t kv_empty[kKvStages];
     uint64_t s_full[2];
+    uint64_t p_half[2];  // P of keys 0..BN/2-1 is in TMEM
     uint64_t p_full[2];
     uint64_t o_done[2];
     uint64_t drain;
@@ -104,11 +105,14 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc, uint6
 // next box (leading offset), the next 8 keys +1024 bytes (stride offset), so one
 // K=16 step advances 2048 bytes (128 in 16-byte units).
 template <int DV, bool F16>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t accumulate) {
+__device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, int half,
+                                              uint32_t accumulate) {
     constexpr uint32_t idesc = idesc_kind_f16(BM, DV, 0, 1, F16);
-    umma_ts(o_tmem, p_tmem, v_desc, idesc, accumulate);
 #pragma unroll
-    for (int kk = 1; kk < BN / 16; ++kk) umma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)(kk * 128), idesc, 1u);
+    for (int k = 0; k < BN / 32; ++k) {
+        const int kk = half * (BN / 32) + k;
+        umma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)(kk * 128), idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
 }
 
 template <int D, int DV, bool F16>
@@ -137,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(&bars->s_full[g], 1);
-            mbar_init(&bars->p_full[g], 4);  // one arrival per softmax warp
+            mbar_init(&bars->p_half[g], 4);  // one arrival per softmax warp
+            mbar_init(&bars->p_full[g], 4);
             mbar_init(&bars->o_done[g], 1);
         }
         mbar_init(&bars->drain, 1);
@@ -223,32 +228,37 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
             const bool more = j + 1 < nkv;
             const int s1 = (j + 1) % kKvStages;
             const uint64_t dk1 = dk0 + s1 * kStageStep;
-            // map 1: PV1(j), then S1(j+1)
-            if (!mbar_wait_warp(&bars->p_full[0], j & 1, abort_flag, p.err, 0x36)) break;
-            if (more && !mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x37)) break;
-            tc_fence_after();
-            if (elect_one()) {
-                issue_pv<DV, F16>(tO[0], tS[0], dv, j > 0 ? 1u : 0u);
-                umma_commit(&bars->o_done[0]);
-                if (more) {
-                    issue_qk<D, F16>(tS[0], dq[0], dk1);
-                    umma_commit(&bars->s_full[0]);
+            // Per map: the first half of PV(j) as soon as the softmax has written the
+            // first half of P(j), then the second half and S(j+1).
+            for (int m = 0; m < 2; ++m) {
+                if (!mbar_wait_warp(&bars->p_half[m], j & 1, abort_flag, p.err, 0x36 + m)) {
+                    ok = false;
+                    break;
                 }
-            }
-            __syncwarp();
-            // map 2: PV2(j), release the stage, then S2(j+1)
-            if (!mbar_wait_warp(&bars->p_full[1], j & 1, abort_flag, p.err, 0x38)) break;
-            tc_fence_after();
-            if (elect_one()) {
-                issue_pv<DV, F16>(tO[1], tS[1], dv, j > 0 ? 1u : 0u);
-                umma_commit(&bars->o_done[1]);
-                umma_commit(&bars->kv_empty[s]);
-                if (more) {
-                    issue_qk<D, F16>(tS[1], dq[1], dk1 + kK2Step);
-                    umma_commit(&bars->s_full[1]);
+                tc_fence_after();
+                if (elect_one()) issue_pv_half<DV, F16>(tO[m], tS[m], dv, 0, j > 0 ? 1u : 0u);
+                __syncwarp();
+                if (!mbar_wait_warp(&bars->p_full[m], j & 1, abort_flag, p.err, 0x3b + m)) {
+                    ok = false;
+                    break;
                 }
+                if (m == 0 && more &&
+                    !mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x38)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_pv_half<DV, F16>(tO[m], tS[m], dv, 1, 1u);
+                    umma_commit(&bars->o_done[m]);
+                    if (m == 1) umma_commit(&bars->kv_empty[s]);
+                    if (more) {
+                        issue_qk<D, F16>(tS[m], dq[m], dk1 + m * kK2Step);
+                        umma_commit(&bars->s_full[m]);
+                    }
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
     } else {
         // ------------------------------------------------------------ softmax (map g)
@@ -300,46 +310,47 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 m_used = m_new;
                 rescale = true;
             }
-            // P = exp2(S * scale - max), row sum in fp32.
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[BN / 2];
-#pragma unroll
-            for (int i = 0; i < BN; i += 2) {
-                const float e0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sl2, -m_used));
-                const float e1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sl2, -m_used));
-                rs[(i >> 1) & 3] += e0 + e1;
-                pk[i / 2] = pack_p<F16>(e0, e1);
-            }
-            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-
-            if (j > 0) {
-                // PV(j-1) must be finished before O is rescaled (it already is once S(j)
-                // has landed, since MMAs complete in issue order).
+            // O must hold PV(j-1) before it is rescaled; S(j) landing already implies
+            // that (MMAs complete in issue order), so this wait returns at once.
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                 if (!mbar_wait_warp(&bars->o_done[g], (j - 1) & 1, abort_flag, p.err, 0x42 + g)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                    for (int c = 0; c < DV / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c * 32, o);
-                        tmem_ld_wait();
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(tO + c * 32, o);
-                    }
-                    tmem_st_wait();
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO + c * 32, o);
                 }
             }
-            // P row (bf16 pairs, lower key in the low half) -> the first BN/2 columns of S.
+            // P = exp2(S * scale - max) as 16-bit pairs (lower key in the low half) into
+            // the first BN/2 columns of S, row sum in fp32. The first half of the keys is
+            // handed to the MMA warp before the second half is exponentiated, so the
+            // first half of PV(j) overlaps the rest of the softmax.
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) tmem_st32(tS + c * 32, pk + c * 32);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[g]);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[BN / 4];
+#pragma unroll
+                for (int i = 0; i < BN / 2; i += 2) {
+                    const int k = hf * (BN / 2) + i;
+                    const float e0 = fast_exp2(fmaf(__uint_as_float(sr[k]), sl2, -m_used));
+                    const float e1 = fast_exp2(fmaf(__uint_as_float(sr[k + 1]), sl2, -m_used));
+                    rs[(i >> 1) & 3] += e0 + e1;
+                    pk[i / 2] = pack_p<F16>(e0, e1);
+                }
+                tmem_st32(tS + hf * (BN / 4), pk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hf == 0 ? &bars->p_half[g] : &bars->p_full[g]);
+            }
+            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         }
 
         // ------------------------------------------------------------ epilogue
