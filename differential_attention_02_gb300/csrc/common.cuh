@@ -293,6 +293,18 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Register reallocation between warpgroups (all 128 threads of a warpgroup
+// execute it). An increase waits until other warpgroups have released enough
+// registers of the block's launch allotment.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // True in exactly one lane of the (fully converged) calling warp; the same
 // lane each time for the same member mask. MMAs and the commits that track
 // them are issued by that lane: a commit covers only its own thread's MMAs.

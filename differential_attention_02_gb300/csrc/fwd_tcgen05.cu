@@ -14,15 +14,15 @@
 // epilogue forms O1/l1 - lambda O2/l2. (The pages' remark that FlashAttention
 // can be reused is prior art only; nothing of it is followed here.)
 //
-// CTA = one 128-row query tile of one (b, h); 10 warps:
-//   warp 0       TMA producer: Q1, Q2 once, then a 3-stage ring of (K1, K2, V)
+// CTA = one 128-row query tile of one (b, h); 12 warps:
+//   warp 8       TMA producer: Q1, Q2 once, then a 3-stage ring of (K1, K2, V)
 //                tiles of 128 keys, all 128-byte swizzled.
-//   warp 1       allocates 512 TMEM columns; the warp walks the MMA loop
+//   warp 9       allocates 512 TMEM columns; the warp walks the MMA loop
 //                converged and one elected lane issues every MMA:
 //                S1 = Q1 K1^T, S2 = Q2 K2^T (fp32 in TMEM), O1 += P1 V,
 //                O2 += P2 V (P read from TMEM, V from shared memory, fp32 O
 //                in TMEM).
-//   warps 2..5   softmax of map 1; warps 6..9 softmax of map 2 (warp w reads
+//   warps 0..3   softmax of map 1; warps 4..7 softmax of map 2 (warp w reads
 //                TMEM lanes 32*(w%4)..+31). Thread r of a
 //                group owns query row r (TMEM lane r): it reads its S row,
 //                updates max and sum, writes its P row as bf16 back into the
@@ -46,7 +46,17 @@ namespace da {
 namespace {
 
 constexpr int BM = kFwdBM, BN = kFwdBN;
-constexpr int kThreads = 10 * 32;
+// Warps 0..3: softmax of map 1, 4..7: softmax of map 2 (warp w reads TMEM lanes
+// 32*(w%4)..+31), 8: TMA producer, 9: TMEM owner and MMA issuer, 10..11: idle
+// (they complete the third warpgroup, which register reallocation works on).
+constexpr int kThreads = 12 * 32;
+constexpr int kWarpProducer = 8, kWarpMma = 9;
+// Register split: the softmax warpgroups grow to kRegsSoftmax, the third
+// warpgroup shrinks to kRegsOther. The launch provides kRegsLaunch per thread;
+// 2*128*kRegsSoftmax + 128*kRegsOther must not exceed 384*kRegsLaunch, or the
+// increase would wait forever. The launcher checks the compiled count.
+constexpr int kRegsLaunch = 168, kRegsSoftmax = 224, kRegsOther = 56;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split");
 constexpr int kKvStages = 3;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -149,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         bars->abort = 0;
         fence_mbarrier_init();
     }
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tmem_alloc(&bars->tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
@@ -162,107 +172,125 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     uint8_t* q2s = smem + C::kOffQ2;
     uint8_t* stages = smem + C::kOffStages;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&p.tm_q1);
-            tma_prefetch_desc(&p.tm_q2);
-            tma_prefetch_desc(&p.tm_k1);
-            tma_prefetch_desc(&p.tm_k2);
-            tma_prefetch_desc(&p.tm_v);
-            mbar_arrive_expect_tx(&bars->q_full, 2 * C::kQBytes);
-#pragma unroll
-            for (int x = 0; x < D / 64; ++x) {
-                tma_load_4d(q1s + x * C::kBoxBytes, &p.tm_q1, &bars->q_full, x * 64, q0, h, b);
-                tma_load_4d(q2s + x * C::kBoxBytes, &p.tm_q2, &bars->q_full, x * 64, q0, h, b);
-            }
-            int j = 0;
-            for (; j < nkv; ++j) {
-                const int s = j % kKvStages;
-                if (!mbar_wait(&bars->kv_empty[s], ((j / kKvStages) & 1) ^ 1, abort_flag, p.err, 0x31)) break;
-                uint8_t* st = stages + s * C::kStageBytes;
-                mbar_arrive_expect_tx(&bars->kv_full[s], C::kStageBytes);
-#pragma unroll
+    if (warp >= 8) {
+        // Third warpgroup: producer, MMA issuer, two idle warps. Each warpgroup
+        // reallocates registers at the top of its own branch, so the compiler
+        // applies each limit to that branch's code.
+        setmaxnreg_dec<kRegsOther>();
+        if (warp == kWarpProducer) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                tma_prefetch_desc(&p.tm_q1);
+                tma_prefetch_desc(&p.tm_q2);
+                tma_prefetch_desc(&p.tm_k1);
+                tma_prefetch_desc(&p.tm_k2);
+                tma_prefetch_desc(&p.tm_v);
+                mbar_arrive_expect_tx(&bars->q_full, 2 * C::kQBytes);
+    #pragma unroll
                 for (int x = 0; x < D / 64; ++x) {
-                    tma_load_4d(st + x * C::kBoxBytes, &p.tm_k1, &bars->kv_full[s], x * 64, j * BN, h, b);
-                    tma_load_4d(st + C::kKBytes + x * C::kBoxBytes, &p.tm_k2, &bars->kv_full[s], x * 64, j * BN, h,
-                                b);
+                    tma_load_4d(q1s + x * C::kBoxBytes, &p.tm_q1, &bars->q_full, x * 64, q0, h, b);
+                    tma_load_4d(q2s + x * C::kBoxBytes, &p.tm_q2, &bars->q_full, x * 64, q0, h, b);
                 }
-#pragma unroll
-                for (int x = 0; x < DV / 64; ++x)
-                    tma_load_4d(st + 2 * C::kKBytes + x * C::kBoxBytes, &p.tm_v, &bars->kv_full[s], x * 64, j * BN,
-                                h, b);
+                int j = 0;
+                for (; j < nkv; ++j) {
+                    const int s = j % kKvStages;
+                    if (!mbar_wait(&bars->kv_empty[s], ((j / kKvStages) & 1) ^ 1, abort_flag, p.err, 0x31)) break;
+                    uint8_t* st = stages + s * C::kStageBytes;
+                    mbar_arrive_expect_tx(&bars->kv_full[s], C::kStageBytes);
+    #pragma unroll
+                    for (int x = 0; x < D / 64; ++x) {
+                        tma_load_4d(st + x * C::kBoxBytes, &p.tm_k1, &bars->kv_full[s], x * 64, j * BN, h, b);
+                        tma_load_4d(st + C::kKBytes + x * C::kBoxBytes, &p.tm_k2, &bars->kv_full[s], x * 64, j * BN, h,
+                                    b);
+                    }
+    #pragma unroll
+                    for (int x = 0; x < DV / 64; ++x)
+                        tma_load_4d(st + 2 * C::kKBytes + x * C::kBoxBytes, &p.tm_v, &bars->kv_full[s], x * 64, j * BN,
+                                    h, b);
+                }
+                // Drain: no copy may still be landing in shared memory when the CTA exits.
+                mbar_wait(&bars->q_full, 0, nullptr, p.err, 0x32);
+                for (int u = max(0, j - kKvStages); u < j; ++u)
+                    mbar_wait(&bars->kv_full[u % kKvStages], (u / kKvStages) & 1, nullptr, p.err, 0x33);
             }
-            // Drain: no copy may still be landing in shared memory when the CTA exits.
-            mbar_wait(&bars->q_full, 0, nullptr, p.err, 0x32);
-            for (int u = max(0, j - kKvStages); u < j; ++u)
-                mbar_wait(&bars->kv_full[u % kKvStages], (u / kKvStages) & 1, nullptr, p.err, 0x33);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp walks the loop and waits; one elected lane issues each
-        // group of MMAs together with the commits that track them.
-        const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + BN};
-        const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + DV};
-        const uint64_t dq[2] = {sdesc_sw128(smem_u32(q1s), 16, 1024), sdesc_sw128(smem_u32(q2s), 16, 1024)};
-        // Stage s descriptors = stage-0 descriptors + s * kStageBytes (in 16-byte units).
-        const uint64_t dk0 = sdesc_sw128(smem_u32(stages), 16, 1024);
-        const uint64_t dv0 = sdesc_sw128(smem_u32(stages) + 2 * C::kKBytes, BN * 128, 1024);
-        constexpr uint64_t kStageStep = C::kStageBytes >> 4;
-        constexpr uint64_t kK2Step = C::kKBytes >> 4;
-        bool ok = mbar_wait_warp(&bars->q_full, 0, abort_flag, p.err, 0x34) &&
-                  mbar_wait_warp(&bars->kv_full[0], 0, abort_flag, p.err, 0x35);
-        if (ok) {
-            tc_fence_after();
-            if (elect_one()) {
-                issue_qk<D, F16>(tS[0], dq[0], dk0);
-                umma_commit(&bars->s_full[0]);
-                issue_qk<D, F16>(tS[1], dq[1], dk0 + kK2Step);
-                umma_commit(&bars->s_full[1]);
-            }
-            __syncwarp();
-        }
-        for (int j = 0; ok && j < nkv; ++j) {
-            const int s = j % kKvStages;
-            const uint64_t dv = dv0 + s * kStageStep;
-            const bool more = j + 1 < nkv;
-            const int s1 = (j + 1) % kKvStages;
-            const uint64_t dk1 = dk0 + s1 * kStageStep;
-            // Per map: the first half of PV(j) as soon as the softmax has written the
-            // first half of P(j), then the second half and S(j+1).
-            for (int m = 0; m < 2; ++m) {
-                if (!mbar_wait_warp(&bars->p_half[m], j & 1, abort_flag, p.err, 0x36 + m)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (elect_one()) issue_pv_half<DV, F16>(tO[m], tS[m], dv, 0, j > 0 ? 1u : 0u);
-                __syncwarp();
-                if (!mbar_wait_warp(&bars->p_full[m], j & 1, abort_flag, p.err, 0x3b + m)) {
-                    ok = false;
-                    break;
-                }
-                if (m == 0 && more &&
-                    !mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x38)) {
-                    ok = false;
-                    break;
-                }
+        } else if (warp == kWarpMma) {
+            // ------------------------------------------------------------ MMA issuer
+            // The whole warp walks the loop and waits; one elected lane issues each
+            // group of MMAs together with the commits that track them.
+            const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + BN};
+            const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + DV};
+            const uint64_t dq[2] = {sdesc_sw128(smem_u32(q1s), 16, 1024), sdesc_sw128(smem_u32(q2s), 16, 1024)};
+            // Stage s descriptors = stage-0 descriptors + s * kStageBytes (in 16-byte units).
+            const uint64_t dk0 = sdesc_sw128(smem_u32(stages), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(stages) + 2 * C::kKBytes, BN * 128, 1024);
+            constexpr uint64_t kStageStep = C::kStageBytes >> 4;
+            constexpr uint64_t kK2Step = C::kKBytes >> 4;
+            bool ok = mbar_wait_warp(&bars->q_full, 0, abort_flag, p.err, 0x34) &&
+                      mbar_wait_warp(&bars->kv_full[0], 0, abort_flag, p.err, 0x35);
+            if (ok) {
                 tc_fence_after();
                 if (elect_one()) {
-                    issue_pv_half<DV, F16>(tO[m], tS[m], dv, 1, 1u);
-                    umma_commit(&bars->o_done[m]);
-                    if (m == 1) umma_commit(&bars->kv_empty[s]);
-                    if (more) {
-                        issue_qk<D, F16>(tS[m], dq[m], dk1 + m * kK2Step);
-                        umma_commit(&bars->s_full[m]);
-                    }
+                    issue_qk<D, F16>(tS[0], dq[0], dk0);
+                    umma_commit(&bars->s_full[0]);
+                    issue_qk<D, F16>(tS[1], dq[1], dk0 + kK2Step);
+                    umma_commit(&bars->s_full[1]);
                 }
                 __syncwarp();
             }
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int s = j % kKvStages;
+                const uint64_t dv = dv0 + s * kStageStep;
+                const bool more = j + 1 < nkv;
+                const int s1 = (j + 1) % kKvStages;
+                const uint64_t dk1 = dk0 + s1 * kStageStep;
+                // Per map: the first half of PV(j) as soon as the softmax has written the
+                // first half of P(j), then the second half and S(j+1).
+                for (int m = 0; m < 2; ++m) {
+                    if (!mbar_wait_warp(&bars->p_half[m], j & 1, abort_flag, p.err, 0x36 + m)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (elect_one()) issue_pv_half<DV, F16>(tO[m], tS[m], dv, 0, j > 0 ? 1u : 0u);
+                    __syncwarp();
+                    if (!mbar_wait_warp(&bars->p_full[m], j & 1, abort_flag, p.err, 0x3b + m)) {
+                        ok = false;
+                        break;
+                    }
+                    if (m == 0 && more &&
+                        !mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x38)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_pv_half<DV, F16>(tO[m], tS[m], dv, 1, 1u);
+                        umma_commit(&bars->o_done[m]);
+                        if (m == 1) umma_commit(&bars->kv_empty[s]);
+                        if (more) {
+                            issue_qk<D, F16>(tS[m], dq[m], dk1 + m * kK2Step);
+                            umma_commit(&bars->s_full[m]);
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            // Every MMA issued (also before an abort) must finish before TMEM is freed.
+            if (elect_one()) umma_commit(&bars->drain);  // the lane that issued the MMAs
+            __syncwarp();
+            mbar_wait(&bars->drain, 0, nullptr, p.err, 0x39);
+        }
+        // ---------------------------------------------------------------- teardown
+        tc_fence_before();
+        named_bar_sync(2, kThreads);  // every role is done with TMEM and shared memory
+        if (warp == kWarpMma) {
+            tc_fence_after();
+            tmem_dealloc(tmem, C::kTmemCols);
         }
     } else {
+        setmaxnreg_inc<kRegsSoftmax>();
         // ------------------------------------------------------------ softmax (map g)
-        const int g = (warp - 2) >> 2;
+        const int g = warp >> 2;
         const int lg = warp & 3;
         const int r = lg * 32 + lane;  // query row within the tile == TMEM lane
         const int qrow = q0 + r;
@@ -429,26 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         }
         fence_proxy_async_shared();
         named_bar_sync(1, 256);
-        if (threadIdx.x == 128 && !*abort_flag) {
+        if (threadIdx.x == 0 && !*abort_flag) {
             const int bw = p.out_bf16 ? 64 : 32;  // elements per 128-byte box row
             for (int i = 0; i < DV / bw; ++i) tma_store_3d(&p.tm_out, stage + i * (BM * 128), h * DV + i * bw, q0, b);
             tma_store_commit();
             tma_store_wait_read();
         }
-    }
-
-    // ---------------------------------------------------------------- teardown
-    // Every MMA issued (also before an abort) must finish before TMEM is freed.
-    if (warp == 1) {
-        if (elect_one()) umma_commit(&bars->drain);  // the lane that issued the MMAs
-        __syncwarp();
-        mbar_wait(&bars->drain, 0, nullptr, p.err, 0x39);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, C::kTmemCols);
+        tc_fence_before();
+        named_bar_sync(2, kThreads);  // releases the MMA warp to free TMEM
     }
 }
 
@@ -458,6 +474,11 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
     auto k = fwd_bf16_kernel<D, DV, F16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
+    // The register split assumes the compiled per-thread count (see kRegsLaunch).
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, k);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
     const int n_tiles = (p.N + BM - 1) / BM;
     k<<<n_tiles * p.B * p.H, kThreads, C::kSmem, stream>>>(p);
     return cudaGetLastError();
