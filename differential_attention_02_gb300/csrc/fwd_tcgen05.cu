@@ -253,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                     tc_fence_after();
                     if (elect_one()) issue_pv_half<DV, F16>(tO[m], tS[m], dv, 0, j > 0 ? 1u : 0u);
                     __syncwarp();
-                    if (!mbar_wait_warp(&bars->p_full[m], j & 1, abort_flag, p.err, 0x3b + m)) {
+                    // The next K/V tile is checked while the softmax still works on the
+                    // second half of P, off the path from p_full to the MMAs.
+                    if (m == 0 && more &&
+                        !mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x38)) {
                         ok = false;
                         break;
                     }
-                    if (m == 0 && more &&
-                        !mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kKvStages) & 1, abort_flag, p.err, 0x38)) {
+                    if (!mbar_wait_warp(&bars->p_full[m], j & 1, abort_flag, p.err, 0x3b + m)) {
                         ok = false;
                         break;
                     }
