@@ -299,25 +299,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 pk[i / 2] = pack_p<F16>(e0, e1);
             }
             l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-            if (j > 0) {
-                // PV(j-1) must be finished before O is rescaled.
+            // Only a rescale of O has to wait for PV(j-1); P(j) goes to the other
+            // score buffer. S(j) was issued after PV(j-2), so once it has landed
+            // o_done is at most one phase behind and the parity wait is exact.
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                 if (!mbar_wait_warp(&bars->o_done, (j - 1) & 1, abort_flag, p.err, 0x61)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                    for (int c = 0; c < DV / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + c * 32, o);
-                        tmem_ld_wait();
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(tO + c * 32, o);
-                    }
-                    tmem_st_wait();
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO + c * 32, o);
                 }
+                tmem_st_wait();
             }
             // P row (bf16 pairs, lower key in the low half) -> the first BN/2 columns of S.
 #pragma unroll
