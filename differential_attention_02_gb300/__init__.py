@@ -162,9 +162,10 @@ def diffattn_fwd(q1, q2, k1, k2, v, lam: float, lam_init: float, eps: float = 1e
     if out is None:
         out = torch.empty((B, N, H, Dv), dtype=out_dtype, device=q1.device)
     lib = load_library()
-    nbytes = ctypes.c_size_t()
-    _check(lib.diffattn_fwd_workspace_size(B, H, N, d, Dv, ctypes.byref(nbytes)), "diffattn_fwd_workspace_size")
-    ws = workspace(nbytes.value, q1.device) if ws is None else ws
+    if ws is None:
+        nbytes = ctypes.c_size_t()
+        _check(lib.diffattn_fwd_workspace_size(B, H, N, d, Dv, ctypes.byref(nbytes)), "diffattn_fwd_workspace_size")
+        ws = workspace(nbytes.value, q1.device)
     w = None if norm_weight is None else ctypes.c_void_p(norm_weight.data_ptr())
     _check(lib.diffattn_fwd(_t4(q1), _t4(q2), _t4(k1), _t4(k2), _t4(v), ctypes.c_void_p(out.data_ptr()), w,
                             B, H, N, d, Dv, int(bool(causal)), float(lam), float(lam_init), float(eps),

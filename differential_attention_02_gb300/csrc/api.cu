@@ -34,10 +34,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 int device_sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
+    int n = 0;
+    return da::device_sm_count(&n) == cudaSuccess ? n : 0;
 }
 
 // 4-D bf16 map over a [B, H, rows, width] operand (strides in elements).
@@ -100,7 +98,8 @@ int32_t* err_word(void* ws) { return reinterpret_cast<int32_t*>(ws); }
 // Decode split count: the smallest split count whose CTA waves are at least 90%
 // full on this GPU, capped so that every split keeps at least 256 keys.
 int decode_auto_splits(int B, int H, int L, int d) {
-    const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
+    const int n_sm = device_sm_count();
+    const int sms = n_sm > 0 ? n_sm : 148;
     const int per_sm = (d == 64) ? 2 : 1;  // resident split CTAs per SM (shared-memory bound)
     const double slots = (double)sms * per_sm;
     const int smax = std::max(1, std::min(256, L / 256));

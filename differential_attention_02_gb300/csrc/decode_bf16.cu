@@ -302,7 +302,7 @@ template <int D, int DV>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
     using C = DecodeCfg<D, DV>;
     auto k = decode_split_kernel<D, DV>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    cudaError_t e = prepare_once<decode_split_kernel<D, DV>>((int)C::kSmem);
     if (e != cudaSuccess) return e;
     k<<<dim3(p.num_splits, p.H, p.B), kThreads, C::kSmem, stream>>>(p);
     e = cudaGetLastError();

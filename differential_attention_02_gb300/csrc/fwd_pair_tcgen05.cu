@@ -333,11 +333,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------------- epilogue
     // Every thread of both CTAs takes part in the three pair_sync calls below.
-    // TMEM and peer shared-memory reads are done by whole warps (tcgen05.ld is
-    // warp-collective); only the global stores depend on the row being < N.
+    // TMEM reads are done by whole warps (tcgen05.ld is warp-collective); only
+    // the global stores depend on the row being < N. The pair exchanges data by
+    // pushing it into the peer's shared memory (remote stores), then reads its
+    // own shared memory.
     constexpr int H2 = C::kHalf;
-    float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);  // [BM][kXStride]: other half, scaled
-    float* ssbuf = reinterpret_cast<float*>(smem + C::kOffSS);
+    float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);  // [BM][kXStride]: the peer's part of my half
+    float* ssbuf = reinterpret_cast<float*>(smem + C::kOffSS);  // the peer's sums of squares
     const bool epi = warp >= 2;
     const int lg = warp & 3;
     const int r = lg * 32 + lane;
@@ -345,26 +347,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t peer = rank ^ 1u;
     const float coef = (rank == 0) ? 1.0f / l : -p.lambda / l;  // this map's weight in O1/l1 - lambda O2/l2
     const uint32_t own0 = rank * H2, other0 = peer * H2;
+    // The exchange buffers live in the K/V rings: both CTAs must be past their
+    // last MMA before either writes into the other's.
+    ok = pair_sync(&bars->xsync, peer, 0, abort_flag, p.err, 0x63) && ok;
+    ok = __all_sync(0xffffffffu, ok);
     if (epi && ok) {
-        // Phase A: the half of this map's row the peer finishes -> own shared memory.
+        // Phase A: the half of this map's row the peer finishes -> the peer's buffer.
+        const uint32_t peer_x = mapa_shared(smem_u32(xbuf + r * C::kXStride), peer);
 #pragma unroll 1
         for (int c = 0; c < H2 / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tO + other0 + c * 32, o);
             tmem_ld_wait();
-            float4* dst = reinterpret_cast<float4*>(xbuf + r * C::kXStride + c * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(o[4 * i]) * coef, __uint_as_float(o[4 * i + 1]) * coef,
-                                     __uint_as_float(o[4 * i + 2]) * coef, __uint_as_float(o[4 * i + 3]) * coef);
+                st_dsmem_f4(peer_x + (uint32_t)(c * 32 + 4 * i) * 4u,
+                            make_float4(__uint_as_float(o[4 * i]) * coef, __uint_as_float(o[4 * i + 1]) * coef,
+                                        __uint_as_float(o[4 * i + 2]) * coef, __uint_as_float(o[4 * i + 3]) * coef));
         }
     }
-    ok = pair_sync(&bars->xsync, peer, 0, abort_flag, p.err, 0x63) && ok;
+    ok = pair_sync(&bars->xsync, peer, 1, abort_flag, p.err, 0x64) && ok;
     ok = __all_sync(0xffffffffu, ok);
-    const uint32_t peer_x = mapa_shared(smem_u32(xbuf + r * C::kXStride), peer);
+    const float* xrow = xbuf + r * C::kXStride;
     float ss = 0.f;
     if (epi && ok) {
-        // Phase B: this CTA's half of O1/l1 - lambda O2/l2 and its sum of squares.
+        // Phase B: this CTA's half of O1/l1 - lambda O2/l2 and its sum of squares,
+        // which goes to the peer as well.
 #pragma unroll 1
         for (int c = 0; c < H2 / 32; ++c) {
             uint32_t o[32];
@@ -372,7 +380,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float4 q = ld_dsmem_f4(peer_x + (uint32_t)(c * 32 + 4 * i) * 4u);
+                const float4 q = *reinterpret_cast<const float4*>(xrow + c * 32 + 4 * i);
                 const float x0 = fmaf(__uint_as_float(o[4 * i]), coef, q.x);
                 const float x1 = fmaf(__uint_as_float(o[4 * i + 1]), coef, q.y);
                 const float x2 = fmaf(__uint_as_float(o[4 * i + 2]), coef, q.z);
@@ -380,13 +388,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ss = fmaf(x0, x0, fmaf(x1, x1, fmaf(x2, x2, fmaf(x3, x3, ss))));
             }
         }
-        ssbuf[r] = ss;
+        st_dsmem_f32(mapa_shared(smem_u32(ssbuf + r), peer), ss);
     }
-    ok = pair_sync(&bars->xsync, peer, 1, abort_flag, p.err, 0x64) && ok;
+    ok = pair_sync(&bars->xsync, peer, 2, abort_flag, p.err, 0x65) && ok;
     ok = __all_sync(0xffffffffu, ok && !*abort_flag);
     if (epi && ok) {
         // Phase C: normalise and store this CTA's half of the row.
-        const float tot = ss + ld_dsmem_f32(mapa_shared(smem_u32(ssbuf + r), peer));
+        const float tot = ss + ssbuf[r];
         const float rsc = (1.0f - p.lambda_init) / sqrtf(tot / (float)DV + p.eps);
         // Stage the half row in 128-byte-swizzled boxes of 128 rows; one TMA store per
         // box writes the tile and clips the rows past N.
@@ -399,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float y[32];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float4 q = ld_dsmem_f4(peer_x + (uint32_t)(c * 32 + 4 * i) * 4u);
+                const float4 q = *reinterpret_cast<const float4*>(xrow + c * 32 + 4 * i);
                 y[4 * i] = fmaf(__uint_as_float(o[4 * i]), coef, q.x) * rsc;
                 y[4 * i + 1] = fmaf(__uint_as_float(o[4 * i + 1]), coef, q.y) * rsc;
                 y[4 * i + 2] = fmaf(__uint_as_float(o[4 * i + 2]), coef, q.z) * rsc;
@@ -437,8 +445,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_store_wait_read();
         }
     }
-    // The peer must have finished reading this CTA's shared memory before it exits.
-    pair_sync(&bars->xsync, peer, 2, abort_flag, p.err, 0x65);
+    // No remote access follows the third rendezvous: each CTA's pushes into the
+    // other landed before it, so either may exit.
 
     tc_fence_before();
     __syncthreads();
@@ -452,7 +460,7 @@ template <int D, int DV, bool F16>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
     using C = PairCfg<D, DV>;
     auto k = fwd_pair_kernel<D, DV, F16>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    cudaError_t e = prepare_once<fwd_pair_kernel<D, DV, F16>>((int)C::kSmem);
     if (e != cudaSuccess) return e;
     const int n_tiles = (p.N + BM - 1) / BM;
     k<<<2 * n_tiles * p.B * p.H, kThreads, C::kSmem, stream>>>(p);

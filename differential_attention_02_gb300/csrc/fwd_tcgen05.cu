@@ -474,13 +474,9 @@ template <int D, int DV, bool F16>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D, DV>;
     auto k = fwd_bf16_kernel<D, DV, F16>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-    if (e != cudaSuccess) return e;
     // The register split assumes the compiled per-thread count (see kRegsLaunch).
-    cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, k);
+    cudaError_t e = prepare_once<fwd_bf16_kernel<D, DV, F16>>((int)C::kSmem, kRegsLaunch);
     if (e != cudaSuccess) return e;
-    if (attr.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
     const int n_tiles = (p.N + BM - 1) / BM;
     k<<<n_tiles * p.B * p.H, kThreads, C::kSmem, stream>>>(p);
     return cudaGetLastError();

@@ -229,11 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
 }  // namespace
 
 cudaError_t launch_gemm_bf16(const GemmParams& p, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    cudaError_t e = prepare_once<gemm_bf16_kernel>((int)kSmem);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
     const int tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
     gemm_bf16_kernel<<<tiles < sms ? tiles : sms, kThreads, kSmem, stream>>>(p);
     return cudaGetLastError();

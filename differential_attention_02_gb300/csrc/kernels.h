@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace da {
 
 // fp32 SIMT prefill (any d <= 128 multiple of 4, Dv <= 256 multiple of 32).
@@ -78,5 +80,41 @@ constexpr int kFwdBN = 128;
 
 // One CTA whose single wait can never complete (bounded-wait self-test).
 cudaError_t launch_selftest_timeout(int32_t* err, cudaStream_t stream);
+
+// One-time setup of a kernel on the current device (first call per device):
+// the dynamic shared-memory opt-in and, when want_regs > 0, a check that the
+// compiled per-thread register count is the one the kernel's register split
+// was computed from. Later calls on that device return at once.
+template <auto Kernel>
+cudaError_t prepare_once(int smem_bytes, int want_regs = 0) {
+    static std::atomic<uint64_t> ready{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+    if (bit != 0 && (ready.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    if (want_regs > 0) {
+        cudaFuncAttributes a;
+        e = cudaFuncGetAttributes(&a, Kernel);
+        if (e != cudaSuccess) return e;
+        if (a.numRegs != want_regs) return cudaErrorInvalidConfiguration;
+    }
+    ready.fetch_or(bit, std::memory_order_release);
+    return cudaSuccess;
+}
+
+// Number of SMs of the current device (queried once per device).
+inline cudaError_t device_sm_count(int* sms) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && (*sms = cache[dev].load(std::memory_order_relaxed)) > 0) return cudaSuccess;
+    if ((e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (dev < 64) cache[dev].store(*sms, std::memory_order_relaxed);
+    return cudaSuccess;
+}
 
 }  // namespace da
