@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 tma_prefetch_desc(&p.tm_k2);
                 tma_prefetch_desc(&p.tm_v);
                 mbar_arrive_expect_tx(&bars->q_full, 2 * C::kQBytes);
-    #pragma unroll
+#pragma unroll
                 for (int x = 0; x < D / 64; ++x) {
                     tma_load_4d(q1s + x * C::kBoxBytes, &p.tm_q1, &bars->q_full, x * 64, q0, h, b);
                     tma_load_4d(q2s + x * C::kBoxBytes, &p.tm_q2, &bars->q_full, x * 64, q0, h, b);
@@ -197,13 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                     if (!mbar_wait(&bars->kv_empty[s], ((j / kKvStages) & 1) ^ 1, abort_flag, p.err, 0x31)) break;
                     uint8_t* st = stages + s * C::kStageBytes;
                     mbar_arrive_expect_tx(&bars->kv_full[s], C::kStageBytes);
-    #pragma unroll
+#pragma unroll
                     for (int x = 0; x < D / 64; ++x) {
                         tma_load_4d(st + x * C::kBoxBytes, &p.tm_k1, &bars->kv_full[s], x * 64, j * BN, h, b);
                         tma_load_4d(st + C::kKBytes + x * C::kBoxBytes, &p.tm_k2, &bars->kv_full[s], x * 64, j * BN, h,
                                     b);
                     }
-    #pragma unroll
+#pragma unroll
                     for (int x = 0; x < DV / 64; ++x)
                         tma_load_4d(st + 2 * C::kKBytes + x * C::kBoxBytes, &p.tm_v, &bars->kv_full[s], x * 64, j * BN,
                                     h, b);
