@@ -11,11 +11,11 @@
 // so the CTAs running at once share W and each A row block through L2). Two
 // 256-column TMEM accumulators let the epilogue of one tile overlap the MMAs
 // of the next. Warp roles: warp 0 = TMA producer (one lane; A K-major
-// 128 x 64 boxes, W N-major 64 x 64 boxes, both 128-byte swizzled, 3-stage
+// 128 x 64 boxes, W N-major 64 x 64 boxes, both 128-byte swizzled, 4-stage
 // ring), warp 1 = TMEM owner and MMA issuer (an elected lane of the converged warp; B given as MN-major),
 // warps 2..5 = epilogue: warp w owns TMEM lanes (tile rows) 32*(w%4)..+31 and
 // writes them through 128-byte-swizzled shared-memory boxes with TMA stores,
-// 128 columns per pass.
+// 64 columns per pass.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -23,13 +23,14 @@ namespace da {
 namespace {
 
 constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
-constexpr int kStages = 3;
+constexpr int kStages = 4;  // 48 KB each: ~2K cycles of MMA work in flight
 constexpr int kABytes = BM * BK * 2;             // 16 KB
 constexpr int kWBoxBytes = BK * 64 * 2;          // 8 KB: 64 K-rows x 64 N-columns
 constexpr int kWBytes = (BN / 64) * kWBoxBytes;  // 32 KB
 constexpr int kStageBytes = kABytes + kWBytes;
 constexpr int kOutBoxBytes = 32 * 128;           // one [32 rows][128 bytes] output box
-constexpr int kOutWarpBytes = 4 * kOutBoxBytes;  // one epilogue warp's staging: 128 columns of fp32
+constexpr int kOutCols = 64;                     // output columns per epilogue pass
+constexpr int kOutWarpBytes = 2 * kOutBoxBytes;  // one epilogue warp's staging: 64 columns of fp32
 constexpr int kOffOut = kStages * kStageBytes;
 constexpr int kOffBar = kOffOut + 4 * kOutWarpBytes;
 constexpr int kThreads = 6 * 32;
@@ -166,18 +167,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
             const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
             const uint32_t t_row = tmem + buf * BN + ((uint32_t)(lg * 32) << 16);
 #pragma unroll 1
-            for (int pass = 0; pass < BN / 128; ++pass) {
+            for (int pass = 0; pass < BN / kOutCols; ++pass) {
                 // The staging boxes of this warp must be free (its previous stores read them).
                 if (lane == 0) tma_store_wait_read();
                 __syncwarp();
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kOutCols / 32; ++c) {
                     uint32_t r[32];
-                    tmem_ld32(t_row + pass * 128 + c * 32, r);
+                    tmem_ld32(t_row + pass * kOutCols + c * 32, r);
                     tmem_ld_wait();
                     if (eb == 2) {
-                        // 32 columns = half a box row: box c/2, 16-byte chunks (c%2)*4 .. +3.
-                        uint8_t* box = stage + (c >> 1) * kOutBoxBytes;
+                        // 32 columns = half a box row: 16-byte chunks c*4 .. c*4+3 of the one box.
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const float* f = reinterpret_cast<const float*>(r + 8 * j);
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                             else
                                 v = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                                                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-                            *reinterpret_cast<uint4*>(box + sw128_offset(lane, (c & 1) * 4 + j)) = v;
+                            *reinterpret_cast<uint4*>(stage + sw128_offset(lane, c * 4 + j)) = v;
                         }
                     } else {
                         // 32 fp32 columns = one box row.
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                                 make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
                     }
                 }
-                if (pass == BN / 128 - 1) {
+                if (pass == BN / kOutCols - 1) {
                     // Done reading this accumulator: the MMA warp may reuse it.
                     tc_fence_before();
                     __syncwarp();
@@ -208,9 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                 fence_proxy_async_shared();
                 __syncwarp();
                 if (lane == 0) {
-                    const int nbox = 128 / bw;
+                    const int nbox = kOutCols / bw;
                     for (int i = 0; i < nbox; ++i)
-                        tma_store_2d(&p.tm_c, stage + i * kOutBoxBytes, n0 + pass * 128 + i * bw, m0 + lg * 32);
+                        tma_store_2d(&p.tm_c, stage + i * kOutBoxBytes, n0 + pass * kOutCols + i * bw, m0 + lg * 32);
                     tma_store_commit();
                 }
             }
