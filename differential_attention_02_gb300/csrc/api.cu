@@ -220,7 +220,8 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
     if (!encode_4d(&p.tm_q1, q1, d, N, H, B, 64, kFwdBM, sw, dt) || !encode_4d(&p.tm_q2, q2, d, N, H, B, 64, kFwdBM, sw, dt) ||
         !encode_4d(&p.tm_k1, k1, d, N, H, B, 64, kFwdBN, sw, dt) || !encode_4d(&p.tm_k2, k2, d, N, H, B, 64, kFwdBN, sw, dt) ||
-        !encode_4d(&p.tm_v, v, Dv, N, H, B, 64, kFwdBN, sw, dt) ||
+        // V boxes: 128 keys for the single-CTA kernel, 64 for the CTA pair (half-tile V ring).
+        !encode_4d(&p.tm_v, v, Dv, N, H, B, 64, d == 64 ? kFwdBN : kFwdBN / 2, sw, dt) ||
         !encode_out_3d(&p.tm_out, out, H * Dv, N, B, out_dtype == DIFFATTN_F32 ? 4 : 2, kFwdBM))
         return DIFFATTN_ERR_INVALID_ARG;
     p.in_f16 = in_dtype == DIFFATTN_F16;

@@ -39,10 +39,12 @@ struct PairCfg {
     static constexpr int kQBytes = BM * D * 2;
     static constexpr int kKBytes = BN * D * 2;
     static constexpr int kVBytes = BN * DV * 2;
+    static constexpr int kVHBytes = kVBytes / 2;      // half a V tile: 64 keys
     static constexpr int kBoxBytes = 128 * 128;  // one [128 rows][64 bf16] box
     // Separate K and V rings: S(j+2) needs K two tiles ahead, PV(j) needs V(j).
     static constexpr int kKStages = (D == 128) ? 2 : 4;
     static constexpr int kVStages = (D == 128) ? 2 : 4;
+    static constexpr int kVHStages = 2 * kVStages;   // the V ring holds half tiles
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKBytes;
@@ -60,6 +62,7 @@ struct PairCfg {
     static_assert(kOffOut >= kOffSS + BM * 4 && kOffOut % 1024 == 0, "staging after the exchange buffers");
     static_assert(kOffOut + BM * 128 * (kHalf / 32) <= kOffBar, "fp32 staging fits");
     static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(kKStages <= 4 && kVHStages <= 8 && kVHStages % 2 == 0, "barrier arrays");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 2 * BN;
     static_assert(2 * BN + DV <= 512, "TMEM budget");
@@ -67,11 +70,12 @@ struct PairCfg {
 
 struct PairBars {
     uint64_t q_full;
-    uint64_t k_full[4];
+    uint64_t k_full[4];  // kKStages <= 4
     uint64_t k_empty[4];
-    uint64_t v_full[4];
-    uint64_t v_empty[4];
+    uint64_t v_full[8];
+    uint64_t v_empty[8];
     uint64_t s_full[2];
+    uint64_t p_half[2];  // P of keys 0..BN/2-1 of score buffer b is in TMEM
     uint64_t p_full[2];
     uint64_t o_done;
     uint64_t drain;
@@ -92,12 +96,19 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc, uint6
 
 // O (+)= P V with P in TMEM (lane r = row r, 16 keys per 8 columns) and the V
 // tile's descriptor advancing 2048 bytes (16 keys) per step.
+// O (+)= P V for one half of the keys: P from TMEM (keys half*BN/2 .. +BN/2, 16
+// keys per 8 columns), V from a half-tile stage: boxes of [BN/2 keys][64 columns]
+// (leading offset to the next 64 columns), 8 keys per 1024 bytes, so one K=16 step
+// advances 2048 bytes (128 in 16-byte units).
 template <int DV, bool F16>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t accumulate) {
+__device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, uint64_t vh_desc, int half,
+                                              uint32_t accumulate) {
     constexpr uint32_t idesc = idesc_kind_f16(BM, DV, 0, 1, F16);
-    umma_ts(o_tmem, p_tmem, v_desc, idesc, accumulate);
 #pragma unroll
-    for (int kk = 1; kk < BN / 16; ++kk) umma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)(kk * 128), idesc, 1u);
+    for (int k = 0; k < BN / 32; ++k) {
+        const int kk = half * (BN / 32) + k;
+        umma_ts(o_tmem, p_tmem + kk * 8, vh_desc + (uint64_t)(k * 128), idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
 }
 
 template <int D, int DV, bool F16>
@@ -124,15 +135,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
-        for (int s = 0; s < 4; ++s) {
+        for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->k_empty[s], 1);
+        }
+        for (int s = 0; s < C::kVHStages; ++s) {
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->p_full[i], 4);  // one arrival per softmax warp
+            mbar_init(&bars->p_half[i], 4);  // one arrival per softmax warp
+            mbar_init(&bars->p_full[i], 4);
         }
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
@@ -172,7 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int jk = 0, jv = 0;
             bool go = true;
             for (int j = 0; go && j < nkv; ++j) {
-                const int sk = j % C::kKStages, sv = j % C::kVStages;
+                const int sk = j % C::kKStages;
                 go = mbar_wait(&bars->k_empty[sk], ((j / C::kKStages) & 1) ^ 1, abort_flag, p.err, 0x51);
                 if (!go) break;
                 mbar_arrive_expect_tx(&bars->k_full[sk], C::kKBytes);
@@ -181,21 +195,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tma_load_4d(ks + sk * C::kKBytes + x * C::kBoxBytes, tm_k, &bars->k_full[sk], x * 64, j * BN, h,
                                 b);
                 jk = j + 1;
-                go = mbar_wait(&bars->v_empty[sv], ((j / C::kVStages) & 1) ^ 1, abort_flag, p.err, 0x52);
-                if (!go) break;
-                mbar_arrive_expect_tx(&bars->v_full[sv], C::kVBytes);
+                // V(j) as two half tiles of BN/2 keys, each in its own stage of the V ring.
+                for (int hh = 0; go && hh < 2; ++hh) {
+                    const int u = 2 * j + hh, su = u % C::kVHStages;
+                    go = mbar_wait(&bars->v_empty[su], ((u / C::kVHStages) & 1) ^ 1, abort_flag, p.err, 0x52);
+                    if (!go) break;
+                    mbar_arrive_expect_tx(&bars->v_full[su], C::kVHBytes);
 #pragma unroll
-                for (int x = 0; x < DV / 64; ++x)
-                    tma_load_4d(vs + sv * C::kVBytes + x * C::kBoxBytes, &p.tm_v, &bars->v_full[sv], x * 64, j * BN,
-                                h, b);
-                jv = j + 1;
+                    for (int x = 0; x < DV / 64; ++x)
+                        tma_load_4d(vs + su * C::kVHBytes + x * (BN / 2) * 128, &p.tm_v, &bars->v_full[su], x * 64,
+                                    j * BN + hh * (BN / 2), h, b);
+                    jv = u + 1;
+                }
             }
             // Drain: no copy may still be landing in shared memory when the CTA exits.
             mbar_wait(&bars->q_full, 0, nullptr, p.err, 0x53);
             for (int u = max(0, jk - C::kKStages); u < jk; ++u)
                 mbar_wait(&bars->k_full[u % C::kKStages], (u / C::kKStages) & 1, nullptr, p.err, 0x53);
-            for (int u = max(0, jv - C::kVStages); u < jv; ++u)
-                mbar_wait(&bars->v_full[u % C::kVStages], (u / C::kVStages) & 1, nullptr, p.err, 0x53);
+            for (int u = max(0, jv - C::kVHStages); u < jv; ++u)
+                mbar_wait(&bars->v_full[u % C::kVHStages], (u / C::kVHStages) & 1, nullptr, p.err, 0x53);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -206,8 +224,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + C::kColO;
         const uint64_t dq = sdesc_sw128(smem_u32(qs), 16, 1024);
         const uint64_t dk0 = sdesc_sw128(smem_u32(ks), 16, 1024);
-        const uint64_t dv0 = sdesc_sw128(smem_u32(vs), BN * 128, 1024);
-        constexpr uint64_t kKStep = C::kKBytes >> 4, kVStep = C::kVBytes >> 4;
+        const uint64_t dv0 = sdesc_sw128(smem_u32(vs), (BN / 2) * 128, 1024);
+        constexpr uint64_t kKStep = C::kKBytes >> 4, kVHStep = C::kVHBytes >> 4;
         // S(j) = Q K(j)^T into score buffer j % 2, then K(j) is released.
         auto issue_s = [&](int j) -> bool {
             const int sk = j % C::kKStages;
@@ -224,14 +242,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool go = mbar_wait_warp(&bars->q_full, 0, abort_flag, p.err, 0x54) && issue_s(0) && (nkv < 2 || issue_s(1));
         for (int j = 0; go && j < nkv; ++j) {
             const int bf = j & 1;
-            const int sv = j % C::kVStages;
-            if (!mbar_wait_warp(&bars->p_full[bf], (j >> 1) & 1, abort_flag, p.err, 0x57)) break;
-            if (!mbar_wait_warp(&bars->v_full[sv], (j / C::kVStages) & 1, abort_flag, p.err, 0x58)) break;
+            // Half h of PV(j) reads V half tile u = 2j + h and the h-th half of P(j); the
+            // first starts as soon as the softmax has written the first half of P(j).
+            const int u0 = (2 * j) % C::kVHStages, u1 = (2 * j + 1) % C::kVHStages;
+            const uint32_t pu = (uint32_t)((2 * j) / C::kVHStages) & 1;  // same phase for both halves
+            if (!mbar_wait_warp(&bars->v_full[u0], pu, abort_flag, p.err, 0x58)) break;
+            if (!mbar_wait_warp(&bars->p_half[bf], (j >> 1) & 1, abort_flag, p.err, 0x56)) break;
             tc_fence_after();
             if (elect_one()) {
-                issue_pv<DV, F16>(tO, tS[bf], dv0 + sv * kVStep, j > 0 ? 1u : 0u);
+                issue_pv_half<DV, F16>(tO, tS[bf], dv0 + u0 * kVHStep, 0, j > 0 ? 1u : 0u);
+                umma_commit(&bars->v_empty[u0]);
+            }
+            __syncwarp();
+            if (!mbar_wait_warp(&bars->v_full[u1], pu, abort_flag, p.err, 0x5a)) break;
+            if (!mbar_wait_warp(&bars->p_full[bf], (j >> 1) & 1, abort_flag, p.err, 0x57)) break;
+            tc_fence_after();
+            if (elect_one()) {
+                issue_pv_half<DV, F16>(tO, tS[bf], dv0 + u1 * kVHStep, 1, 1u);
                 umma_commit(&bars->o_done);
-                umma_commit(&bars->v_empty[sv]);
+                umma_commit(&bars->v_empty[u1]);
             }
             __syncwarp();
             // S(j+2) reuses buffer bf: it is issued after PV(j), which reads P(j)
@@ -289,16 +318,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 m_used = m_new;
                 rescale = true;
             }
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[BN / 2];
-#pragma unroll
-            for (int i = 0; i < BN; i += 2) {
-                const float e0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sl2, -m_used));
-                const float e1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sl2, -m_used));
-                rs[(i >> 1) & 3] += e0 + e1;
-                pk[i / 2] = pack_p<F16>(e0, e1);
-            }
-            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
             // Only a rescale of O has to wait for PV(j-1); P(j) goes to the other
             // score buffer. S(j) was issued after PV(j-2), so once it has landed
             // o_done is at most one phase behind and the parity wait is exact.
@@ -317,15 +336,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                     tmem_st32(tO + c * 32, o);
                 }
-                tmem_st_wait();
             }
-            // P row (bf16 pairs, lower key in the low half) -> the first BN/2 columns of S.
+            // P row (16-bit pairs, lower key in the low half) -> the first BN/2 columns of
+            // S, in two halves: the first is handed to the MMA warp before the second is
+            // exponentiated, so the first half of PV(j) overlaps the rest of the softmax.
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) tmem_st32(tS + c * 32, pk + c * 32);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full[bf]);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[BN / 4];
+#pragma unroll
+                for (int i = 0; i < BN / 2; i += 2) {
+                    const int kx = hf * (BN / 2) + i;
+                    const float e0 = fast_exp2(fmaf(__uint_as_float(sr[kx]), sl2, -m_used));
+                    const float e1 = fast_exp2(fmaf(__uint_as_float(sr[kx + 1]), sl2, -m_used));
+                    rs[(i >> 1) & 3] += e0 + e1;
+                    pk[i / 2] = pack_p<F16>(e0, e1);
+                }
+                tmem_st32(tS + hf * (BN / 4), pk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hf == 0 ? &bars->p_half[bf] : &bars->p_full[bf]);
+            }
+            l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         }
         if (ok && nkv > 0) ok = mbar_wait_warp(&bars->o_done, (nkv - 1) & 1, abort_flag, p.err, 0x62);
         tc_fence_after();
