@@ -251,12 +251,57 @@ def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float,
     return y.view(B, N, dm)
 
 
+_side_streams = {}
+
+
+def _streams_for(device):
+    """Three side streams per device (copies in, compute, copies out), created once."""
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    if key not in _side_streams:
+        _side_streams[key] = tuple(torch.cuda.Stream(device=key) for _ in range(3))
+    return _side_streams[key]
+
+
 def diffattn_fwd_host(q1, q2, k1, k2, v, lam, lam_init, eps=1e-5, out_dtype=torch.float32, device="cuda",
-                      stream=None, out_host=None):
-    """End-to-end call from pinned HOST tensors: copy in, run the fused prefill, copy the result out."""
-    dev = [t.to(device, non_blocking=True) for t in (q1, q2, k1, k2, v)]
-    out = diffattn_fwd(*dev, lam, lam_init, eps, out_dtype=out_dtype, stream=stream)
+                      stream=None, out_host=None, chunks=None):
+    """End-to-end call from pinned HOST tensors [B,H,N,*]; returns the host output [B,N,H,Dv].
+
+    The batch is processed in `chunks` pieces (default: up to 4) on three streams, so the
+    host-to-device copies of one piece overlap the prefill of another and the copy back of
+    a third. (Two streams for the copies in were measured slower than one.) Device buffers are allocated on the caller's stream (default: the current one),
+    and that stream waits for all three before the call returns, so work enqueued on it
+    afterwards, including reuse of those buffers, is ordered after this call.
+    """
+    caller = torch.cuda.current_stream(device) if stream is None else stream
+    names = (q1, q2, k1, k2, v)
+    B, H, N, d = q1.shape
+    Dv = v.shape[-1]
+    n = max(1, min(B, chunks or 4))
+    bounds = [(B * i) // n for i in range(n + 1)]
+    s_in, s_run, s_out = _streams_for(device)
+    with torch.cuda.stream(caller):
+        dev = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in names]
+        out = torch.empty((B, N, H, Dv), dtype=out_dtype, device=device)
+        nbytes = ctypes.c_size_t()
+        _check(load_library().diffattn_fwd_workspace_size(B, H, N, d, Dv, ctypes.byref(nbytes)),
+               "diffattn_fwd_workspace_size")
+        ws = workspace(nbytes.value, device)
     if out_host is None:
         out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    out_host.copy_(out, non_blocking=True)
+    for s in (s_in, s_run, s_out):
+        s.wait_stream(caller)
+    for i in range(n):
+        lo, hi = bounds[i], bounds[i + 1]
+        if lo == hi:
+            continue
+        with torch.cuda.stream(s_in):
+            for dst, src in zip(dev, names):
+                dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+        s_run.wait_stream(s_in)
+        diffattn_fwd(*(t[lo:hi] for t in dev), lam, lam_init, eps, out_dtype=out_dtype, out=out[lo:hi], ws=ws,
+                     stream=s_run)
+        s_out.wait_stream(s_run)
+        with torch.cuda.stream(s_out):
+            out_host[lo:hi].copy_(out[lo:hi], non_blocking=True)
+    caller.wait_stream(s_out)
     return out_host

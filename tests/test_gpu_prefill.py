@@ -181,3 +181,20 @@ def test_f16_operands(d, Dv, N):
     ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, 1e-5)
     assert_bf16_parity(_run(t, lam, lam_init), ref, f"f16 d{d} N{N}")
     assert_bf16_out_parity(_run(t, lam, lam_init, out_dtype=torch.bfloat16), ref, f"f16 d{d} N{N} bf16 out")
+
+
+def test_host_entry_point_matches_device_call():
+    """diffattn_fwd_host (pinned host buffers, batch pipelined over copy/compute/copy
+    streams, uneven chunks) returns exactly what one device call returns, and meets the
+    oracle."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    host = gi.prefill_inputs(w, B=3, H=2, N=300)
+    pin = [host[k].pin_memory() for k in NAMES]
+    lam, lam_init = 0.45, 0.47
+    for chunks in (2, 3):
+        got = da.diffattn_fwd_host(*pin, lam, lam_init, out_dtype=torch.bfloat16, chunks=chunks)
+        torch.cuda.synchronize()
+        want = da.diffattn_fwd(*(t.cuda() for t in pin), lam, lam_init, out_dtype=torch.bfloat16)
+        assert torch.equal(got, want.cpu()), f"chunks={chunks}"
+    ref = orc.diffattn_fwd(*(host[k] for k in NAMES), lam, lam_init)
+    assert_bf16_out_parity(got, ref, "host entry point B3 H2 N300")
