@@ -380,12 +380,49 @@ def run_decode(args, da, gi, dev, stream, peaks, peak_kind):
     gbs = kvb / (dms * 1e-3) / 1e9
     per_seq = profiled_traffic("decode_split_per_sequence_H16L8192", ["decode_bf16.cu", "common.cuh", "kernels.h"])
     traffic = per_seq * wd.B if (per_seq is not None and wd.H == 16 and wd.N == 8192) else None
+    serving = run_serving(args, da, wd, y, lam, lam_init, dev, stream, peaks, kvb)
     return {"workload": f"decode {wd.B} seqs x 1 token, H{wd.H}, L{wd.N}, d{wd.d}, Dv{wd.Dv}, layer {wd.layer}",
             "ms_per_step": dms, "value": gbs, "unit": "GB/s", "kv_bytes_per_step": kvb,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "peak_kind": peak_kind,
                          "frac_of_spec_8tbs": gbs / 8000.0},
-            "gpu_launches_per_step": 2}
+            "gpu_launches_per_step": 2, "serving": serving}
+
+
+def run_serving(args, da, wd, y, lam, lam_init, dev, stream, peaks, kvb):
+    """The decode workload as a serving step over a paged KV cache: the same caches
+    scattered into shuffled 64-token pages; each step appends every sequence's new
+    token (position L-1) and decodes."""
+    B, H, L = wd.B, wd.H, wd.N
+    maxp = L // 64
+    g = torch.Generator(device="cpu").manual_seed(17)
+    table = torch.randperm(B * maxp, generator=g).view(B, maxp).to(torch.int32).to(dev)
+    pools = {}
+    for k in ("k1", "k2", "v"):
+        c = y[k]
+        pool = torch.empty(B * maxp, H, 64, c.shape[-1], dtype=c.dtype, device=dev)
+        pool[table.view(-1).long()] = c.view(B, H, maxp, 64, -1).permute(0, 2, 1, 3, 4).reshape(B * maxp, H, 64, -1)
+        pools[k] = pool
+    new = {k: y[k][:, :, L - 1].contiguous() for k in ("k1", "k2", "v")}
+    lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    out = torch.empty((B, H, wd.Dv), dtype=torch.bfloat16, device=dev)
+    ws = da.workspace(da.decode_workspace_bytes(B, H, L, wd.d, wd.Dv), dev)
+
+    def step():
+        da.diffattn_kv_append_paged(new["k1"], new["k2"], new["v"], pools["k1"], pools["k2"], pools["v"], table,
+                                    lens, stream=stream)
+        da.diffattn_decode_paged(y["q1"], y["q2"], pools["k1"], pools["k2"], pools["v"], table, lens, lam,
+                                 lam_init, L=L, eps=wd.eps, out_dtype=torch.bfloat16, out=out, ws=ws, stream=stream)
+
+    ms = time_device(step, args.steps, max(3, args.warmup), stream)
+    assert da.read_error(ws) == 0
+    gbs = kvb / (ms * 1e-3) / 1e9
+    del pools
+    return {"workload": f"decode {B} seqs, H{H}, L{L}: new token appended to a paged KV cache (64-token pages, "
+                        f"shuffled) then decoded", "ms_per_step": ms, "value": gbs, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "frac_of_spec_8tbs": gbs / 8000.0},
+            "gpu_launches_per_step": 3}
 
 
 def run_ours(args, rank: int, world: int, local_rank: int):

@@ -281,6 +281,86 @@ diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor 
     p.norm_w = norm_weight;
     p.B = B; p.H = H; p.d = d; p.Dv = Dv;
     p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
+    p.kv_group = 1;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.err = err_word(workspace);
+    p.part_stats = reinterpret_cast<float*>(ws + kControlBytes);
+    p.part_o = p.part_stats + (size_t)B * H * p.num_splits * 4;
+    return cuda_status(launch_decode_bf16(p, static_cast<cudaStream_t>(stream)));
+}
+
+diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new, const void* v_new,
+                                         diffattn_tensor k1_pages, diffattn_tensor k2_pages, diffattn_tensor v_pages,
+                                         const int32_t* block_table, int max_pages, int num_pages,
+                                         const int32_t* seq_lens, int B, int H_kv, int d, int Dv, void* stream) {
+    if (B < 0 || H_kv < 0 || d < 8 || Dv < 8 || (d % 8) || (Dv % 8) || max_pages < 1 || num_pages < 1)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B == 0 || H_kv == 0) return DIFFATTN_OK;
+    if (!k1_new || !k2_new || !v_new || !aligned16(k1_new) || !aligned16(k2_new) || !aligned16(v_new) ||
+        !block_table || !seq_lens)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (!check_operand(k1_pages, d, 2) || !check_operand(k2_pages, d, 2) || !check_operand(v_pages, Dv, 2))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (k1_pages.stride_b != k2_pages.stride_b || k1_pages.stride_h != k2_pages.stride_h ||
+        k1_pages.stride_n != k2_pages.stride_n)
+        return DIFFATTN_ERR_INVALID_ARG;
+    KvAppendParams p{};
+    p.k1_new = k1_new; p.k2_new = k2_new; p.v_new = v_new;
+    p.k1_pages = const_cast<void*>(k1_pages.ptr);
+    p.k2_pages = const_cast<void*>(k2_pages.ptr);
+    p.v_pages = const_cast<void*>(v_pages.ptr);
+    p.k_stride_page = k1_pages.stride_b; p.k_stride_h = k1_pages.stride_h; p.k_stride_row = k1_pages.stride_n;
+    p.v_stride_page = v_pages.stride_b; p.v_stride_h = v_pages.stride_h; p.v_stride_row = v_pages.stride_n;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.max_pages = max_pages; p.num_pages = num_pages;
+    p.B = B; p.H_kv = H_kv; p.d = d; p.Dv = Dv;
+    return cuda_status(launch_kv_append_paged(p, static_cast<cudaStream_t>(stream)));
+}
+
+diffattn_status diffattn_decode_paged(const void* q1, const void* q2, diffattn_tensor k1_pages,
+                                      diffattn_tensor k2_pages, diffattn_tensor v_pages, const int32_t* block_table,
+                                      int max_pages, int num_pages, const int32_t* seq_lens, int L, void* out,
+                                      const float* norm_weight, int B, int H, int kv_group, int d, int Dv,
+                                      float lambda, float lambda_init, float eps, int num_splits, int out_dtype,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || H < 0 || L < 1 || d < 1 || Dv < 1 || num_splits < 0 || num_splits > 256 || kv_group < 1 ||
+        max_pages < 1 || num_pages < 1)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if (!isfinite(lambda) || !isfinite(lambda_init) || !(eps >= 0.f) || !isfinite(eps))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0) return DIFFATTN_OK;
+    const int stage = decode_keys_per_stage(d);  // one page = one stage of keys
+    if (H % kv_group != 0 || L > (int64_t)stage * max_pages) return DIFFATTN_ERR_INVALID_ARG;
+    if (!q1 || !q2 || !aligned16(q1) || !aligned16(q2) || !out || !aligned16(out) || !block_table || !seq_lens)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (!check_operand(k1_pages, d, 2) || !check_operand(k2_pages, d, 2) || !check_operand(v_pages, Dv, 2))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (norm_weight != nullptr && !aligned16(norm_weight)) return DIFFATTN_ERR_INVALID_ARG;
+    if (!((d == 64 && Dv == 128) || (d == 128 && Dv == 256))) return DIFFATTN_ERR_UNSUPPORTED;
+    DecodeParams p{};
+    decode_geometry(B, H, L, d, num_splits, &p.num_splits, &p.keys_per_split);
+    const size_t need = decode_ws_bytes(B, H, p.num_splits, Dv);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DIFFATTN_ERR_WORKSPACE;
+    const int H_kv = H / kv_group;
+    if (!encode_4d(&p.tm_k1, k1_pages, d, stage, H_kv, num_pages, 64, stage, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_4d(&p.tm_k2, k2_pages, d, stage, H_kv, num_pages, 64, stage, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_4d(&p.tm_v, v_pages, Dv, stage, H_kv, num_pages, Dv, stage, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return DIFFATTN_ERR_INVALID_ARG;
+    p.q1 = q1;
+    p.q2 = q2;
+    p.seq_lens = seq_lens;
+    p.L = L;
+    p.out = out;
+    p.out_bf16 = out_dtype == DIFFATTN_BF16;
+    p.norm_w = norm_weight;
+    p.B = B; p.H = H; p.d = d; p.Dv = Dv;
+    p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
+    p.block_table = block_table;
+    p.max_pages = max_pages;
+    p.kv_group = kv_group;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.err = err_word(workspace);
     p.part_stats = reinterpret_cast<float*>(ws + kControlBytes);

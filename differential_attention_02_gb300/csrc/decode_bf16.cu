@@ -86,19 +86,29 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
             tma_prefetch_desc(&p.tm_k1);
             tma_prefetch_desc(&p.tm_k2);
             tma_prefetch_desc(&p.tm_v);
+            const int hk = h / p.kv_group;  // the KV head this query head reads
+            // Paged cache: stage t is the sequence's page key / 64; its physical page is
+            // read from the block table one stage ahead, off the path to the copy.
+            const int32_t* pages = p.block_table ? p.block_table + (int64_t)b * p.max_pages : nullptr;
+            int next_page = (pages && n_stages > 0) ? pages[key_begin / kStageKeys] : 0;
             int t = 0;
             for (; t < n_stages; ++t) {
                 const int s = t % C::kStages;
+                const int page = next_page;
+                if (pages && t + 1 < n_stages) next_page = pages[key_begin / kStageKeys + t + 1];
                 if (!mbar_wait(&empty[s], ((t / C::kStages) & 1) ^ 1, abort_flag, p.err, 0x11)) break;
                 uint8_t* st = stages + s * C::kStageBytes;
-                const int key = key_begin + t * kStageKeys;
+                // Coordinates (row, batch) of the stage: (key, b) in a contiguous cache,
+                // (0, page) in a paged one.
+                const int row = pages ? 0 : key_begin + t * kStageKeys;
+                const int bz = pages ? page : b;
                 mbar_arrive_expect_tx(&full[s], C::kStageBytes);
 #pragma unroll
                 for (int x = 0; x < C::kBoxesK; ++x) {
-                    tma_load_4d(st + x * kStageKeys * 128, &p.tm_k1, &full[s], x * 64, key, h, b);
-                    tma_load_4d(st + C::kKBytes + x * kStageKeys * 128, &p.tm_k2, &full[s], x * 64, key, h, b);
+                    tma_load_4d(st + x * kStageKeys * 128, &p.tm_k1, &full[s], x * 64, row, hk, bz);
+                    tma_load_4d(st + C::kKBytes + x * kStageKeys * 128, &p.tm_k2, &full[s], x * 64, row, hk, bz);
                 }
-                tma_load_4d(st + 2 * C::kKBytes, &p.tm_v, &full[s], 0, key, h, b);
+                tma_load_4d(st + 2 * C::kKBytes, &p.tm_v, &full[s], 0, row, hk, bz);
             }
             // Do not leave while copies into this CTA's shared memory may still land.
             for (int u = max(0, t - C::kStages); u < t; ++u)
@@ -311,9 +321,46 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Appends each sequence's new token (K1, K2, V rows of every KV head) to a paged
+// cache: position pos = seq_lens[b] - 1 goes to row pos % 64 of page
+// block_table[b][pos / 64]. One warp per (sequence, KV head), 16-byte copies.
+// Positions or pages outside the table or the pool are skipped.
+__global__ void kv_append_paged_kernel(const __grid_constant__ KvAppendParams p) {
+    const int b = blockIdx.x / p.H_kv, h = blockIdx.x % p.H_kv;
+    const int pos = p.seq_lens[b] - 1;
+    if (pos < 0 || pos / kStageKeys >= p.max_pages) return;
+    const int page = p.block_table[(int64_t)b * p.max_pages + pos / kStageKeys];
+    if (page < 0 || page >= p.num_pages) return;
+    const int row = pos % kStageKeys;
+    const int64_t src_k = ((int64_t)b * p.H_kv + h) * p.d, src_v = ((int64_t)b * p.H_kv + h) * p.Dv;
+    const int64_t dst_k = page * p.k_stride_page + h * p.k_stride_h + row * p.k_stride_row;
+    const int64_t dst_v = page * p.v_stride_page + h * p.v_stride_h + row * p.v_stride_row;
+    const int ck = p.d / 8, cv = p.Dv / 8;  // 16-byte chunks per row
+    for (int c = threadIdx.x; c < 2 * ck + cv; c += blockDim.x) {
+        const uint4* src;
+        uint4* dst;
+        if (c < ck) {
+            src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.k1_new) + src_k) + c;
+            dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.k1_pages) + dst_k) + c;
+        } else if (c < 2 * ck) {
+            src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.k2_new) + src_k) + (c - ck);
+            dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.k2_pages) + dst_k) + (c - ck);
+        } else {
+            src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v_new) + src_v) + (c - 2 * ck);
+            dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.v_pages) + dst_v) + (c - 2 * ck);
+        }
+        *dst = *src;
+    }
+}
+
 }  // namespace
 
 int decode_keys_per_stage(int) { return kStageKeys; }
+
+cudaError_t launch_kv_append_paged(const KvAppendParams& p, cudaStream_t stream) {
+    kv_append_paged_kernel<<<p.B * p.H_kv, 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream) {
     if (p.d == 64 && p.Dv == 128) return launch_t<64, 128>(p, stream);

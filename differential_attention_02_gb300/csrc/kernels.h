@@ -28,7 +28,7 @@ cudaError_t launch_fwd_simt_f32(const SimtF32Params& p, cudaStream_t stream);
 
 // bf16 split-KV decode (+ merge).
 struct DecodeParams {
-    CUtensorMap tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H, L, width]
+    CUtensorMap tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H_kv, L, width], or [pages, H_kv, 64, width] when paged
     const void* q1;                  // [B, H, d] bf16
     const void* q2;
     const int32_t* seq_lens;  // [B] or null
@@ -41,8 +41,25 @@ struct DecodeParams {
     float* part_stats;  // [B*H*S][4]
     float* part_o;      // [B*H*S][2][Dv]
     int32_t* err;
+    const int32_t* block_table;  // [B][max_pages] physical page of each 64-token page, or null (contiguous cache)
+    int max_pages;
+    int kv_group;  // query heads per KV head (query head h reads KV head h / kv_group)
 };
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream);
+struct KvAppendParams {
+    const void* k1_new;  // [B, H_kv, d] bf16, contiguous
+    const void* k2_new;
+    const void* v_new;   // [B, H_kv, Dv] bf16, contiguous
+    void* k1_pages;      // [pages, H_kv, 64, d]: element strides below
+    void* k2_pages;
+    void* v_pages;
+    int64_t k_stride_page, k_stride_h, k_stride_row;  // shared by k1_pages and k2_pages
+    int64_t v_stride_page, v_stride_h, v_stride_row;
+    const int32_t* block_table;  // [B][max_pages]
+    const int32_t* seq_lens;     // [B]: the new token is at position seq_lens[b] - 1
+    int max_pages, num_pages, B, H_kv, d, Dv;
+};
+cudaError_t launch_kv_append_paged(const KvAppendParams& p, cudaStream_t stream);
 int decode_keys_per_stage(int d);
 
 // bf16 GEMM on tcgen05: C = A * W.

@@ -192,6 +192,62 @@ diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2,
                                         int num_splits, int out_dtype, void* stream);
 
 /*
+ * diffattn_decode_paged — diffattn_decode against a paged KV cache, with query
+ * heads optionally sharing KV heads (grouped-query attention). Same
+ * computation, kernels and split geometry as diffattn_decode; only where each
+ * key's K1, K2 and V rows are read from changes. The pages name the KV cache
+ * read at every decoding step as the decode cost ("Tag: Attention Mechanism",
+ * priorstack.com, Multi-Head Latent Attention article) and mention GQA
+ * (hada page, Hacker News discussion); paging and sharing are serving layouts,
+ * not part of the method.
+ *
+ * k1_pages, k2_pages: [num_pages, H_kv, 64, d] bf16; v_pages: [num_pages, H_kv,
+ *   64, Dv] bf16 (a page holds 64 consecutive tokens of one sequence for every
+ *   KV head; stride_b of the tensors is the page stride, stride_n the token
+ *   stride within a page; last dimension contiguous).
+ * block_table: device int32 [B, max_pages]; block_table[b * max_pages + i] is
+ *   the physical page holding tokens 64i .. 64i+63 of sequence b, for every i
+ *   < ceil(seq_lens[b] / 64). Entries outside [0, num_pages) are not checked
+ *   on the device: they read zeros (the copy engine fills out-of-range tiles)
+ *   and give a wrong result, never a memory fault.
+ * seq_lens: device int32 [B], required; clamped to [0, L] as in diffattn_decode.
+ * L: the largest sequence length (<= 64 * max_pages); sizes the split geometry.
+ * H: query heads; kv_group >= 1 divides H, and query head h reads KV head
+ *   h / kv_group (H_kv = H / kv_group).
+ * Other arguments, the workspace (diffattn_decode_workspace_size with the same
+ * B, H, L, d, Dv, num_splits) and errors: as diffattn_decode.
+ */
+diffattn_status diffattn_decode_paged(const void* q1, const void* q2,
+                                      diffattn_tensor k1_pages, diffattn_tensor k2_pages, diffattn_tensor v_pages,
+                                      const int32_t* block_table, int max_pages, int num_pages,
+                                      const int32_t* seq_lens, int L,
+                                      void* out, const float* norm_weight,
+                                      int B, int H, int kv_group, int d, int Dv,
+                                      float lambda, float lambda_init, float eps,
+                                      int num_splits, int out_dtype,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * diffattn_kv_append_paged — writes each sequence's new token into a paged KV
+ * cache (the layout of diffattn_decode_paged) before the decode step that
+ * attends to it: for every sequence b and KV head h, the rows k1_new[b, h],
+ * k2_new[b, h] and v_new[b, h] go to row pos % 64 of page
+ * block_table[b * max_pages + pos / 64], where pos = seq_lens[b] - 1 (the new
+ * token is the last of its sequence, as in the decode calls). A plain copy,
+ * bit-exact; a sequence whose position or page falls outside the table or the
+ * pool is skipped.
+ *
+ * k1_new, k2_new: [B, H_kv, d] bf16, v_new: [B, H_kv, Dv] bf16, contiguous and
+ *   16-byte aligned. k1_pages and k2_pages must share their strides.
+ * block_table, seq_lens: device int32, as for diffattn_decode_paged.
+ * d and Dv multiples of 8. B or H_kv equal to 0: returns DIFFATTN_OK.
+ */
+diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new, const void* v_new,
+                                         diffattn_tensor k1_pages, diffattn_tensor k2_pages, diffattn_tensor v_pages,
+                                         const int32_t* block_table, int max_pages, int num_pages,
+                                         const int32_t* seq_lens, int B, int H_kv, int d, int Dv, void* stream);
+
+/*
  * diffattn_gemm_bf16 — C[M, N] = A[M, K] . W[K, N], bf16 operands, fp32
  * accumulation, tcgen05 tensor cores. The module's projections: [Q|K|V] = X W
  * and Y = concat(heads) W_O ("A Simple Principle From Noise-Cancelling

@@ -127,6 +127,36 @@ def test_decode_and_gemm_argument_validation(lib):
     assert g(N=250) == da.ERR_INVALID_ARG
 
 
+def test_paged_decode_argument_validation(lib):
+    t = _tensor(sb=2 * 64 * 64, sh=64 * 64, sn=64)  # [pages, H_kv=2, 64, 64]
+    vp = ctypes.c_void_p
+    call = lambda **kw: lib.diffattn_decode_paged(
+        vp(0x1000), vp(0x1000), t, t, _tensor(sb=2 * 64 * 128, sh=64 * 128, sn=128),
+        None if kw.get("table", 1) is None else vp(0x3000), kw.get("max_pages", 4), 8,
+        None if kw.get("lens", 1) is None else vp(0x3100), kw.get("L", 200), vp(0x2000), None, kw.get("B", 2),
+        kw.get("H", 2), kw.get("g", 1), 64, 128, 0.5, 0.2, 1e-5, 0, da.F32, vp(0x4000), kw.get("wsb", 1 << 20), None)
+    assert call(B=0) == da.OK
+    assert call(g=0) == da.ERR_INVALID_ARG
+    assert call(H=2, g=3) == da.ERR_INVALID_ARG        # kv_group must divide H
+    assert call(L=300) == da.ERR_INVALID_ARG           # more than 64 * max_pages tokens
+    assert call(table=None) == da.ERR_INVALID_ARG
+    assert call(lens=None) == da.ERR_INVALID_ARG        # lengths are required with pages
+    assert call(wsb=256) == da.ERR_WORKSPACE
+
+
+def test_kv_append_argument_validation(lib):
+    t = _tensor(sb=2 * 64 * 64, sh=64 * 64, sn=64)
+    vp = ctypes.c_void_p
+    call = lambda **kw: lib.diffattn_kv_append_paged(
+        vp(kw.get("k1", 0x1000)), vp(0x1000), vp(0x1000), t, kw.get("k2", t), _tensor(sb=2 * 64 * 128, sh=64 * 128,
+        sn=128), vp(0x3000), 4, 8, vp(0x3100), kw.get("B", 2), 2, kw.get("d", 64), 128, None)
+    assert call(B=0) == da.OK
+    assert call(k1=0) == da.ERR_INVALID_ARG
+    assert call(k1=0x1004) == da.ERR_INVALID_ARG                 # not 16-byte aligned
+    assert call(d=60) == da.ERR_INVALID_ARG                      # rows are copied in 16-byte chunks
+    assert call(k2=_tensor(sb=4 * 64 * 64, sh=64 * 64, sn=64)) == da.ERR_INVALID_ARG  # K1/K2 strides differ
+
+
 def test_python_binding_refuses_without_library(tmp_path):
     saved = da._lib
     da._lib = None
