@@ -38,6 +38,12 @@ Readings where the pages are silent (each also listed in the design notes):
 * Module projections: Q = X W with W stored [d_in, d_out]; inside head i the
   first d channels of its 2d-wide Q (and K) slice are Q_i1, the next d are Q_i2;
   V channels [i*Dv, (i+1)*Dv) belong to head i.
+* Layer (intoai, "The Overall Architecture Of The Multi-Head Differential
+  Transformer"; hada, "Estrutura multi-head e arquitetura completa"): the pages
+  give Y = MultiHead(LN(X)) + X and X' = SwiGLU(LN(Y)) + Y with pre-RMSNorm "as
+  in LLaMA". Readings: LN is RMSNorm over d_model, y = x / sqrt(mean(x^2) + eps)
+  * g with eps = 1e-5 and an optional gain g; SwiGLU(x) is the LLaMA FFN
+  (SiLU(x W_gate) * (x W_up)) W_down with SiLU(t) = t / (1 + e^-t).
 """
 
 from __future__ import annotations
@@ -56,6 +62,10 @@ __all__ = [
     "diffattn_fwd",
     "diffattn_decode",
     "module_fwd",
+    "rmsnorm_rows",
+    "silu",
+    "swiglu_ffn",
+    "layer_fwd",
 ]
 
 
@@ -234,3 +244,41 @@ def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float,
                                   vv[b, :, Dv * i: Dv * (i + 1)], lam, causal)
             cat[b, :, Dv * i: Dv * (i + 1)] = head_rmsnorm_scale(o_hat, lam_init, eps, weight)
     return cat @ w_o
+
+
+# --------------------------------------------------------------------------
+# The layer around the module ("The Overall Architecture Of The Multi-Head
+# Differential Transformer"; "Estrutura multi-head e arquitetura completa")
+# --------------------------------------------------------------------------
+
+def rmsnorm_rows(x, eps: float = 1e-5, weight=None) -> np.ndarray:
+    """Pre-RMSNorm over the last axis: x / sqrt(mean(x^2) + eps), times the gain if given."""
+    x = _f64(x)
+    y = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return y if weight is None else y * _f64(weight).reshape(-1)
+
+
+def silu(t) -> np.ndarray:
+    """SiLU(t) = t / (1 + e^-t)."""
+    t = _f64(t)
+    return t / (1.0 + np.exp(-t))
+
+
+def swiglu_ffn(x, w_gate, w_up, w_down) -> np.ndarray:
+    """The LLaMA feed-forward block: (SiLU(x W_gate) * (x W_up)) W_down."""
+    x, w_gate, w_up, w_down = (_f64(a) for a in (x, w_gate, w_up, w_down))
+    return (silu(x @ w_gate) * (x @ w_up)) @ w_down
+
+
+def layer_fwd(x, w_q, w_k, w_v, w_o, w_gate, w_up, w_down, n_heads: int, lam: float, lam_init: float,
+              eps: float = 1e-5, norm1_weight=None, norm2_weight=None, head_weight=None,
+              causal: bool = True) -> np.ndarray:
+    """One DIFF Transformer layer: Y = MultiHead(RMSNorm(X)) + X, then SwiGLU(RMSNorm(Y)) + Y.
+
+    x: [B, N, d_model]; the module weights as in module_fwd; w_gate, w_up: [d_model, d_ff];
+    w_down: [d_ff, d_model]. The head RMSNorm uses `eps` and `head_weight`.
+    """
+    x = _f64(x)
+    y = x + module_fwd(rmsnorm_rows(x, eps, norm1_weight), w_q, w_k, w_v, w_o, n_heads, lam, lam_init, eps,
+                       head_weight, causal)
+    return y + swiglu_ffn(rmsnorm_rows(y, eps, norm2_weight), w_gate, w_up, w_down)

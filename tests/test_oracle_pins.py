@@ -309,3 +309,69 @@ def test_module_projection_orientation_and_output_linearity():
                                   xv[b, :, Dv * i: Dv * (i + 1)], 0.5)
             np.testing.assert_allclose(y_cat[b, :, Dv * i: Dv * (i + 1)], orc.head_rmsnorm_scale(o, 0.2),
                                        atol=1e-12)
+
+
+# ------------------------------------------------------------------ the layer around the module
+def test_silu_matches_library_sigmoid():
+    from scipy.special import expit
+    t = np.linspace(-30, 30, 2001)
+    np.testing.assert_allclose(orc.silu(t), t * expit(t), rtol=1e-14, atol=1e-300)
+
+
+def test_rmsnorm_rows_has_closed_form_rms():
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(7, 64)) * rng.uniform(0.01, 10, size=(7, 1))
+    eps = 1e-5
+    y = orc.rmsnorm_rows(x, eps)
+    ms = np.mean(x * x, axis=1)
+    np.testing.assert_allclose(np.mean(y * y, axis=1), ms / (ms + eps), rtol=1e-12)
+    g = rng.uniform(0.5, 2, size=64)
+    np.testing.assert_allclose(orc.rmsnorm_rows(x, eps, g), y * g, rtol=1e-14)
+
+
+def test_swiglu_ffn_matches_torch_float64():
+    import torch
+    rng = np.random.default_rng(4)
+    x, wg, wu, wd = rng.normal(size=(5, 16)), rng.normal(size=(16, 24)), rng.normal(size=(16, 24)), \
+        rng.normal(size=(24, 16))
+    T = lambda a: torch.from_numpy(a)
+    want = (torch.nn.functional.silu(T(x) @ T(wg)) * (T(x) @ T(wu))) @ T(wd)
+    np.testing.assert_allclose(orc.swiglu_ffn(x, wg, wu, wd), want.numpy(), rtol=1e-12)
+
+
+def _layer_weights(rng, dm, h, d, dff):
+    w = lambda *s: rng.normal(size=s) / np.sqrt(s[0])
+    return dict(w_q=w(dm, 2 * d * h), w_k=w(dm, 2 * d * h), w_v=w(dm, 2 * d * h), w_o=w(2 * d * h, dm),
+                w_gate=w(dm, dff), w_up=w(dm, dff), w_down=w(dff, dm))
+
+
+def test_layer_residual_branches():
+    """With zero output weights in both branches the layer is the identity; with only the FFN's
+    output weights zero it is X + module(RMSNorm(X))."""
+    rng = np.random.default_rng(5)
+    dm, h, d, dff = 32, 2, 8, 48
+    x = rng.normal(size=(1, 6, dm))
+    w = _layer_weights(rng, dm, h, d, dff)
+    zero = dict(w, w_o=np.zeros_like(w["w_o"]), w_down=np.zeros_like(w["w_down"]))
+    np.testing.assert_array_equal(orc.layer_fwd(x, **zero, n_heads=h, lam=0.4, lam_init=0.2), x)
+    only_attn = dict(w, w_down=np.zeros_like(w["w_down"]))
+    want = x + orc.module_fwd(orc.rmsnorm_rows(x), w["w_q"], w["w_k"], w["w_v"], w["w_o"], h, 0.4, 0.2)
+    np.testing.assert_allclose(orc.layer_fwd(x, **only_attn, n_heads=h, lam=0.4, lam_init=0.2), want, rtol=1e-13)
+
+
+def test_layer_ffn_branch_matches_torch_rms_norm():
+    """With the attention output weights zero, the layer is X + FFN(RMSNorm(X)); RMSNorm and
+    the FFN evaluated with torch's own float64 rms_norm and silu."""
+    import torch
+    F = torch.nn.functional
+    rng = np.random.default_rng(6)
+    dm, h, d, dff = 32, 2, 8, 48
+    x = rng.normal(size=(2, 5, dm))
+    w = _layer_weights(rng, dm, h, d, dff)
+    g2 = rng.uniform(0.5, 1.5, size=dm)
+    got = orc.layer_fwd(x, **dict(w, w_o=np.zeros_like(w["w_o"])), n_heads=h, lam=0.4, lam_init=0.2,
+                        norm2_weight=g2)
+    T = lambda a: torch.from_numpy(a)
+    n = F.rms_norm(T(x), (dm,), T(g2), eps=1e-5)
+    want = T(x) + (F.silu(n @ T(w["w_gate"])) * (n @ T(w["w_up"]))) @ T(w["w_down"])
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-11, atol=1e-12)
