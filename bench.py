@@ -346,6 +346,36 @@ def run_module(args, da, gi, dev, stream, peaks, peak_kind):
             "gpu_launches_per_step": 5}
 
 
+def run_layer(args, da, gi, dev, stream, peaks, peak_kind):
+    """One DIFF Transformer layer on X [2,4096,2048]: pre-RMSNorm, the module above,
+    residual add + RMSNorm, the SwiGLU FFN (d_ff 5632, gate and up in one GEMM) and the
+    second residual add."""
+    w = gi.WORKLOADS["layer_bf16"]
+    # Weights as fp16 copies of the bf16 draws (exact above 2^-14 in magnitude; the ~0.3% of
+    # smaller values move by at most 2^-25), so the GEMM operands are fp16 as well.
+    t = {k: (v.to(dev).half() if k.startswith("w_") else v.to(dev)) for k, v in gi.layer_inputs(w).items()}
+    wgu = torch.cat([t.pop("w_gate"), t.pop("w_up")], dim=1).contiguous()
+    lv = gi.lambda_vectors(w)
+    lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+    ws = da.workspace(256, dev)
+    fn = lambda: da.layer_fwd(t["x"], t["w_q"], t["w_k"], t["w_v"], t["w_o"], wgu, t["w_down"], w.H, lam, lam_init,
+                              w.eps, ws=ws, stream=stream)
+    ms = time_device(fn, max(3, args.steps // 4), args.warmup, stream)
+    assert da.read_error(ws) == 0
+    n_pairs = w.N * (w.N + 1) / 2
+    att = w.B * w.H * (4 * n_pairs * w.d + 2 * n_pairs * w.Dv)
+    M = w.B * w.N
+    gemm = 2.0 * M * w.d_model * (2 * w.H * 2 * w.d + w.H * w.Dv) + 2.0 * M * w.H * w.Dv * w.d_model
+    ffn = 6.0 * M * w.d_model * w.d_ff
+    tf = (att + gemm + ffn) / (ms * 1e-3) / 1e12
+    return {"workload": "layer X[2,4096,2048], h8 d128 Dv256, SwiGLU d_ff 5632, causal, layer 1; fp16 copies of "
+                        "bf16 weights, fp16 GEMM operands, fp32 residual stream",
+            "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "flops_per_step": att + gemm + ffn,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 burst"},
+            "gpu_launches_per_step": 11}
+
+
 def run_decode(args, da, gi, dev, stream, peaks, peak_kind):
     """Times the split-KV decode (split kernel + merge kernel) on the decode workload."""
     import dataclasses
@@ -495,6 +525,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if not args.skip_extra:
         extra["long_prefill"] = run_long_prefill(args, da, gi, dev, stream, peaks, peak_kind)
         extra["module"] = run_module(args, da, gi, dev, stream, peaks, peak_kind)
+        extra["layer"] = run_layer(args, da, gi, dev, stream, peaks, peak_kind)
     if rank != 0:
         return
     cpu = None

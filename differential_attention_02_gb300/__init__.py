@@ -20,9 +20,10 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = ran
 F32, BF16, F16 = 0, 1, 2
 
 EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_workspace_size",
-            "diffattn_decode", "diffattn_decode_workspace_size", "diffattn_gemm_bf16",
+            "diffattn_decode", "diffattn_decode_workspace_size", "diffattn_gemm_bf16", "diffattn_gemm_f16",
             "diffattn_gemm_workspace_size", "diffattn_read_error", "diffattn_decode_noalloc",
-            "diffattn_decode_paged", "diffattn_kv_append_paged", "diffattn_selftest_timeout")
+            "diffattn_decode_paged", "diffattn_kv_append_paged", "diffattn_add_rmsnorm", "diffattn_swiglu",
+            "diffattn_selftest_timeout")
 
 
 class DiffAttnError(RuntimeError):
@@ -66,6 +67,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_decode_workspace_size.argtypes = [i32] * 6 + [ctypes.POINTER(sz)]
     lib.diffattn_gemm_bf16.restype = i32
     lib.diffattn_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i64, i32, vp, sz, vp]
+    lib.diffattn_gemm_f16.restype = i32
+    lib.diffattn_gemm_f16.argtypes = lib.diffattn_gemm_bf16.argtypes
     lib.diffattn_gemm_workspace_size.restype = i32
     lib.diffattn_gemm_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
     lib.diffattn_decode_noalloc.restype = i32
@@ -77,6 +80,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_kv_append_paged.restype = i32
     lib.diffattn_kv_append_paged.argtypes = [vp, vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, i32, vp, i32, i32, i32,
                                              i32, vp]
+    lib.diffattn_add_rmsnorm.restype = i32
+    lib.diffattn_add_rmsnorm.argtypes = [vp, i32, vp, vp, vp, i32, vp, i32, i32, f32, vp]
+    lib.diffattn_swiglu.restype = i32
+    lib.diffattn_swiglu.argtypes = [vp, vp, i32, i32, i32, vp]
     lib.diffattn_selftest_timeout.restype = i32
     lib.diffattn_selftest_timeout.argtypes = [vp, sz, vp]
     lib.diffattn_read_error.restype = i32
@@ -253,20 +260,76 @@ def diffattn_kv_append_paged(k1_new, k2_new, v_new, k1_pages, k2_pages, v_pages,
         "diffattn_kv_append_paged")
 
 
-def gemm_bf16(a: torch.Tensor, w: torch.Tensor, out_dtype=torch.bfloat16, out=None, ws=None, stream=None):
-    """C = a @ w with a [M,K] and w [K,N] bf16 row-major (unit last stride); C fp32, bf16 or fp16."""
+def add_rmsnorm(x, z=None, weight=None, eps: float = 1e-5, want_y: bool = False, want_n: bool = True,
+                n_dtype=torch.bfloat16, stream=None):
+    """Row-wise y = x + z and n = RMSNorm(y) * weight over the last dimension.
+    x [.., N] bf16 or fp32, z fp32 or None. Returns (y fp32 or None, n of n_dtype
+    (bf16 or fp16) or None)."""
+    N = x.shape[-1]
+    M = x.numel() // N
+    y = torch.empty(x.shape, dtype=torch.float32, device=x.device) if want_y else None
+    n = torch.empty(x.shape, dtype=n_dtype, device=x.device) if want_n else None
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    _check(load_library().diffattn_add_rmsnorm(
+        ptr(x), F32 if x.dtype == torch.float32 else BF16, ptr(z), ptr(y), ptr(n), _dtype_code(n_dtype), ptr(weight),
+        M, N, float(eps), _stream_ptr(stream)), "diffattn_add_rmsnorm")
+    return y, n
+
+
+def swiglu(gate_up, out_dtype=torch.bfloat16, stream=None):
+    """h = SiLU(g) * u for rows [g | u] of gate_up ([M, 2H] fp16). Returns [M, H] of out_dtype."""
+    M, H2 = gate_up.shape
+    h = torch.empty((M, H2 // 2), dtype=out_dtype, device=gate_up.device)
+    _check(load_library().diffattn_swiglu(ctypes.c_void_p(gate_up.data_ptr()), ctypes.c_void_p(h.data_ptr()),
+                                          _dtype_code(out_dtype), M, H2 // 2, _stream_ptr(stream)),
+           "diffattn_swiglu")
+    return h
+
+
+def layer_fwd(x, w_q, w_k, w_v, w_o, w_gate_up, w_down, n_heads: int, lam: float, lam_init: float,
+              eps: float = 1e-5, norm1_weight=None, norm2_weight=None, head_weight=None, ws=None, stream=None):
+    """One DIFF Transformer layer: Y = MultiHead(RMSNorm(X)) + X, X' = SwiGLU(RMSNorm(Y)) + Y.
+
+    x: [B, N, d_model] bf16 or fp32; module weights as in module_fwd; w_gate_up: [d_model, 2*d_ff]
+    = [W_gate | W_up]; w_down: [d_ff, d_model]; every weight bf16, or every weight fp16, and the
+    GEMM operands (the RMSNorm outputs, the attention output, the SwiGLU output) take that type;
+    norm weights fp32 [d_model], head_weight fp32 [Dv] (the per-head RMSNorm's gain). Returns
+    X' [B, N, d_model] fp32 (the residual stream is kept in fp32; the gate/up output is fp16)."""
+    B, N, dm = x.shape
+    M = B * N
+    op = w_q.dtype
+    _, n1 = add_rmsnorm(x, weight=norm1_weight, eps=eps, n_dtype=op, stream=stream)
+    a = module_fwd(n1, w_q, w_k, w_v, w_o, n_heads, lam, lam_init, eps, norm_weight=head_weight, ws=ws,
+                   stream=stream, out_dtype=torch.float32)
+    y, n2 = add_rmsnorm(x, a, weight=norm2_weight, eps=eps, want_y=True, n_dtype=op, stream=stream)
+    gu = gemm(n2.view(M, dm), w_gate_up, out_dtype=torch.float16, ws=ws, stream=stream)
+    h = swiglu(gu, out_dtype=op, stream=stream)
+    f = gemm(h, w_down, out_dtype=torch.float32, ws=ws, stream=stream)
+    out, _ = add_rmsnorm(y, f.view(B, N, dm), eps=eps, want_y=True, want_n=False, stream=stream)
+    return out
+
+
+def gemm(a: torch.Tensor, w: torch.Tensor, out_dtype=torch.bfloat16, out=None, ws=None, stream=None):
+    """C = a @ w with a [M,K] and w [K,N] row-major (unit last stride), both bf16 or both fp16;
+    C fp32, bf16 or fp16."""
     M, K = a.shape
     K2, N = w.shape
     if K2 != K or a.stride(1) != 1 or w.stride(1) != 1:
         raise ValueError("a [M,K] and w [K,N] with contiguous rows")
+    if a.dtype != w.dtype or a.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("a and w must both be bf16 or both fp16")
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
     ws = workspace(256, a.device) if ws is None else ws
-    _check(load_library().diffattn_gemm_bf16(
+    name = "diffattn_gemm_f16" if a.dtype == torch.float16 else "diffattn_gemm_bf16"
+    _check(getattr(load_library(), name)(
         ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(out.data_ptr()), M, N, K,
         a.stride(0), w.stride(0), out.stride(0), _dtype_code(out.dtype), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
-        _stream_ptr(stream)), "diffattn_gemm_bf16")
+        _stream_ptr(stream)), name)
     return out
+
+
+gemm_bf16 = gemm
 
 
 def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float, eps: float = 1e-5,
@@ -275,26 +338,26 @@ def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float,
     attention reading Q/K/V in place through strided views, and the W_O GEMM.
 
     x [B,N,d_model]; w_q, w_k [d_model, h*2d]; w_v [d_model, h*Dv]; w_o [h*Dv, d_model],
-    all bf16. Head i uses Q[..., 2di:2di+d] as Q1 and Q[..., 2di+d:2d(i+1)] as Q2
+    all bf16 or all fp16. Head i uses Q[..., 2di:2di+d] as Q1 and Q[..., 2di+d:2d(i+1)] as Q2
     (K likewise). The projections are written in fp16 (bf16 rounding of Q, K and V
     alone would cost about 3e-3 relative error at the output); the attention output
-    that W_O multiplies is bf16.
+    that W_O multiplies has the operands' type.
     """
     B, N, dm = x.shape
     h = n_heads
     d = w_q.shape[1] // (2 * h)
     Dv = w_v.shape[1] // h
     x2 = x.reshape(B * N, dm)
-    q = gemm_bf16(x2, w_q, out_dtype=torch.float16, ws=ws, stream=stream)
-    k = gemm_bf16(x2, w_k, out_dtype=torch.float16, ws=ws, stream=stream)
-    v = gemm_bf16(x2, w_v, out_dtype=torch.float16, ws=ws, stream=stream)
+    q = gemm(x2, w_q, out_dtype=torch.float16, ws=ws, stream=stream)
+    k = gemm(x2, w_k, out_dtype=torch.float16, ws=ws, stream=stream)
+    v = gemm(x2, w_v, out_dtype=torch.float16, ws=ws, stream=stream)
     # [B*N, h*2d] -> [B, h, N, 2d] views (no copies): strides (N*h*2d, 2d, h*2d, 1)
     q4 = q.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
     k4 = k.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
     v4 = v.view(B, N, h, Dv).permute(0, 2, 1, 3)
     att = diffattn_fwd(q4[..., :d], q4[..., d:], k4[..., :d], k4[..., d:], v4, lam, lam_init, eps, norm_weight,
-                       out_dtype=torch.bfloat16, ws=ws, stream=stream)
-    y = gemm_bf16(att.view(B * N, h * Dv), w_o, out_dtype=out_dtype, ws=ws, stream=stream)
+                       out_dtype=x.dtype, ws=ws, stream=stream)
+    y = gemm(att.view(B * N, h * Dv), w_o, out_dtype=out_dtype, ws=ws, stream=stream)
     return y.view(B, N, dm)
 
 

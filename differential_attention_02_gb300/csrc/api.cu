@@ -69,14 +69,16 @@ bool encode_out_3d(CUtensorMap* m, void* ptr, int W, int N, int B, int elem_byte
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_2d(CUtensorMap* m, const void* ptr, int inner, int outer, int64_t ld, int box_inner, int box_outer) {
+bool encode_2d(CUtensorMap* m, const void* ptr, int inner, int outer, int64_t ld, int box_inner, int box_outer,
+               bool f16) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
     cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
     cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
     cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+    return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+               dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -175,7 +177,8 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
                              int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
     if (B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
     if ((in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16 && in_dtype != DIFFATTN_F16) ||
-        (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16))
+        (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16 && out_dtype != DIFFATTN_F16) ||
+        (in_dtype == DIFFATTN_F32 && out_dtype == DIFFATTN_F16))
         return DIFFATTN_ERR_INVALID_ARG;
     if (!isfinite(lambda) || !isfinite(lambda_init) || !(eps >= 0.f) || !isfinite(eps))
         return DIFFATTN_ERR_INVALID_ARG;
@@ -227,6 +230,7 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     p.in_f16 = in_dtype == DIFFATTN_F16;
     p.out = out;
     p.out_bf16 = out_dtype == DIFFATTN_BF16;
+    p.out_f16 = out_dtype == DIFFATTN_F16;
     p.norm_w = norm_weight;
     p.B = B; p.H = H; p.N = N; p.d = d; p.Dv = Dv; p.causal = causal != 0;
     p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
@@ -287,6 +291,35 @@ diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor 
     p.part_stats = reinterpret_cast<float*>(ws + kControlBytes);
     p.part_o = p.part_stats + (size_t)B * H * p.num_splits * 4;
     return cuda_status(launch_decode_bf16(p, static_cast<cudaStream_t>(stream)));
+}
+
+diffattn_status diffattn_add_rmsnorm(const void* x, int x_dtype, const float* z, float* y_out, void* n_out,
+                                     int n_dtype, const float* weight, int M, int N, float eps, void* stream) {
+    if (M < 0 || N < 8 || N % 8 || (x_dtype != DIFFATTN_F32 && x_dtype != DIFFATTN_BF16)) return DIFFATTN_ERR_INVALID_ARG;
+    if (n_dtype != DIFFATTN_BF16 && n_dtype != DIFFATTN_F16) return DIFFATTN_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return DIFFATTN_ERR_INVALID_ARG;
+    if (M == 0) return DIFFATTN_OK;
+    if (!x || !aligned16(x) || (z && !aligned16(z)) || (y_out && !aligned16(y_out)) || (n_out && !aligned16(n_out)) ||
+        (weight && !aligned16(weight)))
+        return DIFFATTN_ERR_INVALID_ARG;
+    AddNormParams p{};
+    p.x = x;
+    p.x_f32 = x_dtype == DIFFATTN_F32;
+    p.z = z;
+    p.y_out = y_out;
+    p.n_out = n_out;
+    p.n_f16 = n_dtype == DIFFATTN_F16;
+    p.weight = weight;
+    p.M = M; p.N = N; p.eps = eps;
+    return cuda_status(launch_add_rmsnorm(p, static_cast<cudaStream_t>(stream)));
+}
+
+diffattn_status diffattn_swiglu(const void* gate_up, void* h_out, int h_dtype, int M, int H, void* stream) {
+    if (M < 0 || H < 8 || H % 8 || (h_dtype != DIFFATTN_BF16 && h_dtype != DIFFATTN_F16)) return DIFFATTN_ERR_INVALID_ARG;
+    if (M == 0) return DIFFATTN_OK;
+    if (!gate_up || !h_out || !aligned16(gate_up) || !aligned16(h_out)) return DIFFATTN_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_swiglu(gate_up, h_out, h_dtype == DIFFATTN_F16, M, H, static_cast<cudaStream_t>(stream)));
 }
 
 diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new, const void* v_new,
@@ -418,9 +451,10 @@ diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes)
     return DIFFATTN_OK;
 }
 
-diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M, int N, int K, int64_t lda,
-                                   int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,
-                                   void* stream) {
+namespace {
+diffattn_status gemm_16bit(bool ab_f16, const void* A, const void* W, void* C, int M, int N, int K, int64_t lda,
+                           int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,
+                           void* stream) {
     if (M < 1 || N < 1 || K < 1) return DIFFATTN_ERR_INVALID_ARG;
     if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16 && out_dtype != DIFFATTN_F16)
         return DIFFATTN_ERR_INVALID_ARG;
@@ -430,7 +464,8 @@ diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M,
     if (workspace == nullptr || workspace_bytes < kControlBytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return DIFFATTN_ERR_WORKSPACE;
     GemmParams p{};
-    if (!encode_2d(&p.tm_a, A, K, M, lda, kGemmBK, kGemmBM) || !encode_2d(&p.tm_w, W, N, K, ldw, 64, kGemmBK))
+    if (!encode_2d(&p.tm_a, A, K, M, lda, kGemmBK, kGemmBM, ab_f16) ||
+        !encode_2d(&p.tm_w, W, N, K, ldw, 64, kGemmBK, ab_f16))
         return DIFFATTN_ERR_INVALID_ARG;
     {
         // Output map for the epilogue's TMA stores: 128-byte x 32-row boxes.
@@ -453,8 +488,22 @@ diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M,
     p.M = M; p.N = N; p.K = K;
     p.out_bf16 = out_dtype == DIFFATTN_BF16;
     p.out_f16 = out_dtype == DIFFATTN_F16;
+    p.ab_f16 = ab_f16;
     p.err = err_word(workspace);
     return cuda_status(launch_gemm_bf16(p, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M, int N, int K, int64_t lda,
+                                   int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    return gemm_16bit(false, A, W, C, M, N, K, lda, ldw, ldc, out_dtype, workspace, workspace_bytes, stream);
+}
+
+diffattn_status diffattn_gemm_f16(const void* A, const void* W, void* C, int M, int N, int K, int64_t lda,
+                                  int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+    return gemm_16bit(true, A, W, C, M, N, K, lda, ldw, ldc, out_dtype, workspace, workspace_bytes, stream);
 }
 
 diffattn_status diffattn_selftest_timeout(void* workspace, size_t workspace_bytes, void* stream) {

@@ -435,6 +435,11 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Packs two floats as fp16 when `f16`, else as bf16 (16-bit outputs chosen at run time).
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, bool f16) {
+    return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
 // P tile packing for an MMA operand of 16-bit type F16 ? fp16 : bf16.
 template <bool F16>
 __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {

@@ -450,14 +450,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) y[i] *= p.norm_w[own0 + c * 32 + i];
             }
-            if (p.out_bf16) {
+            if (p.out_bf16 || p.out_f16) {
+                const bool f16 = p.out_f16 != 0;
                 // 32 columns = half a box row: box c/2, 16-byte chunks (c%2)*4 .. +3.
                 uint8_t* box = stage + (c >> 1) * (BM * 128);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     *reinterpret_cast<uint4*>(box + sw128_offset(r, (c & 1) * 4 + i)) =
-                        make_uint4(pack_bf16x2(y[8 * i], y[8 * i + 1]), pack_bf16x2(y[8 * i + 2], y[8 * i + 3]),
-                                   pack_bf16x2(y[8 * i + 4], y[8 * i + 5]), pack_bf16x2(y[8 * i + 6], y[8 * i + 7]));
+                        make_uint4(pack_16x2(y[8 * i], y[8 * i + 1], f16), pack_16x2(y[8 * i + 2], y[8 * i + 3], f16),
+                                   pack_16x2(y[8 * i + 4], y[8 * i + 5], f16),
+                                   pack_16x2(y[8 * i + 6], y[8 * i + 7], f16));
             } else {
                 uint8_t* box = stage + c * (BM * 128);
 #pragma unroll
@@ -471,7 +473,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_shared();
         named_bar_sync(1, 128);  // all four epilogue warps, on every path
         if (warp == 2 && lane == 0 && !*abort_flag) {
-            const int bw = p.out_bf16 ? 64 : 32;  // elements per 128-byte box row
+            const int bw = p.out_bf16 || p.out_f16 ? 64 : 32;  // elements per 128-byte box row
             for (int i = 0; i < H2 / bw; ++i)
                 tma_store_3d(&p.tm_out, smem + C::kOffOut + i * (BM * 128), h * DV + own0 + i * bw, q0, b);
             tma_store_commit();

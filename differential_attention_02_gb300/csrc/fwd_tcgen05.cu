@@ -423,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
             const float tot = epi[2 * BM + r] + epi[3 * BM + r];
             const float rsc = (1.0f - p.lambda_init) / sqrtf(tot / (float)DV + p.eps);
             const float* w = p.norm_w ? p.norm_w + g * kHalf : nullptr;
-            if (p.out_bf16) {
+            if (p.out_bf16 || p.out_f16) {
+                const bool f16 = p.out_f16 != 0;
 #pragma unroll
                 for (int bx = 0; bx < kHalf / 64; ++bx) {
                     uint8_t* box = stage + (g * (kHalf / 64) + bx) * (BM * 128);
@@ -436,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                             y[e] = oh[i] * rsc * (w ? w[i] : 1.f);
                         }
                         *reinterpret_cast<uint4*>(box + sw128_offset(r, c)) =
-                            make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                                       pack_bf16x2(y[6], y[7]));
+                            make_uint4(pack_16x2(y[0], y[1], f16), pack_16x2(y[2], y[3], f16),
+                                       pack_16x2(y[4], y[5], f16), pack_16x2(y[6], y[7], f16));
                     }
                 }
             } else {
@@ -460,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         fence_proxy_async_shared();
         named_bar_sync(1, 256);
         if (threadIdx.x == 0 && !*abort_flag) {
-            const int bw = p.out_bf16 ? 64 : 32;  // elements per 128-byte box row
+            const int bw = p.out_bf16 || p.out_f16 ? 64 : 32;  // elements per 128-byte box row
             for (int i = 0; i < DV / bw; ++i) tma_store_3d(&p.tm_out, stage + i * (BM * 128), h * DV + i * bw, q0, b);
             tma_store_commit();
             tma_store_wait_read();

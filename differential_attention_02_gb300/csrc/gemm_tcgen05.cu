@@ -1,4 +1,4 @@
-// bf16 GEMM C[M, N] = A[M, K] . W[K, N] on the 5th-generation tensor cores
+// bf16 or fp16 GEMM C[M, N] = A[M, K] . W[K, N] on the 5th-generation tensor cores
 // (tcgen05.mma, fp32 accumulator in tensor memory), fed by TMA.
 //
 // Used for the projections of the multi-head differential attention module:
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
         // ------------------------------------------------------------ MMA issuer
         // The whole warp walks the loop and waits; one elected lane issues each
         // k-block's MMAs together with the commit that tracks them.
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1);
+        const uint32_t idesc = idesc_kind_f16(BM, BN, /*A MN-major*/ 0, /*B MN-major*/ 1, p.ab_f16);
         // A: K-major, 128-byte rows; one K=16 step is 32 bytes along the row.
         // B: MN-major; 64-column boxes are kWBoxBytes apart (leading offset),
         // 8-row K groups 1024 bytes apart (stride offset); K=16 is 16 rows.

@@ -60,6 +60,20 @@ struct KvAppendParams {
     int max_pages, num_pages, B, H_kv, d, Dv;
 };
 cudaError_t launch_kv_append_paged(const KvAppendParams& p, cudaStream_t stream);
+
+struct AddNormParams {
+    const void* x;        // [M, N] bf16 or fp32 (x_f32)
+    int x_f32;
+    const float* z;       // [M, N] fp32 added to x, or null
+    float* y_out;         // [M, N] fp32 = x + z, or null
+    void* n_out;          // [M, N] bf16 or fp16 (n_f16) = RMSNorm(x + z) * weight, or null
+    int n_f16;
+    const float* weight;  // [N] or null
+    int M, N;
+    float eps;
+};
+cudaError_t launch_add_rmsnorm(const AddNormParams& p, cudaStream_t stream);
+cudaError_t launch_swiglu(const void* gate_up, void* h, int h_f16, int64_t M, int H, cudaStream_t stream);
 int decode_keys_per_stage(int d);
 
 // bf16 GEMM on tcgen05: C = A * W.
@@ -70,6 +84,7 @@ struct GemmParams {
     void* C;
     int64_t ldc;
     int M, N, K, out_bf16, out_f16;  // output bf16, fp16, or fp32 when both are 0
+    int ab_f16;                      // operands A and W fp16 (1) or bf16 (0)
     int32_t* err;
 };
 cudaError_t launch_gemm_bf16(const GemmParams& p, cudaStream_t stream);
@@ -82,7 +97,7 @@ struct FwdParams {
     CUtensorMap tm_q1, tm_q2, tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H, N, width]
     CUtensorMap tm_out;                            // 3-D map over the output [B, N, H*Dv], 128-byte boxes
     void* out;                                     // [B, N, H, Dv]
-    int out_bf16;                                  // output bf16 (1) or fp32 (0)
+    int out_bf16, out_f16;                         // output bf16, fp16, or fp32 when both are 0
     int in_f16;                                    // operands fp16 (1) or bf16 (0)
     const float* norm_w;
     int B, H, N, d, Dv, causal;

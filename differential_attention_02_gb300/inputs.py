@@ -23,7 +23,8 @@ import torch
 # Tensor tags: fixed so that a tensor's values never depend on which others are drawn.
 TAG = {"q1": 0, "q2": 1, "k1": 2, "k2": 3, "v": 4,
        "lq1": 5, "lk1": 6, "lq2": 7, "lk2": 8,
-       "x": 10, "w_q": 11, "w_k": 12, "w_v": 13, "w_o": 14, "norm_w": 15}
+       "x": 10, "w_q": 11, "w_k": 12, "w_v": 13, "w_o": 14, "norm_w": 15,
+       "w_gate": 16, "w_up": 17, "w_down": 18, "norm1_w": 19, "norm2_w": 20}
 
 
 def sub_seed(seed: int, tag: int, row: int) -> int:
@@ -63,7 +64,7 @@ def randn_rows(seed: int, tag: int, shape, std: float = 1.0, dtype=torch.bfloat1
 class Workload:
     """One synthetic workload: shapes, dtype, seed and layer index."""
     name: str
-    kind: str               # "prefill", "decode" or "module"
+    kind: str               # "prefill", "decode", "module" or "layer"
     B: int
     H: int
     N: int                  # query length (prefill/module) or cache length L (decode)
@@ -72,7 +73,8 @@ class Workload:
     dtype: str              # "f32" or "bf16"
     seed: int
     layer: int
-    d_model: int = 0        # module only
+    d_model: int = 0        # module and layer only
+    d_ff: int = 0           # layer only: the SwiGLU hidden width
     eps: float = 1e-5
     lam_std: float = 0.1
     layers: tuple = field(default=())   # module sweep
@@ -90,6 +92,10 @@ WORKLOADS = {
     "decode_bf16": Workload("decode_bf16", "decode", B=64, H=16, N=8192, d=64, Dv=128, dtype="bf16", seed=4, layer=3),
     "module_bf16": Workload("module_bf16", "module", B=2, H=8, N=4096, d=128, Dv=256, dtype="bf16", seed=5,
                             layer=1, d_model=2048, layers=tuple(range(1, 25))),
+    "layer_bf16": Workload("layer_bf16", "layer", B=2, H=8, N=4096, d=128, Dv=256, dtype="bf16", seed=6, layer=1,
+                           d_model=2048, d_ff=5632),
+    "layer_small_bf16": Workload("layer_small_bf16", "layer", B=1, H=2, N=256, d=128, Dv=256, dtype="bf16", seed=7,
+                                 layer=4, d_model=512, d_ff=1536),
 }
 
 
@@ -135,4 +141,19 @@ def module_inputs(w: Workload, B=None, N=None):
     for name, shape in (("w_q", (dm, w.H * 2 * w.d)), ("w_k", (dm, w.H * 2 * w.d)),
                         ("w_v", (dm, w.H * w.Dv)), ("w_o", (w.H * w.Dv, dm))):
         t[name] = randn_rows(w.seed, TAG[name], shape, std=wstd, dtype=w.torch_dtype)
+    return t
+
+
+def layer_inputs(w: Workload, B=None, N=None, norm_weights: bool = False):
+    """module_inputs plus the SwiGLU weights w_gate, w_up [d_model, d_ff] (variance
+    1/d_model) and w_down [d_ff, d_model] (variance 1/d_ff); with ``norm_weights`` also
+    the two pre-RMSNorm gains norm1_w, norm2_w [d_model] = 1 + N(0, 0.1^2) (float32)."""
+    t = module_inputs(w, B, N)
+    dm, dff = w.d_model, w.d_ff
+    t["w_gate"] = randn_rows(w.seed, TAG["w_gate"], (dm, dff), std=1.0 / math.sqrt(dm), dtype=w.torch_dtype)
+    t["w_up"] = randn_rows(w.seed, TAG["w_up"], (dm, dff), std=1.0 / math.sqrt(dm), dtype=w.torch_dtype)
+    t["w_down"] = randn_rows(w.seed, TAG["w_down"], (dff, dm), std=1.0 / math.sqrt(dff), dtype=w.torch_dtype)
+    if norm_weights:
+        for k in ("norm1_w", "norm2_w"):
+            t[k] = 1.0 + randn_rows(w.seed, TAG[k], (1, dm), std=0.1, dtype=torch.float32)[0]
     return t

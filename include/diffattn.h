@@ -106,7 +106,8 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
  * (multiple of 32), fp32 arithmetic throughout; in_dtype bf16 or f16 with
  * (d, Dv) = (64, 128) or (128, 256), tcgen05 tensor-core kernels with fp32
  * accumulation (the probability tile P is rounded to the operand type for the
- * P.V product). out_dtype f32 or bf16 for every in_dtype.
+ * P.V product). out_dtype f32 or bf16 for every in_dtype; f16 as well for bf16
+ * and f16 inputs.
  * B, H or N equal to 0: nothing to do, returns DIFFATTN_OK.
  * workspace: at least diffattn_fwd_workspace_size() bytes, 256-byte aligned;
  *   its first 4 bytes are the device error word, which must be zero before the
@@ -248,6 +249,35 @@ diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new,
                                          const int32_t* seq_lens, int B, int H_kv, int d, int Dv, void* stream);
 
 /*
+ * diffattn_add_rmsnorm — the pre-RMSNorm and residual add of the DIFF
+ * Transformer layer ("A Simple Principle From Noise-Cancelling Headphones...",
+ * section "The Overall Architecture Of The Multi-Head Differential
+ * Transformer": each block is pre-normalised with RMSNorm, as in LLaMA, and
+ * added back to its input). Row by row: y = x + z (z optional) and
+ * n = y / sqrt(mean(y^2) + eps) * weight (weight optional).
+ *
+ * x: [M, N] row-major contiguous, bf16 or f32 (x_dtype); z: [M, N] f32 or NULL.
+ * y_out: [M, N] f32 or NULL (y is not written); n_out: [M, N] of n_dtype (bf16
+ * or f16) or NULL.
+ * weight: [N] f32 or NULL. N a multiple of 8; every pointer 16-byte aligned.
+ * M equal to 0: returns DIFFATTN_OK.
+ */
+diffattn_status diffattn_add_rmsnorm(const void* x, int x_dtype, const float* z, float* y_out, void* n_out,
+                                     int n_dtype, const float* weight, int M, int N, float eps, void* stream);
+
+/*
+ * diffattn_swiglu — the SwiGLU activation of the layer's feed-forward block
+ * (same section: "Feed-forward network (FFN) (applying the SwiGLU activation
+ * function)"; LLaMA's form): h = SiLU(g) * u, SiLU(t) = t / (1 + e^-t), where
+ * each row of gate_up holds [g | u].
+ *
+ * gate_up: [M, 2H] f16 contiguous (the output of one GEMM against [W_gate |
+ * W_up]); h_out: [M, H] contiguous, h_dtype bf16 or f16. H a multiple of 8;
+ * pointers 16-byte aligned. M equal to 0: returns DIFFATTN_OK.
+ */
+diffattn_status diffattn_swiglu(const void* gate_up, void* h_out, int h_dtype, int M, int H, void* stream);
+
+/*
  * diffattn_gemm_bf16 — C[M, N] = A[M, K] . W[K, N], bf16 operands, fp32
  * accumulation, tcgen05 tensor cores. The module's projections: [Q|K|V] = X W
  * and Y = concat(heads) W_O ("A Simple Principle From Noise-Cancelling
@@ -265,6 +295,16 @@ diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new,
 diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M, int N, int K,
                                    int64_t lda, int64_t ldw, int64_t ldc, int out_dtype,
                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * diffattn_gemm_f16 — the same GEMM with fp16 operands A and W (arguments,
+ * layout, alignment and errors as diffattn_gemm_bf16). fp16 keeps three more
+ * mantissa bits than bf16 for operands of bounded range, such as the RMSNorm
+ * outputs a DIFF Transformer layer multiplies.
+ */
+diffattn_status diffattn_gemm_f16(const void* A, const void* W, void* C, int M, int N, int K,
+                                  int64_t lda, int64_t ldw, int64_t ldc, int out_dtype,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes);
 

@@ -88,7 +88,8 @@ def test_fwd_argument_validation(lib):
     assert _fwd(lib, q1=_tensor(sh=1028)) == da.ERR_INVALID_ARG           # stride not 16-byte multiple
     assert _fwd(lib, out=0x20004) == da.ERR_INVALID_ARG
     assert _fwd(lib, ind=7) == da.ERR_INVALID_ARG
-    assert _fwd(lib, outd=da.F16) == da.ERR_INVALID_ARG  # outputs are f32 or bf16
+    assert _fwd(lib, outd=7) == da.ERR_INVALID_ARG
+    assert _fwd(lib, ind=da.F32, outd=da.F16, d=32, Dv=64) == da.ERR_INVALID_ARG  # fp32 inputs: f32/bf16 out
     assert _fwd(lib, lam=float("nan")) == da.ERR_INVALID_ARG
     assert _fwd(lib, eps=-1.0) == da.ERR_INVALID_ARG
     assert _fwd(lib, ws=None) == da.ERR_WORKSPACE
@@ -118,13 +119,13 @@ def test_decode_and_gemm_argument_validation(lib):
     n = ctypes.c_size_t()
     assert lib.diffattn_decode_workspace_size(64, 16, 8192, 64, 128, 4, ctypes.byref(n)) == da.OK
     assert n.value == 256 + 64 * 16 * 4 * 4 * 4 + 64 * 16 * 4 * 2 * 128 * 4
-    g = lambda **kw: lib.diffattn_gemm_bf16(vp(kw.get("A", 0x1000)), vp(0x2000), vp(0x3000), kw.get("M", 128),
-                                           kw.get("N", 256), 64, kw.get("lda", 64), 256, 256, da.BF16,
-                                           vp(0x4000), 256, None)
-    assert g(M=0) == da.ERR_INVALID_ARG
-    assert g(A=0x1008) == da.ERR_INVALID_ARG
-    assert g(lda=60) == da.ERR_INVALID_ARG
-    assert g(N=250) == da.ERR_INVALID_ARG
+    for gemm in (lib.diffattn_gemm_bf16, lib.diffattn_gemm_f16):
+        g = lambda **kw: gemm(vp(kw.get("A", 0x1000)), vp(0x2000), vp(0x3000), kw.get("M", 128), kw.get("N", 256),
+                              64, kw.get("lda", 64), 256, 256, da.BF16, vp(0x4000), 256, None)
+        assert g(M=0) == da.ERR_INVALID_ARG
+        assert g(A=0x1008) == da.ERR_INVALID_ARG
+        assert g(lda=60) == da.ERR_INVALID_ARG
+        assert g(N=250) == da.ERR_INVALID_ARG
 
 
 def test_paged_decode_argument_validation(lib):
@@ -155,6 +156,31 @@ def test_kv_append_argument_validation(lib):
     assert call(k1=0x1004) == da.ERR_INVALID_ARG                 # not 16-byte aligned
     assert call(d=60) == da.ERR_INVALID_ARG                      # rows are copied in 16-byte chunks
     assert call(k2=_tensor(sb=4 * 64 * 64, sh=64 * 64, sn=64)) == da.ERR_INVALID_ARG  # K1/K2 strides differ
+
+
+def test_layer_elementwise_argument_validation(lib):
+    vp = ctypes.c_void_p
+    norm = lambda **kw: lib.diffattn_add_rmsnorm(
+        vp(kw.get("x", 0x1000)), kw.get("dt", da.BF16), None, vp(kw.get("y", 0x2000)), vp(0x3000),
+        kw.get("nd", da.BF16), None, kw.get("M", 4), kw.get("N", 64), kw.get("eps", 1e-5), None)
+    assert norm(M=0) == da.OK
+    assert norm(x=0) == da.ERR_INVALID_ARG
+    assert norm(x=0x1008) == da.ERR_INVALID_ARG                  # not 16-byte aligned
+    assert norm(y=0x2004) == da.ERR_INVALID_ARG
+    assert norm(N=60) == da.ERR_INVALID_ARG                      # rows move in 8-element chunks
+    assert norm(dt=da.F16) == da.ERR_INVALID_ARG                 # x is bf16 or fp32
+    assert norm(eps=-1.0) == da.ERR_INVALID_ARG
+    assert norm(eps=float("nan")) == da.ERR_INVALID_ARG
+    assert norm(M=-1) == da.ERR_INVALID_ARG
+    assert norm(nd=da.F32) == da.ERR_INVALID_ARG                 # the normalised rows are bf16 or fp16
+    glu = lambda **kw: lib.diffattn_swiglu(vp(kw.get("gu", 0x1000)), vp(kw.get("h", 0x2000)),
+                                           kw.get("hd", da.F16), kw.get("M", 4), kw.get("H", 64), None)
+    assert glu(M=0) == da.OK
+    assert glu(gu=0) == da.ERR_INVALID_ARG
+    assert glu(h=0x2002) == da.ERR_INVALID_ARG
+    assert glu(H=12) == da.ERR_INVALID_ARG
+    assert glu(M=-3) == da.ERR_INVALID_ARG
+    assert glu(hd=da.F32) == da.ERR_INVALID_ARG
 
 
 def test_python_binding_refuses_without_library(tmp_path):

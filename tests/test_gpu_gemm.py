@@ -32,6 +32,21 @@ def test_gemm_against_float64(M, N, K):
     assert np.max(d - 2.0 ** -8 * np.abs(ref)) <= 1e-3
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 264, 72), (1000, 2048, 2048)])
+def test_gemm_f16_operands(M, N, K):
+    g = torch.Generator().manual_seed(M * 3 + N + K)
+    a = torch.randn(M, K, generator=g).half()
+    w = (torch.randn(K, N, generator=g) / K ** 0.5).half()
+    ref = a.double().numpy() @ w.double().numpy()
+    ws = da.workspace(256)
+    out = da.gemm(a.cuda(), w.cuda(), out_dtype=torch.float32, ws=ws)
+    assert da.read_error(ws) == 0
+    # Exact fp16 products, fp32 accumulation over K: a few fp32 ulps of the partial sums.
+    assert np.max(np.abs(out.cpu().double().numpy() - ref)) <= 1e-4 * max(1.0, K ** 0.5 / 8)
+    with pytest.raises(ValueError):
+        da.gemm(a.cuda(), w.cuda().to(torch.bfloat16))
+
+
 def test_gemm_f16_output():
     g = torch.Generator().manual_seed(3)
     a = torch.randn(300, 512, generator=g).to(torch.bfloat16)

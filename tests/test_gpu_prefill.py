@@ -94,6 +94,17 @@ def test_bf16_non_causal_weight_and_bf16_out():
     assert_bf16_out_parity(out, ref, "bf16 out")
 
 
+@pytest.mark.parametrize("d,Dv,in_dtype", [(64, 128, torch.bfloat16), (128, 256, torch.float16)])
+def test_f16_output_is_the_rounded_f32_output(d, Dv, in_dtype):
+    """The fp16 output path writes exactly the fp32 result rounded to fp16."""
+    g = torch.Generator().manual_seed(d + 11)
+    t = {k: torch.randn(1, 2, 300, Dv if k == "v" else d, generator=g).to(in_dtype) for k in NAMES}
+    out32 = _run(t, 0.45, 0.3)
+    out16 = _run(t, 0.45, 0.3, out_dtype=torch.float16)
+    assert out16.dtype == torch.float16
+    assert torch.equal(out16.cpu(), out32.cpu().half())
+
+
 def test_bf16_strided_views():
     """Q1/Q2 and K1/K2 as halves of one [B, N, H, 2d] buffer (the module's layout)."""
     w = gi.WORKLOADS["prefill_bf16"]
