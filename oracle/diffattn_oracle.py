@@ -38,6 +38,11 @@ Readings where the pages are silent (each also listed in the design notes):
 * Module projections: Q = X W with W stored [d_in, d_out]; inside head i the
   first d channels of its 2d-wide Q (and K) slice are Q_i1, the next d are Q_i2;
   V channels [i*Dv, (i+1)*Dv) belong to head i.
+* Backward pass: the pages train DIFF Transformers but print no gradient. The
+  gradients here are the chain rule of the forward definition above, taken
+  step by step (RMSNorm and scale, the combined map times V, the two row
+  softmaxes, the two score products, lambda's reparameterisation); lambda_init
+  is a constant of the layer and gets no gradient.
 * Layer (intoai, "The Overall Architecture Of The Multi-Head Differential
   Transformer"; hada, "Estrutura multi-head e arquitetura completa"): the pages
   give Y = MultiHead(LN(X)) + X and X' = SwiGLU(LN(Y)) + Y with pre-RMSNorm "as
@@ -66,6 +71,9 @@ __all__ = [
     "silu",
     "swiglu_ffn",
     "layer_fwd",
+    "diffattn_head_bwd",
+    "diffattn_bwd",
+    "reparam_lambda_bwd",
 ]
 
 
@@ -282,3 +290,84 @@ def layer_fwd(x, w_q, w_k, w_v, w_o, w_gate, w_up, w_down, n_heads: int, lam: fl
     y = x + module_fwd(rmsnorm_rows(x, eps, norm1_weight), w_q, w_k, w_v, w_o, n_heads, lam, lam_init, eps,
                        head_weight, causal)
     return y + swiglu_ffn(rmsnorm_rows(y, eps, norm2_weight), w_gate, w_up, w_down)
+
+
+# --------------------------------------------------------------------------
+# Backward pass: the chain rule of the definition above, one step at a time
+# --------------------------------------------------------------------------
+
+def diffattn_head_bwd(q1, q2, k1, k2, v, dy, lam: float, lam_init: float, eps: float = 1e-5, weight=None,
+                      causal: bool = True) -> dict:
+    """Gradients of one head's y = RMSNorm((P1 - lam P2) V) * w * (1 - lam_init).
+
+    q1, q2, k1, k2: [N, d]; v: [N, Dv]; dy: [N, Dv] (the gradient of the loss with
+    respect to y). Returns dq1, dq2, dk1, dk2, dv, dlam (float) and dw ([Dv], the
+    gradient with respect to the RMSNorm gain, taken as 1 when ``weight`` is None).
+    Forward, with S_m = Q_m K_m^T / sqrt(d) + M and P_m its row softmax:
+      A = P1 - lam P2,  O = A V,  r = sqrt(mean_c O^2 + eps),  n = O / r,  y = n w c,
+    c = 1 - lam_init. Backward, row by row:
+      g = dy w c;  dO = (g - n mean_c(g n)) / r;  dw = sum_rows dy n c;
+      dV = A^T dO;  dA = dO V^T;  dlam = -sum(dA * P2);
+      dP1 = dA,  dP2 = -lam dA;  dS_m = P_m (dP_m - rowsum(P_m dP_m));
+      dQ_m = dS_m K_m / sqrt(d),  dK_m = dS_m^T Q_m / sqrt(d).
+    """
+    q1, q2, k1, k2, v, dy = (_f64(a) for a in (q1, q2, k1, k2, v, dy))
+    n_rows, d = q1.shape
+    Dv = v.shape[1]
+    scale = 1.0 / math.sqrt(d)
+    allowed = causal_allowed(np.arange(n_rows), k1.shape[0]) if causal else np.ones((n_rows, k1.shape[0]), bool)
+    p1 = masked_softmax_rows((q1 @ k1.T) * scale, allowed)
+    p2 = masked_softmax_rows((q2 @ k2.T) * scale, allowed)
+    a = p1 - lam * p2
+    o = a @ v
+    r = np.sqrt(np.mean(o * o, axis=1, keepdims=True) + eps)
+    nrm = o / r
+    w = np.ones(Dv) if weight is None else _f64(weight).reshape(-1)
+    c = 1.0 - lam_init
+    # RMSNorm, gain and scale
+    g = dy * w * c
+    d_o = (g - nrm * np.mean(g * nrm, axis=1, keepdims=True)) / r
+    dw = np.sum(dy * nrm * c, axis=0)
+    # O = A V
+    dv = a.T @ d_o
+    da = d_o @ v.T
+    dlam = -float(np.sum(da * p2))
+    # A = P1 - lam P2, then each row softmax
+    dp1, dp2 = da, -lam * da
+    ds1 = p1 * (dp1 - np.sum(p1 * dp1, axis=1, keepdims=True))
+    ds2 = p2 * (dp2 - np.sum(p2 * dp2, axis=1, keepdims=True))
+    # S_m = Q_m K_m^T / sqrt(d)
+    return {"dq1": ds1 @ k1 * scale, "dq2": ds2 @ k2 * scale, "dk1": ds1.T @ q1 * scale,
+            "dk2": ds2.T @ q2 * scale, "dv": dv, "dlam": dlam, "dw": dw}
+
+
+def diffattn_bwd(q1, q2, k1, k2, v, dy, lam: float, lam_init: float, eps: float = 1e-5, weight=None,
+                 causal: bool = True, heads=None) -> dict:
+    """Batched backward: inputs [B, H, N, d] (v [B, H, N, Dv]), dy [B, N, H, Dv] (the
+    forward's output layout). Returns dq1, dq2, dk1, dk2 [B, H, N, d], dv [B, H, N, Dv],
+    dlam (the sum over the heads: lambda is shared by the layer's heads) and dw [Dv].
+    ``heads``, if given, lists the (b, h) pairs to compute; the other gradient entries
+    are NaN and dlam, dw cover only the listed heads."""
+    B, H, N, d = q1.shape
+    Dv = v.shape[-1]
+    out = {k: np.full((B, H, N, Dv if k == "dv" else d), np.nan) for k in ("dq1", "dq2", "dk1", "dk2", "dv")}
+    dlam, dw = 0.0, np.zeros(Dv)
+    pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in pairs:
+        gr = diffattn_head_bwd(q1[b, h], q2[b, h], k1[b, h], k2[b, h], v[b, h], _f64(dy[b, :, h, :]), lam,
+                               lam_init, eps, weight, causal)
+        for k in out:
+            out[k][b, h] = gr[k]
+        dlam += gr["dlam"]
+        dw += gr["dw"]
+    out["dlam"], out["dw"] = dlam, dw
+    return out
+
+
+def reparam_lambda_bwd(lq1, lk1, lq2, lk2, dlam: float):
+    """Gradients of lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init with respect to
+    the four vectors, given dlam: (dlq1, dlk1, dlq2, dlk2)."""
+    lq1, lk1, lq2, lk2 = (_f64(x).reshape(-1) for x in (lq1, lk1, lq2, lk2))
+    e1 = math.exp(float(np.dot(lq1, lk1)))
+    e2 = math.exp(float(np.dot(lq2, lk2)))
+    return dlam * e1 * lk1, dlam * e1 * lq1, -dlam * e2 * lk2, -dlam * e2 * lq2

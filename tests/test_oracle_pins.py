@@ -375,3 +375,100 @@ def test_layer_ffn_branch_matches_torch_rms_norm():
     n = F.rms_norm(T(x), (dm,), T(g2), eps=1e-5)
     want = T(x) + (F.silu(n @ T(w["w_gate"])) * (n @ T(w["w_up"]))) @ T(w["w_down"])
     np.testing.assert_allclose(got, want.numpy(), rtol=1e-11, atol=1e-12)
+
+
+# --------------------------------------------------------------- backward ---
+# The pages print no gradient; the oracle's backward is pinned by central finite
+# differences of its forward (a brute-force derivative of the definition), on
+# shapes where every transposition changes the result (N, d and Dv all differ).
+
+def _head_loss(q1, q2, k1, k2, v, dy, lam, lam_init, eps, w, causal):
+    y = orc.head_rmsnorm_scale(orc.diffattn_head(q1, q2, k1, k2, v, lam, causal), lam_init, eps, w)
+    return float(np.sum(y * dy))
+
+
+def _fd(f, x, h=1e-6):
+    """Central differences of the scalar f() with respect to every entry of x (in place)."""
+    g = np.zeros_like(x)
+    for idx in np.ndindex(*x.shape):
+        keep = x[idx]
+        x[idx] = keep + h
+        fp = f()
+        x[idx] = keep - h
+        fm = f()
+        x[idx] = keep
+        g[idx] = (fp - fm) / (2 * h)
+    return g
+
+
+@pytest.mark.parametrize("causal,lam,with_w", [(True, 0.63, True), (False, -0.4, False), (True, 1.7, False)])
+def test_head_backward_matches_finite_differences(causal, lam, with_w):
+    r = _rng(40 + int(causal))
+    N, d, Dv = 6, 4, 8
+    t = {k: r.standard_normal((N, Dv if k == "v" else d)) for k in ("q1", "q2", "k1", "k2", "v")}
+    dy = r.standard_normal((N, Dv))
+    w = 1 + 0.3 * r.standard_normal(Dv) if with_w else None
+    lam_init, eps = 0.35, 1e-5
+    gr = orc.diffattn_head_bwd(t["q1"], t["q2"], t["k1"], t["k2"], t["v"], dy, lam, lam_init, eps, w, causal)
+    loss = lambda: _head_loss(t["q1"], t["q2"], t["k1"], t["k2"], t["v"], dy, lam_cell[0], lam_init, eps,
+                              w_cell[0], causal)
+    lam_cell, w_cell = [lam], [w]
+    for k in ("q1", "q2", "k1", "k2", "v"):
+        np.testing.assert_allclose(gr["d" + k], _fd(loss, t[k]), rtol=1e-6, atol=1e-8, err_msg=k)
+    lam_arr = np.array([lam])
+
+    def loss_lam():
+        lam_cell[0] = float(lam_arr[0])
+        return loss()
+    assert gr["dlam"] == pytest.approx(float(_fd(loss_lam, lam_arr)[0]), rel=1e-6, abs=1e-8)
+    lam_cell[0] = lam
+    w_arr = np.ones(Dv) if w is None else w.copy()
+
+    def loss_w():
+        w_cell[0] = w_arr
+        return loss()
+    np.testing.assert_allclose(gr["dw"], _fd(loss_w, w_arr), rtol=1e-6, atol=1e-8, err_msg="dw")
+
+
+def test_head_backward_lambda_zero_is_plain_attention_backward():
+    """With lambda = 0 the second map drops out: its gradients vanish and the first map's
+    equal those of softmax attention followed by the same RMSNorm, which torch's float64
+    autograd of scaled_dot_product_attention gives (a library routine)."""
+    r = _rng(44)
+    N, d, Dv = 7, 4, 6
+    q1, q2, k1, k2 = (r.standard_normal((N, d)) for _ in range(4))
+    v, dy = r.standard_normal((N, Dv)), r.standard_normal((N, Dv))
+    gr = orc.diffattn_head_bwd(q1, q2, k1, k2, v, dy, 0.0, 0.2, 1e-5)
+    assert np.all(gr["dq2"] == 0) and np.all(gr["dk2"] == 0)
+    tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (q1, k1, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq[None, None], tk[None, None], tv[None, None],
+                                                         is_causal=True)[0, 0]
+    y = o / torch.sqrt((o * o).mean(-1, keepdim=True) + 1e-5) * 0.8
+    (y * torch.tensor(dy)).sum().backward()
+    np.testing.assert_allclose(gr["dq1"], tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gr["dk1"], tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(gr["dv"], tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_batched_backward_sums_lambda_over_heads():
+    r = _rng(45)
+    B, H, N, d, Dv = 1, 2, 5, 4, 8
+    t = {k: r.standard_normal((B, H, N, Dv if k == "v" else d)) for k in ("q1", "q2", "k1", "k2", "v")}
+    dy = r.standard_normal((B, N, H, Dv))
+    gr = orc.diffattn_bwd(t["q1"], t["q2"], t["k1"], t["k2"], t["v"], dy, 0.5, 0.3)
+    lam_arr = np.array([0.5])
+    loss = lambda: float(np.sum(orc.diffattn_fwd(t["q1"], t["q2"], t["k1"], t["k2"], t["v"], float(lam_arr[0]),
+                                                 0.3) * dy))
+    assert gr["dlam"] == pytest.approx(float(_fd(loss, lam_arr)[0]), rel=1e-6)
+    one = orc.diffattn_head_bwd(t["q1"][0, 1], t["q2"][0, 1], t["k1"][0, 1], t["k2"][0, 1], t["v"][0, 1],
+                                dy[0, :, 1, :], 0.5, 0.3)
+    np.testing.assert_array_equal(gr["dk2"][0, 1], one["dk2"])
+
+
+def test_reparam_lambda_backward_matches_finite_differences():
+    r = _rng(46)
+    vecs = [0.2 * r.standard_normal(5) for _ in range(4)]
+    grads = orc.reparam_lambda_bwd(*vecs, 1.3)
+    for i in range(4):
+        f = lambda: 1.3 * orc.reparam_lambda(*vecs, 3)[0]
+        np.testing.assert_allclose(grads[i], _fd(f, vecs[i]), rtol=1e-7, atol=1e-10)
