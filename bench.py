@@ -376,6 +376,31 @@ def run_layer(args, da, gi, dev, stream, peaks, peak_kind):
             "gpu_launches_per_step": 11}
 
 
+def run_backward(args, da, gi, dev, stream, peaks, peak_kind):
+    """The backward pass (diffattn_bwd) on the prefill workload, bf16 inputs, fp32 gradients."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    x = {k: v.to(dev) for k, v in gi.prefill_inputs(w).items()}
+    dy = gi.output_grad(w).to(dev)
+    lv = gi.lambda_vectors(w)
+    lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+    ws = da.workspace(da.bwd_workspace_bytes(w.B, w.H, w.N, w.d, w.Dv), dev)
+    fn = lambda: da.diffattn_bwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], dy, lam, lam_init, w.eps,
+                                 want_dnorm_weight=True, ws=ws, stream=stream)
+    ms = time_device(fn, max(3, args.steps // 4), args.warmup, stream)
+    n_pairs = w.N * (w.N + 1) / 2
+    # Chain-rule FLOPs per (b, h): per map S recomputed, dQ and dK (2 Np d each); dV and dA (2 Np Dv each).
+    flops = w.B * w.H * (12 * n_pairs * w.d + 4 * n_pairs * w.Dv)
+    tf = flops / (ms * 1e-3) / 1e12
+    # CUDA-core fp32 peak: 152 SMs x 128 FMA lanes x 2 FLOP x the sampled SM clock.
+    sm_mhz = 2070.0
+    alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    return {"workload": "backward of the prefill workload B4 H16 N2048 d64 Dv128 causal, bf16 in, fp32 gradients",
+            "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "flops_per_step": flops,
+            "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
+                         "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 x 2070 MHz"},
+            "gpu_launches_per_step": 4}
+
+
 def run_decode(args, da, gi, dev, stream, peaks, peak_kind):
     """Times the split-KV decode (split kernel + merge kernel) on the decode workload."""
     import dataclasses
@@ -526,6 +551,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         extra["long_prefill"] = run_long_prefill(args, da, gi, dev, stream, peaks, peak_kind)
         extra["module"] = run_module(args, da, gi, dev, stream, peaks, peak_kind)
         extra["layer"] = run_layer(args, da, gi, dev, stream, peaks, peak_kind)
+        extra["backward"] = run_backward(args, da, gi, dev, stream, peaks, peak_kind)
     if rank != 0:
         return
     cpu = None

@@ -23,6 +23,7 @@ EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffat
             "diffattn_decode", "diffattn_decode_workspace_size", "diffattn_gemm_bf16", "diffattn_gemm_f16",
             "diffattn_gemm_workspace_size", "diffattn_read_error", "diffattn_decode_noalloc",
             "diffattn_decode_paged", "diffattn_kv_append_paged", "diffattn_add_rmsnorm", "diffattn_swiglu",
+            "diffattn_bwd", "diffattn_bwd_workspace_size", "diffattn_lambda_bwd",
             "diffattn_selftest_timeout")
 
 
@@ -84,6 +85,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_add_rmsnorm.argtypes = [vp, i32, vp, vp, vp, i32, vp, i32, i32, f32, vp]
     lib.diffattn_swiglu.restype = i32
     lib.diffattn_swiglu.argtypes = [vp, vp, i32, i32, i32, vp]
+    lib.diffattn_bwd.restype = i32
+    lib.diffattn_bwd.argtypes = [Tensor4] * 5 + [vp, vp] + [i32] * 6 + [f32] * 3 + [i32] + [vp] * 7 + [vp, sz, vp]
+    lib.diffattn_bwd_workspace_size.restype = i32
+    lib.diffattn_bwd_workspace_size.argtypes = [i32] * 5 + [ctypes.POINTER(sz)]
+    fpp = ctypes.POINTER(ctypes.c_float)
+    lib.diffattn_lambda_bwd.restype = i32
+    lib.diffattn_lambda_bwd.argtypes = [fpp] * 4 + [i32, f32] + [fpp] * 4
     lib.diffattn_selftest_timeout.restype = i32
     lib.diffattn_selftest_timeout.argtypes = [vp, sz, vp]
     lib.diffattn_read_error.restype = i32
@@ -185,6 +193,57 @@ def diffattn_fwd(q1, q2, k1, k2, v, lam: float, lam_init: float, eps: float = 1e
                             _dtype_code(q1.dtype), _dtype_code(out.dtype), ctypes.c_void_p(ws.data_ptr()),
                             ws.numel(), _stream_ptr(stream)), "diffattn_fwd")
     return out
+
+
+def diffattn_bwd(q1, q2, k1, k2, v, dy, lam: float, lam_init: float, eps: float = 1e-5, norm_weight=None,
+                 causal: bool = True, want_dnorm_weight: bool = False, ws=None, stream=None) -> dict:
+    """Backward of diffattn_fwd. Operands as for diffattn_fwd (one dtype: fp32, bf16 or fp16); dy
+    [B,N,H,Dv] of that dtype. Returns dq1, dq2, dk1, dk2 [B,H,N,d] fp32, dv [B,H,N,Dv] fp32, dlam
+    (a 1-element fp32 device tensor) and dw ([Dv] fp32, or None)."""
+    B, H, N, d = q1.shape
+    Dv = v.shape[-1]
+    for t in (q1, q2, k1, k2, v, dy):
+        if not t.is_cuda or t.dtype != q1.dtype:
+            raise ValueError("all operands and dy must be CUDA tensors of one dtype")
+    if tuple(dy.shape) != (B, N, H, Dv) or not dy.is_contiguous():
+        raise ValueError("dy must be a contiguous [B, N, H, Dv] tensor")
+    lib = load_library()
+    dev = q1.device
+    g = {k: torch.empty((B, H, N, Dv if k == "dv" else d), dtype=torch.float32, device=dev)
+         for k in ("dq1", "dq2", "dk1", "dk2", "dv")}
+    g["dlam"] = torch.empty(4, dtype=torch.float32, device=dev)[:1]
+    g["dw"] = torch.empty(Dv, dtype=torch.float32, device=dev) if want_dnorm_weight else None
+    if ws is None:
+        nbytes = ctypes.c_size_t()
+        _check(lib.diffattn_bwd_workspace_size(B, H, N, d, Dv, ctypes.byref(nbytes)), "diffattn_bwd_workspace_size")
+        ws = workspace(nbytes.value, dev)
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    _check(lib.diffattn_bwd(_t4(q1), _t4(q2), _t4(k1), _t4(k2), _t4(v), ptr(dy), ptr(norm_weight), B, H, N, d, Dv,
+                            int(bool(causal)), float(lam), float(lam_init), float(eps), _dtype_code(q1.dtype),
+                            ptr(g["dq1"]), ptr(g["dq2"]), ptr(g["dk1"]), ptr(g["dk2"]), ptr(g["dv"]), ptr(g["dlam"]),
+                            ptr(g["dw"]), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream)),
+           "diffattn_bwd")
+    return g
+
+
+def bwd_workspace_bytes(B, H, N, d, Dv) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().diffattn_bwd_workspace_size(B, H, N, d, Dv, ctypes.byref(n)), "diffattn_bwd_workspace_size")
+    return n.value
+
+
+def diffattn_lambda_bwd(lq1, lk1, lq2, lk2, dlam: float):
+    """Gradients of lambda with respect to the four lambda vectors (host, double), given dlam."""
+    vs = [torch.as_tensor(v, dtype=torch.float32).contiguous().reshape(-1) for v in (lq1, lk1, lq2, lk2)]
+    d = vs[0].numel()
+    if any(v.numel() != d for v in vs):
+        raise ValueError("lambda vectors must have one common length")
+    outs = [torch.empty(d, dtype=torch.float32) for _ in range(4)]
+    fp = ctypes.POINTER(ctypes.c_float)
+    c = lambda t: ctypes.cast(t.data_ptr(), fp)
+    _check(load_library().diffattn_lambda_bwd(*(c(v) for v in vs), d, float(dlam), *(c(o) for o in outs)),
+           "diffattn_lambda_bwd")
+    return tuple(outs)
 
 
 def decode_workspace_bytes(B, H, L, d, Dv, num_splits=0) -> int:

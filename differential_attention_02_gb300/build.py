@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdiffattn.so")
 SOURCES = ["api.cu", "fwd_simt_f32.cu", "decode_bf16.cu", "gemm_tcgen05.cu", "fwd_tcgen05.cu",
-           "fwd_pair_tcgen05.cu", "layer_ops.cu", "selftest.cu"]
+           "fwd_pair_tcgen05.cu", "layer_ops.cu", "bwd_simt.cu",
+           "selftest.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"),
            os.path.join(ROOT, "include", "diffattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

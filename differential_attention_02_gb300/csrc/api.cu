@@ -293,6 +293,102 @@ diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor 
     return cuda_status(launch_decode_bf16(p, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Byte offsets of the backward's workspace regions after the control block.
+struct BwdLayout {
+    size_t d_o, stats, part_lam, part_w, total;
+};
+BwdLayout bwd_layout(int B, int H, int N, int Dv) {
+    const size_t rows = (size_t)B * H * N;
+    const size_t parts = (size_t)bwd_partial_count(B, H, N);
+    BwdLayout l;
+    l.d_o = kControlBytes;
+    l.stats = l.d_o + round256(rows * Dv * sizeof(float));
+    l.part_lam = l.stats + round256(rows * 4 * sizeof(float));
+    l.part_w = l.part_lam + round256(parts * sizeof(float));
+    l.total = l.part_w + round256(parts * Dv * sizeof(float));
+    return l;
+}
+}  // namespace
+
+diffattn_status diffattn_bwd_workspace_size(int B, int H, int N, int d, int Dv, size_t* bytes) {
+    if (!bytes || B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    *bytes = bwd_layout(B, H, N, Dv).total;
+    return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                             diffattn_tensor v, const void* dy, const float* norm_weight, int B, int H, int N, int d,
+                             int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype, float* dq1,
+                             float* dq2, float* dk1, float* dk2, float* dv, float* dlambda, float* dnorm_weight,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    if (B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16 && in_dtype != DIFFATTN_F16)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (!isfinite(lambda) || !isfinite(lambda_init) || !(eps >= 0.f) || !isfinite(eps))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || N == 0) return DIFFATTN_OK;
+    const int eb = in_dtype == DIFFATTN_F32 ? 4 : 2;
+    if (!check_operand(q1, d, eb) || !check_operand(q2, d, eb) || !check_operand(k1, d, eb) ||
+        !check_operand(k2, d, eb) || !check_operand(v, Dv, eb))
+        return DIFFATTN_ERR_INVALID_ARG;
+    const void* outs[8] = {dy, dq1, dq2, dk1, dk2, dv, dlambda, nullptr};
+    for (int i = 0; i < 7; ++i)
+        if (!outs[i] || !aligned16(outs[i])) return DIFFATTN_ERR_INVALID_ARG;
+    if ((norm_weight && !aligned16(norm_weight)) || (dnorm_weight && !aligned16(dnorm_weight)))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (d % 32 || d > 128 || Dv % 32 || Dv > 256) return DIFFATTN_ERR_UNSUPPORTED;
+    const BwdLayout lay = bwd_layout(B, H, N, Dv);
+    if (workspace == nullptr || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return DIFFATTN_ERR_WORKSPACE;
+    BwdParams p{};
+    p.q1 = q1.ptr; p.q2 = q2.ptr; p.k1 = k1.ptr; p.k2 = k2.ptr; p.v = v.ptr;
+    const diffattn_tensor* ts[5] = {&q1, &q2, &k1, &k2, &v};
+    int64_t* ss[5] = {p.sq1, p.sq2, p.sk1, p.sk2, p.sv};
+    for (int i = 0; i < 5; ++i) {
+        ss[i][0] = ts[i]->stride_b;
+        ss[i][1] = ts[i]->stride_h;
+        ss[i][2] = ts[i]->stride_n;
+    }
+    p.dy = dy;
+    p.norm_w = norm_weight;
+    p.dq1 = dq1; p.dq2 = dq2; p.dk1 = dk1; p.dk2 = dk2; p.dv = dv;
+    p.dlambda = dlambda;
+    p.dnorm_w = dnorm_weight;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.d_o = reinterpret_cast<float*>(ws + lay.d_o);
+    p.stats = reinterpret_cast<float*>(ws + lay.stats);
+    p.part_lam = reinterpret_cast<float*>(ws + lay.part_lam);
+    p.part_w = reinterpret_cast<float*>(ws + lay.part_w);
+    p.B = B; p.H = H; p.N = N; p.d = d; p.Dv = Dv; p.causal = causal != 0;
+    p.in_dtype = in_dtype == DIFFATTN_F32 ? 0 : in_dtype == DIFFATTN_BF16 ? 1 : 2;
+    p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
+    return cuda_status(launch_bwd_simt(p, static_cast<cudaStream_t>(stream)));
+}
+
+diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2, int d,
+                                    float dlambda, float* dlq1, float* dlk1, float* dlq2, float* dlk2) {
+    if (!lq1 || !lk1 || !lq2 || !lk2 || !dlq1 || !dlk1 || !dlq2 || !dlk2 || d < 1 || !isfinite(dlambda))
+        return DIFFATTN_ERR_INVALID_ARG;
+    double d1 = 0.0, d2 = 0.0;
+    for (int i = 0; i < d; ++i) {
+        d1 += (double)lq1[i] * (double)lk1[i];
+        d2 += (double)lq2[i] * (double)lk2[i];
+    }
+    const double e1 = exp(d1), e2 = exp(d2);
+    if (!isfinite(e1) || !isfinite(e2)) return DIFFATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < d; ++i) {
+        const double a = lq1[i], b = lk1[i], c = lq2[i], e = lk2[i];
+        dlq1[i] = (float)(dlambda * e1 * b);
+        dlk1[i] = (float)(dlambda * e1 * a);
+        dlq2[i] = (float)(-dlambda * e2 * e);
+        dlk2[i] = (float)(-dlambda * e2 * c);
+    }
+    return DIFFATTN_OK;
+}
+
 diffattn_status diffattn_add_rmsnorm(const void* x, int x_dtype, const float* z, float* y_out, void* n_out,
                                      int n_dtype, const float* weight, int M, int N, float eps, void* stream) {
     if (M < 0 || N < 8 || N % 8 || (x_dtype != DIFFATTN_F32 && x_dtype != DIFFATTN_BF16)) return DIFFATTN_ERR_INVALID_ARG;

@@ -26,6 +26,26 @@ struct SimtF32Params {
 };
 cudaError_t launch_fwd_simt_f32(const SimtF32Params& p, cudaStream_t stream);
 
+// Backward pass on the CUDA cores (fp32 arithmetic; inputs fp32, bf16 or fp16).
+struct BwdParams {
+    const void *q1, *q2, *k1, *k2, *v;              // [B, H, N, d] / [B, H, N, Dv], in_dtype
+    int64_t sq1[3], sq2[3], sk1[3], sk2[3], sv[3];  // b, h, n strides in elements
+    const void* dy;                                 // [B, N, H, Dv] contiguous, in_dtype
+    const float* norm_w;                            // [Dv] or null
+    float *dq1, *dq2, *dk1, *dk2;                   // [B, H, N, d] contiguous
+    float* dv;                                      // [B, H, N, Dv] contiguous
+    float* dlambda;                                 // [1]
+    float* dnorm_w;                                 // [Dv] or null
+    float* d_o;                                     // workspace [B, H, N, Dv]
+    float* stats;                                   // workspace [B, H, N, 4]: lse1, lse2, D1, D2
+    float* part_lam;                                // workspace [partials]
+    float* part_w;                                  // workspace [partials, Dv]
+    int B, H, N, d, Dv, causal, in_dtype;           // in_dtype 0 fp32, 1 bf16, 2 fp16
+    float lambda, lambda_init, eps;
+};
+int64_t bwd_partial_count(int B, int H, int N);
+cudaError_t launch_bwd_simt(const BwdParams& p, cudaStream_t stream);
+
 // bf16 split-KV decode (+ merge).
 struct DecodeParams {
     CUtensorMap tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H_kv, L, width], or [pages, H_kv, 64, width] when paged

@@ -24,7 +24,7 @@ import torch
 TAG = {"q1": 0, "q2": 1, "k1": 2, "k2": 3, "v": 4,
        "lq1": 5, "lk1": 6, "lq2": 7, "lk2": 8,
        "x": 10, "w_q": 11, "w_k": 12, "w_v": 13, "w_o": 14, "norm_w": 15,
-       "w_gate": 16, "w_up": 17, "w_down": 18, "norm1_w": 19, "norm2_w": 20}
+       "w_gate": 16, "w_up": 17, "w_down": 18, "norm1_w": 19, "norm2_w": 20, "dy": 21}
 
 
 def sub_seed(seed: int, tag: int, row: int) -> int:
@@ -157,3 +157,12 @@ def layer_inputs(w: Workload, B=None, N=None, norm_weights: bool = False):
         for k in ("norm1_w", "norm2_w"):
             t[k] = 1.0 + randn_rows(w.seed, TAG[k], (1, dm), std=0.1, dtype=torch.float32)[0]
     return t
+
+
+def output_grad(w: Workload, B=None, H=None, N=None):
+    """dy [B, N, H, Dv] ~ N(0, 1): the gradient fed to the backward pass, in the prefill
+    output layout and the workload dtype."""
+    B = w.B if B is None else B
+    H = w.H if H is None else H
+    N = w.N if N is None else N
+    return randn_rows(w.seed, TAG["dy"], (B, N, H, w.Dv), dtype=w.torch_dtype)

@@ -249,6 +249,59 @@ diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new,
                                          const int32_t* seq_lens, int B, int H_kv, int d, int Dv, void* stream);
 
 /*
+ * diffattn_bwd — gradients of diffattn_fwd (the backward pass). The pages train
+ * DIFF Transformers ("Differential Transformer: Transformer que cancela ruído
+ * de atenção", section "Eficiência e estabilidade de treinamento") but print no
+ * gradient; this computes the chain rule of the forward definition. With
+ * P_m = softmax(Q_m K_m^T / sqrt d + M), A = P1 - lambda P2, O = A V and
+ * y = O / sqrt(mean(O^2) + eps) * w * (1 - lambda_init):
+ *   dO = (g - n mean(g n)) / r with n = O / r, g = dy w (1 - lambda_init);
+ *   dV = A^T dO; dA = dO V^T; dlambda = -sum(dA P2);
+ *   dS1 = P1 (dA - rowsum(P1 dA)); dS2 = P2 (-lambda dA - rowsum(-lambda P2 dA));
+ *   dQ_m = dS_m K_m / sqrt d; dK_m = dS_m^T Q_m / sqrt d; dw = sum_rows dy n (1 - lambda_init).
+ * lambda_init is a constant of the layer and has no gradient.
+ *
+ * q1..v, norm_weight, B, H, N, d, Dv, causal, lambda, lambda_init, eps,
+ *   in_dtype: as for diffattn_fwd (in_dtype f32, bf16 or f16).
+ * dy: [B, N, H, Dv] contiguous, in_dtype — the gradient with respect to the
+ *   forward's output, in the forward's output layout.
+ * dq1, dq2, dk1, dk2: [B, H, N, d] contiguous f32; dv: [B, H, N, Dv] contiguous
+ *   f32 (written, not accumulated).
+ * dlambda: device f32[1], the sum over every head (lambda is shared by the
+ *   layer's heads); chain it to the lambda vectors with diffattn_lambda_bwd.
+ * dnorm_weight: device f32[Dv] or NULL — the gradient with respect to the
+ *   RMSNorm gain (of a unit gain when norm_weight is NULL).
+ * d and Dv multiples of 32 with d <= 128 and Dv <= 256 (else UNSUPPORTED).
+ * Every pointer 16-byte aligned. Arithmetic is fp32 on the CUDA cores; results
+ * do not depend on scheduling (no atomics). B, H or N equal to 0: DIFFATTN_OK.
+ * workspace: diffattn_bwd_workspace_size() bytes, 256-byte aligned.
+ */
+diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                             diffattn_tensor v, const void* dy, const float* norm_weight,
+                             int B, int H, int N, int d, int Dv, int causal,
+                             float lambda, float lambda_init, float eps, int in_dtype,
+                             float* dq1, float* dq2, float* dk1, float* dk2, float* dv,
+                             float* dlambda, float* dnorm_weight,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes diffattn_bwd needs: the control block, dO and four per-row
+ * statistics in f32, and per-block partial sums of dlambda and dw. */
+diffattn_status diffattn_bwd_workspace_size(int B, int H, int N, int d, int Dv, size_t* bytes);
+
+/*
+ * diffattn_lambda_bwd — on the host, the gradients of
+ *   lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init
+ * with respect to the four vectors, given dlambda:
+ *   dlq1 = dlambda e1 lk1, dlk1 = dlambda e1 lq1, dlq2 = -dlambda e2 lk2,
+ *   dlk2 = -dlambda e2 lq2, with e1 = exp(lq1 . lk1), e2 = exp(lq2 . lk2)
+ * (section "Como a atenção diferencial funciona"). Every pointer is a HOST
+ * pointer to d floats; computed in double. INVALID_ARG on NULL pointers, d < 1
+ * or a non-finite result.
+ */
+diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2, int d,
+                                    float dlambda, float* dlq1, float* dlk1, float* dlq2, float* dlk2);
+
+/*
  * diffattn_add_rmsnorm — the pre-RMSNorm and residual add of the DIFF
  * Transformer layer ("A Simple Principle From Noise-Cancelling Headphones...",
  * section "The Overall Architecture Of The Multi-Head Differential

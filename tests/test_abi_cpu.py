@@ -183,6 +183,52 @@ def test_layer_elementwise_argument_validation(lib):
     assert glu(hd=da.F32) == da.ERR_INVALID_ARG
 
 
+def _bwd(lib, **kw):
+    a = dict(q1=_tensor(), q2=_tensor(), k1=_tensor(), k2=_tensor(), v=_tensor(sn=128), dy=0x20000, w=None,
+             B=1, H=2, N=16, d=64, Dv=128, causal=1, lam=0.5, lam_init=0.2, eps=1e-5, ind=da.BF16,
+             dq1=0x30000, dq2=0x30000, dk1=0x30000, dk2=0x30000, dv=0x30000, dlam=0x30000, dw=None,
+             ws=0x40000, wsb=1 << 30, stream=None)
+    a.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.diffattn_bwd(a["q1"], a["q2"], a["k1"], a["k2"], a["v"], vp(a["dy"]), vp(a["w"]), a["B"], a["H"],
+                            a["N"], a["d"], a["Dv"], a["causal"], a["lam"], a["lam_init"], a["eps"], a["ind"],
+                            vp(a["dq1"]), vp(a["dq2"]), vp(a["dk1"]), vp(a["dk2"]), vp(a["dv"]), vp(a["dlam"]),
+                            vp(a["dw"]), vp(a["ws"]), a["wsb"], a["stream"])
+
+
+def test_bwd_argument_validation(lib):
+    assert _bwd(lib, B=0) == da.OK and _bwd(lib, N=0) == da.OK
+    assert _bwd(lib, N=-1) == da.ERR_INVALID_ARG
+    assert _bwd(lib, ind=7) == da.ERR_INVALID_ARG
+    assert _bwd(lib, lam=float("inf")) == da.ERR_INVALID_ARG
+    assert _bwd(lib, dy=None) == da.ERR_INVALID_ARG
+    assert _bwd(lib, dk2=0x30004) == da.ERR_INVALID_ARG          # not 16-byte aligned
+    assert _bwd(lib, dlam=None) == da.ERR_INVALID_ARG
+    assert _bwd(lib, dw=0x30008) == da.ERR_INVALID_ARG
+    assert _bwd(lib, v=_tensor(sn=100)) == da.ERR_INVALID_ARG
+    assert _bwd(lib, d=48, q1=_tensor(sn=48), q2=_tensor(sn=48), k1=_tensor(sn=48),
+                k2=_tensor(sn=48)) == da.ERR_UNSUPPORTED          # d a multiple of 32
+    assert _bwd(lib, Dv=288, v=_tensor(sn=288)) == da.ERR_UNSUPPORTED
+    n = ctypes.c_size_t()
+    assert lib.diffattn_bwd_workspace_size(1, 2, 16, 64, 128, ctypes.byref(n)) == da.OK
+    rows, parts = 2 * 16, 2 * 2
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert n.value == 256 + r256(rows * 128 * 4) + r256(rows * 16) + r256(parts * 4) + r256(parts * 128 * 4)
+    assert _bwd(lib, wsb=n.value - 1) == da.ERR_WORKSPACE
+    assert _bwd(lib, ws=0x40010) == da.ERR_WORKSPACE
+
+
+def test_host_lambda_backward_matches_oracle(lib):
+    r = np.random.default_rng(3)
+    vecs = [(0.2 * r.standard_normal(64)).astype(np.float32) for _ in range(4)]
+    got = da.diffattn_lambda_bwd(*vecs, -1.7)
+    ref = orc.reparam_lambda_bwd(*vecs, -1.7)
+    for g, e in zip(got, ref):
+        np.testing.assert_allclose(g.numpy(), e, rtol=1e-6, atol=1e-9)
+    with pytest.raises(da.DiffAttnError):
+        da.diffattn_lambda_bwd(*vecs, float("nan"))
+
+
 def test_python_binding_refuses_without_library(tmp_path):
     saved = da._lib
     da._lib = None
