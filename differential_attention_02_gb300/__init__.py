@@ -23,7 +23,8 @@ EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffat
             "diffattn_decode", "diffattn_decode_workspace_size", "diffattn_gemm_bf16", "diffattn_gemm_f16",
             "diffattn_gemm_workspace_size", "diffattn_read_error", "diffattn_decode_noalloc",
             "diffattn_decode_paged", "diffattn_kv_append_paged", "diffattn_add_rmsnorm", "diffattn_swiglu",
-            "diffattn_bwd", "diffattn_bwd_workspace_size", "diffattn_lambda_bwd",
+            "diffattn_bwd", "diffattn_bwd_workspace_size", "diffattn_lambda_bwd", "diffattn_decode_paged_fp8",
+            "diffattn_kv_append_paged_fp8",
             "diffattn_selftest_timeout")
 
 
@@ -81,6 +82,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_kv_append_paged.restype = i32
     lib.diffattn_kv_append_paged.argtypes = [vp, vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, i32, vp, i32, i32, i32,
                                              i32, vp]
+    lib.diffattn_decode_paged_fp8.restype = i32
+    lib.diffattn_decode_paged_fp8.argtypes = [vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, i32, vp, i32, vp, vp, i32,
+                                              i32, i32, i32, i32, f32, f32, f32, f32, f32, f32, i32, i32, vp, sz, vp]
+    lib.diffattn_kv_append_paged_fp8.restype = i32
+    lib.diffattn_kv_append_paged_fp8.argtypes = [vp, vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, i32, vp, i32, i32,
+                                                 i32, i32, f32, f32, f32, vp]
     lib.diffattn_add_rmsnorm.restype = i32
     lib.diffattn_add_rmsnorm.argtypes = [vp, i32, vp, vp, vp, i32, vp, i32, i32, f32, vp]
     lib.diffattn_swiglu.restype = i32
@@ -278,11 +285,19 @@ def diffattn_decode(q1, q2, k1_cache, k2_cache, v_cache, lam: float, lam_init: f
     return out
 
 
+def _is_fp8(t) -> bool:
+    return t.dtype in (torch.float8_e4m3fn, torch.uint8)
+
+
 def diffattn_decode_paged(q1, q2, k1_pages, k2_pages, v_pages, block_table, seq_lens, lam: float, lam_init: float,
                           L: int, kv_group: int = 1, eps: float = 1e-5, norm_weight=None, num_splits: int = 0,
-                          out_dtype=torch.float32, out=None, ws=None, stream=None) -> torch.Tensor:
-    """Split-KV decode against a paged KV cache. q: [B,H,d]; pages [num_pages, H/kv_group, 64, *] bf16;
-    block_table int32 [B, max_pages] and seq_lens int32 [B] on the GPU; L = the largest length. -> [B,H,Dv]."""
+                          out_dtype=torch.float32, out=None, ws=None, stream=None, scales=None) -> torch.Tensor:
+    """Split-KV decode against a paged KV cache. q: [B,H,d]; pages [num_pages, H/kv_group, 64, *] bf16, or
+    fp8 e4m3 (torch.float8_e4m3fn or uint8 bytes) with scales = (k1_scale, k2_scale, v_scale); block_table
+    int32 [B, max_pages] and seq_lens int32 [B] on the GPU; L = the largest length. -> [B,H,Dv]."""
+    fp8 = _is_fp8(k1_pages)
+    if fp8 != (scales is not None) or any(_is_fp8(t) != fp8 for t in (k2_pages, v_pages)):
+        raise ValueError("fp8 pages (all three) go with scales, bf16 pages without")
     B, H, d = q1.shape
     Dv = v_pages.shape[-1]
     num_pages, max_pages = k1_pages.shape[0], block_table.shape[1]
@@ -294,29 +309,41 @@ def diffattn_decode_paged(q1, q2, k1_pages, k2_pages, v_pages, block_table, seq_
     nbytes = decode_workspace_bytes(B, H, int(L), d, Dv, num_splits)
     ws = workspace(nbytes, q1.device) if ws is None else ws
     w = None if norm_weight is None else ctypes.c_void_p(norm_weight.data_ptr())
-    _check(load_library().diffattn_decode_paged(
-        ctypes.c_void_p(q1.data_ptr()), ctypes.c_void_p(q2.data_ptr()), _t4(k1_pages), _t4(k2_pages), _t4(v_pages),
-        ctypes.c_void_p(block_table.data_ptr()), max_pages, num_pages, ctypes.c_void_p(seq_lens.data_ptr()), int(L),
-        ctypes.c_void_p(out.data_ptr()), w, B, H, int(kv_group), d, Dv, float(lam), float(lam_init), float(eps),
-        int(num_splits), _dtype_code(out.dtype), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream)),
-        "diffattn_decode_paged")
+    lib = load_library()
+    head = (ctypes.c_void_p(q1.data_ptr()), ctypes.c_void_p(q2.data_ptr()), _t4(k1_pages), _t4(k2_pages),
+            _t4(v_pages), ctypes.c_void_p(block_table.data_ptr()), max_pages, num_pages,
+            ctypes.c_void_p(seq_lens.data_ptr()), int(L), ctypes.c_void_p(out.data_ptr()), w, B, H, int(kv_group), d,
+            Dv, float(lam), float(lam_init), float(eps))
+    tail = (int(num_splits), _dtype_code(out.dtype), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream))
+    if fp8:
+        _check(lib.diffattn_decode_paged_fp8(*head, *(float(x) for x in scales), *tail), "diffattn_decode_paged_fp8")
+    else:
+        _check(lib.diffattn_decode_paged(*head, *tail), "diffattn_decode_paged")
     return out
 
 
 def diffattn_kv_append_paged(k1_new, k2_new, v_new, k1_pages, k2_pages, v_pages, block_table, seq_lens,
-                             stream=None) -> None:
+                             stream=None, scales=None) -> None:
     """Writes the new token's K1, K2, V rows ([B, H_kv, *] bf16) into the paged cache at position
-    seq_lens[b] - 1 of each sequence (pages [num_pages, H_kv, 64, *], block_table [B, max_pages])."""
+    seq_lens[b] - 1 of each sequence (pages [num_pages, H_kv, 64, *], block_table [B, max_pages]).
+    fp8 pages take scales = (k1_scale, k2_scale, v_scale) and store e4m3(x / scale)."""
     B, Hk, d = k1_new.shape
     Dv = v_new.shape[-1]
     for t in (k1_new, k2_new, v_new):
         if not t.is_contiguous():
             raise ValueError("new-token rows must be contiguous")
-    _check(load_library().diffattn_kv_append_paged(
-        ctypes.c_void_p(k1_new.data_ptr()), ctypes.c_void_p(k2_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
-        _t4(k1_pages), _t4(k2_pages), _t4(v_pages), ctypes.c_void_p(block_table.data_ptr()), block_table.shape[1],
-        k1_pages.shape[0], ctypes.c_void_p(seq_lens.data_ptr()), B, Hk, d, Dv, _stream_ptr(stream)),
-        "diffattn_kv_append_paged")
+    fp8 = _is_fp8(k1_pages)
+    if fp8 != (scales is not None) or any(_is_fp8(t) != fp8 for t in (k2_pages, v_pages)):
+        raise ValueError("fp8 pages (all three) go with scales, bf16 pages without")
+    args = (ctypes.c_void_p(k1_new.data_ptr()), ctypes.c_void_p(k2_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
+            _t4(k1_pages), _t4(k2_pages), _t4(v_pages), ctypes.c_void_p(block_table.data_ptr()), block_table.shape[1],
+            k1_pages.shape[0], ctypes.c_void_p(seq_lens.data_ptr()), B, Hk, d, Dv)
+    lib = load_library()
+    if fp8:
+        _check(lib.diffattn_kv_append_paged_fp8(*args, *(float(x) for x in scales), _stream_ptr(stream)),
+               "diffattn_kv_append_paged_fp8")
+    else:
+        _check(lib.diffattn_kv_append_paged(*args, _stream_ptr(stream)), "diffattn_kv_append_paged")
 
 
 def add_rmsnorm(x, z=None, weight=None, eps: float = 1e-5, want_y: bool = False, want_n: bool = True,

@@ -44,10 +44,11 @@ bool encode_4d(CUtensorMap* m, const diffattn_tensor& t, int width, int rows, in
                CUtensorMapSwizzle sw, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
+    const int eb = dt == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2;  // bytes per element
     const int64_t sn = t.stride_n, sh = (H > 1) ? t.stride_h : (int64_t)rows * sn,
                   sb = (B > 1) ? t.stride_b : (int64_t)H * sh;
     cuuint64_t dims[4] = {(cuuint64_t)width, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)(sn * 2), (cuuint64_t)(sh * 2), (cuuint64_t)(sb * 2)};
+    cuuint64_t strides[3] = {(cuuint64_t)(sn * eb), (cuuint64_t)(sh * eb), (cuuint64_t)(sb * eb)};
     cuuint32_t box[4] = {(cuuint32_t)box_w, (cuuint32_t)box_rows, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, dt, 4, const_cast<void*>(t.ptr), dims, strides, box, es,
@@ -418,17 +419,23 @@ diffattn_status diffattn_swiglu(const void* gate_up, void* h_out, int h_dtype, i
         launch_swiglu(gate_up, h_out, h_dtype == DIFFATTN_F16, M, H, static_cast<cudaStream_t>(stream)));
 }
 
-diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new, const void* v_new,
-                                         diffattn_tensor k1_pages, diffattn_tensor k2_pages, diffattn_tensor v_pages,
-                                         const int32_t* block_table, int max_pages, int num_pages,
-                                         const int32_t* seq_lens, int B, int H_kv, int d, int Dv, void* stream) {
+namespace {
+bool valid_scale(float s) { return isfinite(s) && s > 0.f; }
+
+diffattn_status kv_append(bool fp8, const float* scales, const void* k1_new, const void* k2_new, const void* v_new,
+                          diffattn_tensor k1_pages, diffattn_tensor k2_pages, diffattn_tensor v_pages,
+                          const int32_t* block_table, int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                          int H_kv, int d, int Dv, void* stream) {
     if (B < 0 || H_kv < 0 || d < 8 || Dv < 8 || (d % 8) || (Dv % 8) || max_pages < 1 || num_pages < 1)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (fp8 && !(valid_scale(scales[0]) && valid_scale(scales[1]) && valid_scale(scales[2])))
         return DIFFATTN_ERR_INVALID_ARG;
     if (B == 0 || H_kv == 0) return DIFFATTN_OK;
     if (!k1_new || !k2_new || !v_new || !aligned16(k1_new) || !aligned16(k2_new) || !aligned16(v_new) ||
         !block_table || !seq_lens)
         return DIFFATTN_ERR_INVALID_ARG;
-    if (!check_operand(k1_pages, d, 2) || !check_operand(k2_pages, d, 2) || !check_operand(v_pages, Dv, 2))
+    const int eb = fp8 ? 1 : 2;
+    if (!check_operand(k1_pages, d, eb) || !check_operand(k2_pages, d, eb) || !check_operand(v_pages, Dv, eb))
         return DIFFATTN_ERR_INVALID_ARG;
     if (k1_pages.stride_b != k2_pages.stride_b || k1_pages.stride_h != k2_pages.stride_h ||
         k1_pages.stride_n != k2_pages.stride_n)
@@ -444,27 +451,54 @@ diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new,
     p.seq_lens = seq_lens;
     p.max_pages = max_pages; p.num_pages = num_pages;
     p.B = B; p.H_kv = H_kv; p.d = d; p.Dv = Dv;
+    p.fp8 = fp8;
+    if (fp8) {
+        p.k1_scale = scales[0]; p.k2_scale = scales[1]; p.v_scale = scales[2];
+    }
     return cuda_status(launch_kv_append_paged(p, static_cast<cudaStream_t>(stream)));
 }
+}  // namespace
 
-diffattn_status diffattn_decode_paged(const void* q1, const void* q2, diffattn_tensor k1_pages,
-                                      diffattn_tensor k2_pages, diffattn_tensor v_pages, const int32_t* block_table,
-                                      int max_pages, int num_pages, const int32_t* seq_lens, int L, void* out,
-                                      const float* norm_weight, int B, int H, int kv_group, int d, int Dv,
-                                      float lambda, float lambda_init, float eps, int num_splits, int out_dtype,
-                                      void* workspace, size_t workspace_bytes, void* stream) {
+diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new, const void* v_new,
+                                         diffattn_tensor k1_pages, diffattn_tensor k2_pages, diffattn_tensor v_pages,
+                                         const int32_t* block_table, int max_pages, int num_pages,
+                                         const int32_t* seq_lens, int B, int H_kv, int d, int Dv, void* stream) {
+    return kv_append(false, nullptr, k1_new, k2_new, v_new, k1_pages, k2_pages, v_pages, block_table, max_pages,
+                     num_pages, seq_lens, B, H_kv, d, Dv, stream);
+}
+
+diffattn_status diffattn_kv_append_paged_fp8(const void* k1_new, const void* k2_new, const void* v_new,
+                                             diffattn_tensor k1_pages, diffattn_tensor k2_pages,
+                                             diffattn_tensor v_pages, const int32_t* block_table, int max_pages,
+                                             int num_pages, const int32_t* seq_lens, int B, int H_kv, int d, int Dv,
+                                             float k1_scale, float k2_scale, float v_scale, void* stream) {
+    const float scales[3] = {k1_scale, k2_scale, v_scale};
+    return kv_append(true, scales, k1_new, k2_new, v_new, k1_pages, k2_pages, v_pages, block_table, max_pages,
+                     num_pages, seq_lens, B, H_kv, d, Dv, stream);
+}
+
+namespace {
+diffattn_status decode_paged(bool fp8, const float* scales, const void* q1, const void* q2, diffattn_tensor k1_pages,
+                             diffattn_tensor k2_pages, diffattn_tensor v_pages, const int32_t* block_table,
+                             int max_pages, int num_pages, const int32_t* seq_lens, int L, void* out,
+                             const float* norm_weight, int B, int H, int kv_group, int d, int Dv, float lambda,
+                             float lambda_init, float eps, int num_splits, int out_dtype, void* workspace,
+                             size_t workspace_bytes, void* stream) {
     if (B < 0 || H < 0 || L < 1 || d < 1 || Dv < 1 || num_splits < 0 || num_splits > 256 || kv_group < 1 ||
         max_pages < 1 || num_pages < 1)
         return DIFFATTN_ERR_INVALID_ARG;
     if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16) return DIFFATTN_ERR_INVALID_ARG;
     if (!isfinite(lambda) || !isfinite(lambda_init) || !(eps >= 0.f) || !isfinite(eps))
         return DIFFATTN_ERR_INVALID_ARG;
+    if (fp8 && !(valid_scale(scales[0]) && valid_scale(scales[1]) && valid_scale(scales[2])))
+        return DIFFATTN_ERR_INVALID_ARG;
     if (B == 0 || H == 0) return DIFFATTN_OK;
     const int stage = decode_keys_per_stage(d);  // one page = one stage of keys
     if (H % kv_group != 0 || L > (int64_t)stage * max_pages) return DIFFATTN_ERR_INVALID_ARG;
     if (!q1 || !q2 || !aligned16(q1) || !aligned16(q2) || !out || !aligned16(out) || !block_table || !seq_lens)
         return DIFFATTN_ERR_INVALID_ARG;
-    if (!check_operand(k1_pages, d, 2) || !check_operand(k2_pages, d, 2) || !check_operand(v_pages, Dv, 2))
+    const int eb = fp8 ? 1 : 2;
+    if (!check_operand(k1_pages, d, eb) || !check_operand(k2_pages, d, eb) || !check_operand(v_pages, Dv, eb))
         return DIFFATTN_ERR_INVALID_ARG;
     if (norm_weight != nullptr && !aligned16(norm_weight)) return DIFFATTN_ERR_INVALID_ARG;
     if (!((d == 64 && Dv == 128) || (d == 128 && Dv == 256))) return DIFFATTN_ERR_UNSUPPORTED;
@@ -474,10 +508,22 @@ diffattn_status diffattn_decode_paged(const void* q1, const void* q2, diffattn_t
     if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return DIFFATTN_ERR_WORKSPACE;
     const int H_kv = H / kv_group;
-    if (!encode_4d(&p.tm_k1, k1_pages, d, stage, H_kv, num_pages, 64, stage, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_4d(&p.tm_k2, k2_pages, d, stage, H_kv, num_pages, 64, stage, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_4d(&p.tm_v, v_pages, Dv, stage, H_kv, num_pages, Dv, stage, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return DIFFATTN_ERR_INVALID_ARG;
+    bool ok;
+    if (fp8) {
+        // Whole key rows in one box: 64 bytes unswizzled (d = 64) or 128 bytes swizzled (d = 128).
+        const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        const CUtensorMapSwizzle ksw = d == 64 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+        ok = encode_4d(&p.tm_k1, k1_pages, d, stage, H_kv, num_pages, d, stage, ksw, u8) &&
+             encode_4d(&p.tm_k2, k2_pages, d, stage, H_kv, num_pages, d, stage, ksw, u8) &&
+             encode_4d(&p.tm_v, v_pages, Dv, stage, H_kv, num_pages, Dv, stage, CU_TENSOR_MAP_SWIZZLE_NONE, u8);
+        p.kv_fp8 = 1;
+        p.k1_scale = scales[0]; p.k2_scale = scales[1]; p.v_scale = scales[2];
+    } else {
+        ok = encode_4d(&p.tm_k1, k1_pages, d, stage, H_kv, num_pages, 64, stage, CU_TENSOR_MAP_SWIZZLE_128B) &&
+             encode_4d(&p.tm_k2, k2_pages, d, stage, H_kv, num_pages, 64, stage, CU_TENSOR_MAP_SWIZZLE_128B) &&
+             encode_4d(&p.tm_v, v_pages, Dv, stage, H_kv, num_pages, Dv, stage, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (!ok) return DIFFATTN_ERR_INVALID_ARG;
     p.q1 = q1;
     p.q2 = q2;
     p.seq_lens = seq_lens;
@@ -495,6 +541,31 @@ diffattn_status diffattn_decode_paged(const void* q1, const void* q2, diffattn_t
     p.part_stats = reinterpret_cast<float*>(ws + kControlBytes);
     p.part_o = p.part_stats + (size_t)B * H * p.num_splits * 4;
     return cuda_status(launch_decode_bf16(p, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+diffattn_status diffattn_decode_paged(const void* q1, const void* q2, diffattn_tensor k1_pages,
+                                      diffattn_tensor k2_pages, diffattn_tensor v_pages, const int32_t* block_table,
+                                      int max_pages, int num_pages, const int32_t* seq_lens, int L, void* out,
+                                      const float* norm_weight, int B, int H, int kv_group, int d, int Dv,
+                                      float lambda, float lambda_init, float eps, int num_splits, int out_dtype,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_paged(false, nullptr, q1, q2, k1_pages, k2_pages, v_pages, block_table, max_pages, num_pages,
+                        seq_lens, L, out, norm_weight, B, H, kv_group, d, Dv, lambda, lambda_init, eps, num_splits,
+                        out_dtype, workspace, workspace_bytes, stream);
+}
+
+diffattn_status diffattn_decode_paged_fp8(const void* q1, const void* q2, diffattn_tensor k1_pages,
+                                          diffattn_tensor k2_pages, diffattn_tensor v_pages,
+                                          const int32_t* block_table, int max_pages, int num_pages,
+                                          const int32_t* seq_lens, int L, void* out, const float* norm_weight, int B,
+                                          int H, int kv_group, int d, int Dv, float lambda, float lambda_init,
+                                          float eps, float k1_scale, float k2_scale, float v_scale, int num_splits,
+                                          int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    const float scales[3] = {k1_scale, k2_scale, v_scale};
+    return decode_paged(true, scales, q1, q2, k1_pages, k2_pages, v_pages, block_table, max_pages, num_pages,
+                        seq_lens, L, out, norm_weight, B, H, kv_group, d, Dv, lambda, lambda_init, eps, num_splits,
+                        out_dtype, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- decode without caller workspace

@@ -1,5 +1,5 @@
 // Split-KV decode of differential attention: one new query token per
-// sequence against its KV cache, bf16 cache, fp32 arithmetic.
+// sequence against its KV cache, bf16 or fp8 (e4m3) cache, fp32 arithmetic.
 //
 // What it computes: the last row of the DiffAttn formula of "Differential
 // Transformer: Transformer que cancela ruído de atenção" (section "Como a
@@ -18,6 +18,15 @@
 // partial state (m, l, o[Dv]) per map to the workspace.
 // Kernel 2 (merge): one CTA per (b, h) merges the split partials exactly,
 // combines o1/l1 - lambda o2/l2, applies RMSNorm and (1 - lambda_init).
+//
+// fp8 cache: K1, K2 and V hold e4m3 values with one scale per tensor (cache
+// value = stored value x scale). The pages point to lower-bit quantization as a
+// use of the method's smaller activation outliers ("Differential Transformer:
+// Transformer que cancela ruído de atenção", section "Resultados experimentais
+// e efeitos de aplicação"); here the cache is quantized to halve the bytes the
+// HBM-bound decode reads. The K scales are folded into the query, the V scale
+// into the merged output.
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -32,14 +41,18 @@ constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;  // 8: four lanes per 
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, int DV>
+template <int D, int DV, bool FP8>
 struct DecodeCfg {
-    static constexpr int kBoxesK = D / 64;                      // 64-element (128-byte) swizzled boxes per key row
-    static constexpr int kKBytes = kStageKeys * D * 2;          // one map's keys per stage
-    static constexpr int kVBytes = kStageKeys * DV * 2;
+    static constexpr int kEB = FP8 ? 1 : 2;                     // bytes per cached element
+    // bf16: 64-element (128-byte) swizzled boxes per key row; fp8: one box of the whole row
+    // (64 bytes unswizzled for d = 64, 128 bytes swizzled for d = 128).
+    static constexpr int kBoxesK = FP8 ? 1 : D / 64;
+    static constexpr int kKBytes = kStageKeys * D * kEB;        // one map's keys per stage
+    static constexpr int kVBytes = kStageKeys * DV * kEB;
     static constexpr int kStageBytes = 2 * kKBytes + kVBytes;
-    static constexpr int kStages = (D == 64) ? 3 : 2;
+    static constexpr int kStages = ((D == 64) ? 3 : 2) * (FP8 ? 2 : 1);  // same bytes in flight
     static constexpr int kQuarter = D / 4;                      // dot-product elements per lane
+    static constexpr int kChunks = kQuarter * kEB / 16;         // 16-byte chunks per lane per key
     static constexpr int kDVL = DV / 32;                        // value columns per lane
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 2 * kStages * 8 + 64 +
                                     (size_t)kConsumerWarps * (4 + 2 * DV) * 4;
@@ -52,9 +65,24 @@ __device__ __forceinline__ const uint4* k_chunk(const uint8_t* tile, int r, int 
     return reinterpret_cast<const uint4*>(tile + box * (kStageKeys * 128) + r * 128 + ((cc ^ (r & 7)) << 4));
 }
 
-template <int D, int DV>
+// 16-byte chunk c of key row r in a stage's K tile of either element type.
+template <int D, bool FP8>
+__device__ __forceinline__ const uint4* key_chunk(const uint8_t* tile, int r, int c) {
+    if constexpr (FP8 && D == 64) return reinterpret_cast<const uint4*>(tile + r * 64 + (c << 4));
+    else return k_chunk(tile, r, c);
+}
+
+// Four e4m3 values packed in a 32-bit word (lowest byte first) as floats.
+__device__ __forceinline__ void fp8x4_to_f32(uint32_t w, float* f) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+
+template <int D, int DV, bool FP8>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_constant__ DecodeParams p) {
-    using C = DecodeCfg<D, DV>;
+    using C = DecodeCfg<D, DV, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
@@ -104,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                 const int bz = pages ? page : b;
                 mbar_arrive_expect_tx(&full[s], C::kStageBytes);
 #pragma unroll
-                for (int x = 0; x < C::kBoxesK; ++x) {
+                for (int x = 0; x < C::kBoxesK; ++x) {  // fp8: one box, x = 0
                     tma_load_4d(st + x * kStageKeys * 128, &p.tm_k1, &full[s], x * 64, row, hk, bz);
                     tma_load_4d(st + C::kKBytes + x * kStageKeys * 128, &p.tm_k2, &full[s], x * 64, row, hk, bz);
                 }
@@ -124,10 +152,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
             const __nv_bfloat16* q1 = reinterpret_cast<const __nv_bfloat16*>(p.q1) + ((int64_t)b * p.H + h) * D;
             const __nv_bfloat16* q2 = reinterpret_cast<const __nv_bfloat16*>(p.q2) + ((int64_t)b * p.H + h) * D;
             const float sc = kLog2e / sqrtf((float)D);
+            const float sc1 = sc * p.k1_scale, sc2 = sc * p.k2_scale;  // 1 for a bf16 cache
 #pragma unroll
             for (int e = 0; e < C::kQuarter; ++e) {
-                q1r[e] = __bfloat162float(q1[quarter * C::kQuarter + e]) * sc;
-                q2r[e] = __bfloat162float(q2[quarter * C::kQuarter + e]) * sc;
+                q1r[e] = __bfloat162float(q1[quarter * C::kQuarter + e]) * sc1;
+                q2r[e] = __bfloat162float(q2[quarter * C::kQuarter + e]) * sc2;
             }
         }
         float m1 = -INFINITY, m2 = -INFINITY, l1 = 0.f, l2 = 0.f;
@@ -144,17 +173,31 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
             // Scores: this lane's quarter of both dot products, reduced over the 4 lanes of the key.
             float s1 = 0.f, s2 = 0.f;
 #pragma unroll
-            for (int c = 0; c < C::kQuarter / 8; ++c) {
-                const int chunk = quarter * (C::kQuarter / 8) + c;
-                const uint4 a = *k_chunk(st, r, chunk);
-                const uint4 bb = *k_chunk(st + C::kKBytes, r, chunk);
+            for (int c = 0; c < C::kChunks; ++c) {
+                const int chunk = quarter * C::kChunks + c;
+                const uint4 a = *key_chunk<D, FP8>(st, r, chunk);
+                const uint4 bb = *key_chunk<D, FP8>(st + C::kKBytes, r, chunk);
                 const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bb.x, bb.y, bb.z, bb.w};
+                if constexpr (FP8) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    s1 = fmaf(q1r[c * 8 + 2 * e], bf16lo_to_f32(aw[e]), s1);
-                    s1 = fmaf(q1r[c * 8 + 2 * e + 1], bf16hi_to_f32(aw[e]), s1);
-                    s2 = fmaf(q2r[c * 8 + 2 * e], bf16lo_to_f32(bw[e]), s2);
-                    s2 = fmaf(q2r[c * 8 + 2 * e + 1], bf16hi_to_f32(bw[e]), s2);
+                    for (int e = 0; e < 4; ++e) {
+                        float fa[4], fb[4];
+                        fp8x4_to_f32(aw[e], fa);
+                        fp8x4_to_f32(bw[e], fb);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            s1 = fmaf(q1r[c * 16 + 4 * e + u], fa[u], s1);
+                            s2 = fmaf(q2r[c * 16 + 4 * e + u], fb[u], s2);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        s1 = fmaf(q1r[c * 8 + 2 * e], bf16lo_to_f32(aw[e]), s1);
+                        s1 = fmaf(q1r[c * 8 + 2 * e + 1], bf16hi_to_f32(aw[e]), s1);
+                        s2 = fmaf(q2r[c * 8 + 2 * e], bf16lo_to_f32(bw[e]), s2);
+                        s2 = fmaf(q2r[c * 8 + 2 * e + 1], bf16hi_to_f32(bw[e]), s2);
+                    }
                 }
             }
             s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
@@ -190,8 +233,23 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                 for (int kk = 0; kk < nk; ++kk) {
                     const float w1 = __shfl_sync(0xffffffffu, p1, kk * 4);
                     const float w2 = __shfl_sync(0xffffffffu, p2, kk * 4);
-                    const uint8_t* vrow = vt + (size_t)(warp * kKeysPerWarp + kk) * DV * 2;
-                    if constexpr (C::kDVL == 4) {
+                    const uint8_t* vrow = vt + (size_t)(warp * kKeysPerWarp + kk) * DV * C::kEB;
+                    if constexpr (FP8) {
+                        // kDVL consecutive e4m3 values: columns lane * kDVL ...
+                        float f[C::kDVL];
+                        if constexpr (C::kDVL == 4) {
+                            fp8x4_to_f32(*reinterpret_cast<const uint32_t*>(vrow + lane * 4), f);
+                        } else {
+                            const uint2 vv = *reinterpret_cast<const uint2*>(vrow + lane * 8);
+                            fp8x4_to_f32(vv.x, f);
+                            fp8x4_to_f32(vv.y, f + 4);
+                        }
+#pragma unroll
+                        for (int u = 0; u < C::kDVL; ++u) {
+                            o1[u] = fmaf(w1, f[u], o1[u]);
+                            o2[u] = fmaf(w2, f[u], o2[u]);
+                        }
+                    } else if constexpr (C::kDVL == 4) {
                         const uint2 vv = *reinterpret_cast<const uint2*>(vrow + lane * 8);
                         const float f[4] = {bf16lo_to_f32(vv.x), bf16hi_to_f32(vv.x), bf16lo_to_f32(vv.y),
                                             bf16hi_to_f32(vv.y)};
@@ -292,7 +350,7 @@ __global__ void __launch_bounds__(DV) decode_merge_kernel(const __grid_constant_
             o2 += po[s * 2 * DV + DV + c] * e;
         }
     }
-    const float oh = o1 / l1 - p.lambda * (o2 / l2);
+    const float oh = (o1 / l1 - p.lambda * (o2 / l2)) * p.v_scale;  // v_scale 1 for a bf16 cache
     float ss = warp_sum(oh * oh);
     if ((c & 31) == 0) red[c >> 5] = ss;
     __syncthreads();
@@ -308,11 +366,11 @@ __global__ void __launch_bounds__(DV) decode_merge_kernel(const __grid_constant_
         reinterpret_cast<float*>(p.out)[o] = y;
 }
 
-template <int D, int DV>
+template <int D, int DV, bool FP8>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t stream) {
-    using C = DecodeCfg<D, DV>;
-    auto k = decode_split_kernel<D, DV>;
-    cudaError_t e = prepare_once<decode_split_kernel<D, DV>>((int)C::kSmem);
+    using C = DecodeCfg<D, DV, FP8>;
+    auto k = decode_split_kernel<D, DV, FP8>;
+    cudaError_t e = prepare_once<decode_split_kernel<D, DV, FP8>>((int)C::kSmem);
     if (e != cudaSuccess) return e;
     k<<<dim3(p.num_splits, p.H, p.B), kThreads, C::kSmem, stream>>>(p);
     e = cudaGetLastError();
@@ -353,18 +411,69 @@ __global__ void kv_append_paged_kernel(const __grid_constant__ KvAppendParams p)
     }
 }
 
+// The same append into fp8 (e4m3) pages: each value is stored as
+// sat_e4m3(x / scale), rounded to nearest even. 8 values per lane step.
+__global__ void kv_append_paged_fp8_kernel(const __grid_constant__ KvAppendParams p) {
+    const int b = blockIdx.x / p.H_kv, h = blockIdx.x % p.H_kv;
+    const int pos = p.seq_lens[b] - 1;
+    if (pos < 0 || pos / kStageKeys >= p.max_pages) return;
+    const int page = p.block_table[(int64_t)b * p.max_pages + pos / kStageKeys];
+    if (page < 0 || page >= p.num_pages) return;
+    const int row = pos % kStageKeys;
+    const int64_t src_k = ((int64_t)b * p.H_kv + h) * p.d, src_v = ((int64_t)b * p.H_kv + h) * p.Dv;
+    const int64_t dst_k = page * p.k_stride_page + h * p.k_stride_h + row * p.k_stride_row;
+    const int64_t dst_v = page * p.v_stride_page + h * p.v_stride_h + row * p.v_stride_row;
+    const int ck = p.d / 8, cv = p.Dv / 8;  // 8-value groups per row
+    for (int c = threadIdx.x; c < 2 * ck + cv; c += blockDim.x) {
+        const __nv_bfloat16* src;
+        uint8_t* dst;
+        float scale;
+        if (c < ck) {
+            src = static_cast<const __nv_bfloat16*>(p.k1_new) + src_k + c * 8;
+            dst = static_cast<uint8_t*>(p.k1_pages) + dst_k + c * 8;
+            scale = p.k1_scale;
+        } else if (c < 2 * ck) {
+            src = static_cast<const __nv_bfloat16*>(p.k2_new) + src_k + (c - ck) * 8;
+            dst = static_cast<uint8_t*>(p.k2_pages) + dst_k + (c - ck) * 8;
+            scale = p.k2_scale;
+        } else {
+            src = static_cast<const __nv_bfloat16*>(p.v_new) + src_v + (c - 2 * ck) * 8;
+            dst = static_cast<uint8_t*>(p.v_pages) + dst_v + (c - 2 * ck) * 8;
+            scale = p.v_scale;
+        }
+        const uint4 x = *reinterpret_cast<const uint4*>(src);
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        uint32_t q[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float2 a = make_float2(__fdiv_rn(bf16lo_to_f32(xw[2 * k]), scale),
+                                         __fdiv_rn(bf16hi_to_f32(xw[2 * k]), scale));
+            const float2 bb = make_float2(__fdiv_rn(bf16lo_to_f32(xw[2 * k + 1]), scale),
+                                          __fdiv_rn(bf16hi_to_f32(xw[2 * k + 1]), scale));
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(bb, __NV_SATFINITE, __NV_E4M3);
+            q[k] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint2*>(dst) = make_uint2(q[0], q[1]);
+    }
+}
+
 }  // namespace
 
 int decode_keys_per_stage(int) { return kStageKeys; }
 
 cudaError_t launch_kv_append_paged(const KvAppendParams& p, cudaStream_t stream) {
-    kv_append_paged_kernel<<<p.B * p.H_kv, 32, 0, stream>>>(p);
+    if (p.fp8)
+        kv_append_paged_fp8_kernel<<<p.B * p.H_kv, 32, 0, stream>>>(p);
+    else
+        kv_append_paged_kernel<<<p.B * p.H_kv, 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream) {
-    if (p.d == 64 && p.Dv == 128) return launch_t<64, 128>(p, stream);
-    if (p.d == 128 && p.Dv == 256) return launch_t<128, 256>(p, stream);
+    if (p.d == 64 && p.Dv == 128) return p.kv_fp8 ? launch_t<64, 128, true>(p, stream) : launch_t<64, 128, false>(p, stream);
+    if (p.d == 128 && p.Dv == 256)
+        return p.kv_fp8 ? launch_t<128, 256, true>(p, stream) : launch_t<128, 256, false>(p, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -64,6 +64,8 @@ struct DecodeParams {
     const int32_t* block_table;  // [B][max_pages] physical page of each 64-token page, or null (contiguous cache)
     int max_pages;
     int kv_group;  // query heads per KV head (query head h reads KV head h / kv_group)
+    int kv_fp8;    // cache of fp8 e4m3 values (1) or bf16 (0)
+    float k1_scale = 1.f, k2_scale = 1.f, v_scale = 1.f;  // cache value = stored value * scale
 };
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream);
 struct KvAppendParams {
@@ -78,6 +80,8 @@ struct KvAppendParams {
     const int32_t* block_table;  // [B][max_pages]
     const int32_t* seq_lens;     // [B]: the new token is at position seq_lens[b] - 1
     int max_pages, num_pages, B, H_kv, d, Dv;
+    int fp8;                                          // pages hold fp8 e4m3: store sat(x / scale)
+    float k1_scale = 1.f, k2_scale = 1.f, v_scale = 1.f;
 };
 cudaError_t launch_kv_append_paged(const KvAppendParams& p, cudaStream_t stream);
 

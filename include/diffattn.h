@@ -249,6 +249,46 @@ diffattn_status diffattn_kv_append_paged(const void* k1_new, const void* k2_new,
                                          const int32_t* seq_lens, int B, int H_kv, int d, int Dv, void* stream);
 
 /*
+ * diffattn_decode_paged_fp8 — diffattn_decode_paged against a paged cache of
+ * fp8 e4m3 values with one scale per tensor: cached K1 = k1_pages * k1_scale,
+ * K2 = k2_pages * k2_scale, V = v_pages * v_scale. Half the bytes of the bf16
+ * cache for the HBM-bound decode. The pages point to lower-bit quantization as
+ * a use of differential attention's smaller activation outliers ("Differential
+ * Transformer: Transformer que cancela ruído de atenção", section "Resultados
+ * experimentais e efeitos de aplicação"). Arithmetic is fp32 on the
+ * dequantized values (the query stays bf16), so the result is the decode of
+ * the dequantized cache.
+ *
+ * k1_pages, k2_pages: [num_pages, H_kv, 64, d] e4m3 bytes; v_pages: [num_pages,
+ *   H_kv, 64, Dv] e4m3 bytes (strides in elements = bytes, multiples of 16).
+ * k1_scale, k2_scale, v_scale: finite and > 0 (else INVALID_ARG).
+ * Other arguments, the workspace and errors: as diffattn_decode_paged.
+ */
+diffattn_status diffattn_decode_paged_fp8(const void* q1, const void* q2,
+                                          diffattn_tensor k1_pages, diffattn_tensor k2_pages, diffattn_tensor v_pages,
+                                          const int32_t* block_table, int max_pages, int num_pages,
+                                          const int32_t* seq_lens, int L,
+                                          void* out, const float* norm_weight,
+                                          int B, int H, int kv_group, int d, int Dv,
+                                          float lambda, float lambda_init, float eps,
+                                          float k1_scale, float k2_scale, float v_scale,
+                                          int num_splits, int out_dtype,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * diffattn_kv_append_paged_fp8 — diffattn_kv_append_paged into fp8 e4m3 pages:
+ * each value x of the bf16 rows k1_new, k2_new, v_new is stored as
+ * e4m3(x / scale) (x / scale rounded to fp32, then to the nearest e4m3 value,
+ * ties to even, saturating at +-448). Scales finite and > 0; other arguments
+ * and errors as diffattn_kv_append_paged (page strides in bytes).
+ */
+diffattn_status diffattn_kv_append_paged_fp8(const void* k1_new, const void* k2_new, const void* v_new,
+                                             diffattn_tensor k1_pages, diffattn_tensor k2_pages,
+                                             diffattn_tensor v_pages, const int32_t* block_table, int max_pages,
+                                             int num_pages, const int32_t* seq_lens, int B, int H_kv, int d, int Dv,
+                                             float k1_scale, float k2_scale, float v_scale, void* stream);
+
+/*
  * diffattn_bwd — gradients of diffattn_fwd (the backward pass). The pages train
  * DIFF Transformers ("Differential Transformer: Transformer que cancela ruído
  * de atenção", section "Eficiência e estabilidade de treinamento") but print no

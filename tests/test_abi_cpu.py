@@ -229,6 +229,26 @@ def test_host_lambda_backward_matches_oracle(lib):
         da.diffattn_lambda_bwd(*vecs, float("nan"))
 
 
+def test_fp8_cache_argument_validation(lib):
+    t8 = _tensor(sb=2 * 64 * 64, sh=64 * 64, sn=64)      # [pages, 2, 64, 64] bytes
+    v8 = _tensor(sb=2 * 64 * 128, sh=64 * 128, sn=128)
+    vp = ctypes.c_void_p
+    dec = lambda **kw: lib.diffattn_decode_paged_fp8(
+        vp(0x1000), vp(0x1000), kw.get("k", t8), t8, v8, vp(0x3000), 4, 8, vp(0x3100), 200, vp(0x2000), None,
+        kw.get("B", 2), 2, 1, 64, 128, 0.5, 0.2, 1e-5, kw.get("ks", 0.01), 0.01, kw.get("vs", 0.01), 0, da.F32,
+        vp(0x4000), 1 << 20, None)
+    assert dec(B=0) == da.OK
+    assert dec(ks=0.0) == da.ERR_INVALID_ARG
+    assert dec(vs=float("inf")) == da.ERR_INVALID_ARG
+    assert dec(ks=-1.0) == da.ERR_INVALID_ARG
+    assert dec(k=_tensor(sb=2 * 64 * 64, sh=64 * 64, sn=72)) == da.ERR_INVALID_ARG  # 72-byte rows: not 16-multiple
+    app = lambda **kw: lib.diffattn_kv_append_paged_fp8(
+        vp(0x1000), vp(0x1000), vp(0x1000), t8, t8, v8, vp(0x3000), 4, 8, vp(0x3100), kw.get("B", 2), 2, 64, 128,
+        kw.get("ks", 0.01), 0.01, 0.01, None)
+    assert app(B=0) == da.OK
+    assert app(ks=float("nan")) == da.ERR_INVALID_ARG
+
+
 def test_python_binding_refuses_without_library(tmp_path):
     saved = da._lib
     da._lib = None
