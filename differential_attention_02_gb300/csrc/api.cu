@@ -100,10 +100,11 @@ int32_t* err_word(void* ws) { return reinterpret_cast<int32_t*>(ws); }
 
 // Decode split count: the smallest split count whose CTA waves are at least 90%
 // full on this GPU, capped so that every split keeps at least 256 keys.
-int decode_auto_splits(int B, int H, int L, int d) {
+int decode_auto_splits(int B, int H, int L, int d, bool fp8) {
     const int n_sm = device_sm_count();
     const int sms = n_sm > 0 ? n_sm : 148;
-    const int per_sm = (d == 64) ? 2 : 1;  // resident split CTAs per SM (shared-memory bound)
+    // Resident split CTAs per SM (bound by shared memory; fp8 stages are half the bytes).
+    const int per_sm = (d == 64) ? (fp8 ? 3 : 2) : 1;
     const double slots = (double)sms * per_sm;
     const int smax = std::max(1, std::min(256, L / 256));
     for (int s = 1; s <= smax; ++s) {
@@ -114,8 +115,8 @@ int decode_auto_splits(int B, int H, int L, int d) {
     return smax;
 }
 
-void decode_geometry(int B, int H, int L, int d, int num_splits, int* S, int* kps) {
-    int s = num_splits > 0 ? num_splits : decode_auto_splits(B, H, L, d);
+void decode_geometry(int B, int H, int L, int d, int num_splits, int* S, int* kps, bool fp8 = false) {
+    int s = num_splits > 0 ? num_splits : decode_auto_splits(B, H, L, d, fp8);
     const int stage = decode_keys_per_stage(d);
     int k = (L + s - 1) / s;
     k = (k + stage - 1) / stage * stage;
@@ -245,9 +246,11 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
 diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int Dv, int num_splits, size_t* bytes) {
     if (!bytes || B < 0 || H < 0 || L < 1 || d < 1 || Dv < 1 || num_splits < 0 || num_splits > 256)
         return DIFFATTN_ERR_INVALID_ARG;
-    int S, kps;
-    decode_geometry(B, H, L, d, num_splits, &S, &kps);
-    *bytes = decode_ws_bytes(B, H, S, Dv);
+    // Enough for either cache type: the fp8 decode may choose more splits.
+    int S, S8, kps;
+    decode_geometry(B, H, L, d, num_splits, &S, &kps, false);
+    decode_geometry(B, H, L, d, num_splits, &S8, &kps, true);
+    *bytes = decode_ws_bytes(B, H, std::max(S, S8), Dv);
     return DIFFATTN_OK;
 }
 
@@ -503,7 +506,7 @@ diffattn_status decode_paged(bool fp8, const float* scales, const void* q1, cons
     if (norm_weight != nullptr && !aligned16(norm_weight)) return DIFFATTN_ERR_INVALID_ARG;
     if (!((d == 64 && Dv == 128) || (d == 128 && Dv == 256))) return DIFFATTN_ERR_UNSUPPORTED;
     DecodeParams p{};
-    decode_geometry(B, H, L, d, num_splits, &p.num_splits, &p.keys_per_split);
+    decode_geometry(B, H, L, d, num_splits, &p.num_splits, &p.keys_per_split, fp8);
     const size_t need = decode_ws_bytes(B, H, p.num_splits, Dv);
     if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return DIFFATTN_ERR_WORKSPACE;
@@ -602,7 +605,9 @@ diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2, diffattn
     const diffattn_status st = diffattn_decode_workspace_size(B, H, L, d, Dv, num_splits, &need);
     if (st != DIFFATTN_OK) return st;
     if (B == 0 || H == 0) return DIFFATTN_OK;
-    if (need > sizeof(g_decode_scratch)) return DIFFATTN_ERR_WORKSPACE;
+    int S, kps;  // the bf16-cache geometry diffattn_decode will use
+    decode_geometry(B, H, L, d, num_splits, &S, &kps, false);
+    if (decode_ws_bytes(B, H, S, Dv) > sizeof(g_decode_scratch)) return DIFFATTN_ERR_WORKSPACE;
     void* scratch = decode_scratch_address();
     if (scratch == nullptr) return DIFFATTN_ERR_CUDA;
     // The error word must start at zero; the partial states are fully rewritten by the split kernel.

@@ -50,7 +50,9 @@ struct DecodeCfg {
     static constexpr int kKBytes = kStageKeys * D * kEB;        // one map's keys per stage
     static constexpr int kVBytes = kStageKeys * DV * kEB;
     static constexpr int kStageBytes = 2 * kKBytes + kVBytes;
-    static constexpr int kStages = ((D == 64) ? 3 : 2) * (FP8 ? 2 : 1);  // same bytes in flight
+    // fp8 stages are half the size: the same count keeps a d = 64 CTA at ~58 KB of shared
+    // memory, so three CTAs (24 consumer warps) share an SM instead of two.
+    static constexpr int kStages = (D == 64) ? 3 : 2;
     static constexpr int kQuarter = D / 4;                      // dot-product elements per lane
     static constexpr int kChunks = kQuarter * kEB / 16;         // 16-byte chunks per lane per key
     static constexpr int kDVL = DV / 32;                        // value columns per lane
