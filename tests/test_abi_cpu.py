@@ -36,6 +36,31 @@ def test_header_and_library_agree(lib):
         assert hasattr(lib, n), n
 
 
+def test_header_is_plain_c_and_links_against_the_library(lib, tmp_path):
+    """A C99 translation unit that includes the header and takes the address of every
+    declared function compiles with warnings as errors and links against the library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = _declared_functions()
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "diffattn.h"\n#include <stdio.h>\ntypedef void (*fn_t)(void);\n'
+                   "int main(void) {\n    fn_t fns[] = {\n"
+                   + "".join(f"        (fn_t)&{n},\n" for n in names)
+                   + "    };\n    printf(\"%d\\n\", (int)(sizeof fns / sizeof fns[0]));\n    return 0;\n}\n")
+    pkg = os.path.dirname(da.__file__)
+    out = tmp_path / "use_header"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                        os.path.dirname(HEADER), str(src), "-o", str(out), "-L", pkg, "-ldiffattn"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    # The library carries the CUDA runtime statically: the program loads it with nothing else.
+    r = subprocess.run([str(out)], capture_output=True, text=True, env={**os.environ, "LD_LIBRARY_PATH": pkg})
+    assert r.returncode == 0 and r.stdout.strip() == str(len(names)), (r.stdout, r.stderr)
+
+
 def test_status_strings(lib):
     assert da.status_string(da.OK) == "ok"
     assert "timed out" in da.status_string(da.ERR_TIMEOUT)
@@ -247,6 +272,29 @@ def test_fp8_cache_argument_validation(lib):
         kw.get("ks", 0.01), 0.01, 0.01, None)
     assert app(B=0) == da.OK
     assert app(ks=float("nan")) == da.ERR_INVALID_ARG
+
+
+def test_python_wrappers_reject_inconsistent_arguments(lib):
+    """Checks the bindings make before any device work (CPU tensors suffice)."""
+    t = torch.zeros(1, 2, 64, 64, dtype=torch.bfloat16)
+    v = torch.zeros(1, 2, 64, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        da.diffattn_bwd(t, t, t, t, v, torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16), 0.5, 0.2)
+    p8 = torch.zeros(4, 2, 64, 64, dtype=torch.float8_e4m3fn)
+    v8 = torch.zeros(4, 2, 64, 128, dtype=torch.float8_e4m3fn)
+    pb = torch.zeros(4, 2, 64, 64, dtype=torch.bfloat16)
+    q = torch.zeros(1, 2, 64, dtype=torch.bfloat16)
+    table, lens = torch.zeros(1, 4, dtype=torch.int32), torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="scales"):
+        da.diffattn_decode_paged(q, q, p8, p8, v8, table, lens, 0.5, 0.2, L=64)             # fp8 without scales
+    with pytest.raises(ValueError, match="scales"):
+        da.diffattn_decode_paged(q, q, pb, pb, pb, table, lens, 0.5, 0.2, L=64, scales=(1, 1, 1))
+    with pytest.raises(ValueError, match="scales"):
+        da.diffattn_decode_paged(q, q, p8, pb, v8, table, lens, 0.5, 0.2, L=64, scales=(1, 1, 1))
+    with pytest.raises(ValueError, match="scales"):
+        da.diffattn_kv_append_paged(q, q, torch.zeros(1, 2, 128, dtype=torch.bfloat16), p8, p8, v8, table, lens)
+    with pytest.raises(ValueError, match="both"):
+        da.gemm(torch.zeros(8, 8, dtype=torch.bfloat16), torch.zeros(8, 8, dtype=torch.float16))
 
 
 def test_python_binding_refuses_without_library(tmp_path):
