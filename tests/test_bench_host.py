@@ -27,7 +27,7 @@ def _rank(rank, world, port, out):
 
 
 def test_replicas_take_the_slowest_rank_on_two_gloo_ranks():
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()  # no fork of this multi-threaded process
     out = manager.dict()
     port = 29500 + os.getpid() % 1000
     mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
