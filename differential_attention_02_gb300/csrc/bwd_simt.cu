@@ -25,8 +25,11 @@
 //          dQ1, dQ2;
 //   reduce sums the partials of dlambda and dw in a fixed order.
 // Lane l owns columns l, l + 32, ... of every row it accumulates; rows stream
-// through shared memory 32 at a time with a padded stride (conflict-free
-// lane-strided reads).
+// through shared memory 32 at a time, one warp per row, with a row stride of
+// width + 4 floats: a lane reads its own row 16 bytes at a time and the eight
+// lanes of a quarter-warp land on distinct banks. Dot products run in two
+// independent FMA chains, in the same element order in every kernel, so the
+// scores the key- and query-side passes rebuild equal the row pass's bit for bit.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -57,15 +60,51 @@ __device__ __forceinline__ int64_t row_index(const BwdParams& p, int b, int h, i
     return ((int64_t)b * p.H + h) * p.N + i;
 }
 
+// Rows r0 .. r0 + rows - 1 of operand (b, h) into dst (row stride ld floats): warp w
+// copies rows w, w + kRows, ..., lanes stride the columns. Rows at or past N read 0.
+template <typename T>
+__device__ __forceinline__ void stage_rows(float* dst, int ld, const void* src, const int64_t* s, int b, int h,
+                                           int r0, int rows, int width, int N, int warp, int lane) {
+    for (int r = warp; r < rows; r += kRows) {
+        const bool ok = r0 + r < N;
+        for (int c = lane; c < width; c += 32) dst[r * ld + c] = ok ? ld_op<T>(src, s, b, h, r0 + r, c) : 0.f;
+    }
+}
+
+// The same from a workspace array of per-row records of `width` floats.
+__device__ __forceinline__ void stage_ws_rows(float* dst, int ld, const float* src, const BwdParams& p, int b,
+                                              int h, int r0, int rows, int width, int warp, int lane) {
+    for (int r = warp; r < rows; r += kRows) {
+        const bool ok = r0 + r < p.N;
+        const float* row = src + (ok ? row_index(p, b, h, r0 + r) : 0) * width;
+        for (int c = lane; c < width; c += 32) dst[r * ld + c] = ok ? row[c] : 0.f;
+    }
+}
+
+// sum_c a[c] b[c] over n floats (n a multiple of 4, both 16-byte aligned), two chains.
+__device__ __forceinline__ float dot4(const float* a, const float* b, int n) {
+    const float4* a4 = reinterpret_cast<const float4*>(a);
+    const float4* b4 = reinterpret_cast<const float4*>(b);
+    float x = 0.f, y = 0.f;
+    for (int i = 0; i < n / 4; ++i) {
+        const float4 u = a4[i], v = b4[i];
+        x = fmaf(u.x, v.x, x);
+        y = fmaf(u.y, v.y, y);
+        x = fmaf(u.z, v.z, x);
+        y = fmaf(u.w, v.w, y);
+    }
+    return x + y;
+}
+
 // ------------------------------------------------------------------ rows pass
 template <typename T>
 __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(const BwdParams p) {
     extern __shared__ float smem[];
-    const int d = p.d, Dv = p.Dv, dp = d + 1;
+    const int d = p.d, Dv = p.Dv, dp = d + 4;
     float* q1s = smem;               // [kRows][d]
     float* q2s = q1s + kRows * d;    // [kRows][d]
-    float* k1s = q2s + kRows * d;    // [kChunk][d+1]
-    float* k2s = k1s + kChunk * dp;  // [kChunk][d+1]
+    float* k1s = q2s + kRows * d;    // [kChunk][d+4]
+    float* k2s = k1s + kChunk * dp;  // [kChunk][d+4]
     float* vs = k2s + kChunk * dp;   // [kChunk][Dv]
     float* red_w = vs + kChunk * Dv;  // [kRows][Dv]
     float* red_l = red_w + kRows * Dv;  // [kRows]
@@ -76,12 +115,8 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(const BwdParams p) {
     const int i = row0 + warp;
     const int dvl = Dv / 32;
 
-    for (int t = threadIdx.x; t < kRows * d; t += blockDim.x) {
-        const int r = t / d, c = t % d;
-        const bool ok = row0 + r < p.N;
-        q1s[t] = ok ? ld_op<T>(p.q1, p.sq1, b, h, row0 + r, c) : 0.f;
-        q2s[t] = ok ? ld_op<T>(p.q2, p.sq2, b, h, row0 + r, c) : 0.f;
-    }
+    stage_rows<T>(q1s, d, p.q1, p.sq1, b, h, row0, kRows, d, p.N, warp, lane);
+    stage_rows<T>(q2s, d, p.q2, p.sq2, b, h, row0, kRows, d, p.N, warp, lane);
 
     const float scale = 1.0f / sqrtf((float)d);
     float m1 = -INFINITY, m2 = -INFINITY, l1 = 0.f, l2 = 0.f;
@@ -92,26 +127,16 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(const BwdParams p) {
     const int kend = p.causal ? min(p.N, row0 + kRows) : p.N;
     for (int c0 = 0; c0 < kend; c0 += kChunk) {
         __syncthreads();
-        for (int t = threadIdx.x; t < kChunk * d; t += blockDim.x) {
-            const int r = t / d, c = t % d;
-            const bool ok = c0 + r < p.N;
-            k1s[r * dp + c] = ok ? ld_op<T>(p.k1, p.sk1, b, h, c0 + r, c) : 0.f;
-            k2s[r * dp + c] = ok ? ld_op<T>(p.k2, p.sk2, b, h, c0 + r, c) : 0.f;
-        }
-        for (int t = threadIdx.x; t < kChunk * Dv; t += blockDim.x) {
-            const int r = t / Dv, c = t % Dv;
-            vs[t] = (c0 + r < p.N) ? ld_op<T>(p.v, p.sv, b, h, c0 + r, c) : 0.f;
-        }
+        stage_rows<T>(k1s, dp, p.k1, p.sk1, b, h, c0, kChunk, d, p.N, warp, lane);
+        stage_rows<T>(k2s, dp, p.k2, p.sk2, b, h, c0, kChunk, d, p.N, warp, lane);
+        stage_rows<T>(vs, Dv, p.v, p.sv, b, h, c0, kChunk, Dv, p.N, warp, lane);
         __syncthreads();
         if (i >= p.N) continue;
 
         const int j = c0 + lane;
         const bool visible = (j < p.N) && (!p.causal || j <= i);
-        float s1 = 0.f, s2 = 0.f;
-        for (int c = 0; c < d; ++c) {
-            s1 = fmaf(q1s[warp * d + c], k1s[lane * dp + c], s1);
-            s2 = fmaf(q2s[warp * d + c], k2s[lane * dp + c], s2);
-        }
+        float s1 = dot4(q1s + warp * d, k1s + lane * dp, d);
+        float s2 = dot4(q2s + warp * d, k2s + lane * dp, d);
         s1 = visible ? s1 * scale : -INFINITY;
         s2 = visible ? s2 * scale : -INFINITY;
         const float n1 = fmaxf(m1, warp_max(s1));
@@ -224,13 +249,13 @@ __global__ void __launch_bounds__(kThreads) bwd_rows_kernel(const BwdParams p) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(const BwdParams p) {
     extern __shared__ float smem[];
-    const int d = p.d, Dv = p.Dv, dp = d + 1, dvp = Dv + 1;
+    const int d = p.d, Dv = p.Dv, dp = d + 4, dvp = Dv + 4;
     float* k1w = smem;                 // [kRows][d]   this CTA's keys
     float* k2w = k1w + kRows * d;      // [kRows][d]
     float* vw = k2w + kRows * d;       // [kRows][Dv]
-    float* q1c = vw + kRows * Dv;      // [kChunk][d+1] streamed query rows
-    float* q2c = q1c + kChunk * dp;    // [kChunk][d+1]
-    float* doc = q2c + kChunk * dp;    // [kChunk][Dv+1]
+    float* q1c = vw + kRows * Dv;      // [kChunk][d+4] streamed query rows
+    float* q2c = q1c + kChunk * dp;    // [kChunk][d+4]
+    float* doc = q2c + kChunk * dp;    // [kChunk][Dv+4]
     float* stc = doc + kChunk * dvp;   // [kChunk][4]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -239,16 +264,9 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(const BwdParams p) {
     const int j = key0 + warp;
     const int dl = d / 32, dvl = Dv / 32;
 
-    for (int t = threadIdx.x; t < kRows * d; t += blockDim.x) {
-        const int r = t / d, c = t % d;
-        const bool ok = key0 + r < p.N;
-        k1w[t] = ok ? ld_op<T>(p.k1, p.sk1, b, h, key0 + r, c) : 0.f;
-        k2w[t] = ok ? ld_op<T>(p.k2, p.sk2, b, h, key0 + r, c) : 0.f;
-    }
-    for (int t = threadIdx.x; t < kRows * Dv; t += blockDim.x) {
-        const int r = t / Dv, c = t % Dv;
-        vw[t] = (key0 + r < p.N) ? ld_op<T>(p.v, p.sv, b, h, key0 + r, c) : 0.f;
-    }
+    stage_rows<T>(k1w, d, p.k1, p.sk1, b, h, key0, kRows, d, p.N, warp, lane);
+    stage_rows<T>(k2w, d, p.k2, p.sk2, b, h, key0, kRows, d, p.N, warp, lane);
+    stage_rows<T>(vw, Dv, p.v, p.sv, b, h, key0, kRows, Dv, p.N, warp, lane);
 
     const float scale = 1.0f / sqrtf((float)d);
     float dv[kDVL], dk1[kDL], dk2[kDL];
@@ -261,31 +279,21 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(const BwdParams p) {
     const int qbeg = p.causal ? (key0 / kChunk) * kChunk : 0;
     for (int c0 = qbeg; c0 < p.N; c0 += kChunk) {
         __syncthreads();
-        for (int t = threadIdx.x; t < kChunk * d; t += blockDim.x) {
-            const int r = t / d, c = t % d;
-            const bool ok = c0 + r < p.N;
-            q1c[r * dp + c] = ok ? ld_op<T>(p.q1, p.sq1, b, h, c0 + r, c) : 0.f;
-            q2c[r * dp + c] = ok ? ld_op<T>(p.q2, p.sq2, b, h, c0 + r, c) : 0.f;
-        }
-        for (int t = threadIdx.x; t < kChunk * Dv; t += blockDim.x) {
-            const int r = t / Dv, c = t % Dv;
-            doc[r * dvp + c] = (c0 + r < p.N) ? p.d_o[row_index(p, b, h, c0 + r) * Dv + c] : 0.f;
-        }
-        for (int t = threadIdx.x; t < kChunk * 4; t += blockDim.x) {
-            const int r = t / 4;
-            stc[t] = (c0 + r < p.N) ? p.stats[row_index(p, b, h, c0 + r) * 4 + (t % 4)] : 0.f;
+        stage_rows<T>(q1c, dp, p.q1, p.sq1, b, h, c0, kChunk, d, p.N, warp, lane);
+        stage_rows<T>(q2c, dp, p.q2, p.sq2, b, h, c0, kChunk, d, p.N, warp, lane);
+        stage_ws_rows(doc, dvp, p.d_o, p, b, h, c0, kChunk, Dv, warp, lane);
+        if (threadIdx.x < kChunk * 4) {
+            const int r = threadIdx.x / 4;
+            stc[threadIdx.x] = (c0 + r < p.N) ? p.stats[row_index(p, b, h, c0 + r) * 4 + (threadIdx.x % 4)] : 0.f;
         }
         __syncthreads();
         if (j >= p.N) continue;
 
         const int i = c0 + lane;  // this lane's query row
         const bool visible = (i < p.N) && (!p.causal || j <= i);
-        float s1 = 0.f, s2 = 0.f, da = 0.f;
-        for (int c = 0; c < d; ++c) {
-            s1 = fmaf(q1c[lane * dp + c], k1w[warp * d + c], s1);
-            s2 = fmaf(q2c[lane * dp + c], k2w[warp * d + c], s2);
-        }
-        for (int c = 0; c < Dv; ++c) da = fmaf(doc[lane * dvp + c], vw[warp * Dv + c], da);
+        const float s1 = dot4(q1c + lane * dp, k1w + warp * d, d);
+        const float s2 = dot4(q2c + lane * dp, k2w + warp * d, d);
+        const float da = dot4(doc + lane * dvp, vw + warp * Dv, Dv);
         const float p1 = visible ? expf(s1 * scale - stc[lane * 4 + 0]) : 0.f;
         const float p2 = visible ? expf(s2 * scale - stc[lane * 4 + 1]) : 0.f;
         const float a = p1 - p.lambda * p2;
@@ -327,13 +335,13 @@ __global__ void __launch_bounds__(kThreads) bwd_kv_kernel(const BwdParams p) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdParams p) {
     extern __shared__ float smem[];
-    const int d = p.d, Dv = p.Dv, dp = d + 1, dvp = Dv + 1;
+    const int d = p.d, Dv = p.Dv, dp = d + 4, dvp = Dv + 4;
     float* q1w = smem;                 // [kRows][d]   this CTA's query rows
     float* q2w = q1w + kRows * d;      // [kRows][d]
     float* dow = q2w + kRows * d;      // [kRows][Dv]
-    float* k1c = dow + kRows * Dv;     // [kChunk][d+1] streamed keys
-    float* k2c = k1c + kChunk * dp;    // [kChunk][d+1]
-    float* vc = k2c + kChunk * dp;     // [kChunk][Dv+1]
+    float* k1c = dow + kRows * Dv;     // [kChunk][d+4] streamed keys
+    float* k2c = k1c + kChunk * dp;    // [kChunk][d+4]
+    float* vc = k2c + kChunk * dp;     // [kChunk][Dv+4]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, h = blockIdx.y;
@@ -341,16 +349,9 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdParams p) {
     const int i = row0 + warp;
     const int dl = d / 32;
 
-    for (int t = threadIdx.x; t < kRows * d; t += blockDim.x) {
-        const int r = t / d, c = t % d;
-        const bool ok = row0 + r < p.N;
-        q1w[t] = ok ? ld_op<T>(p.q1, p.sq1, b, h, row0 + r, c) : 0.f;
-        q2w[t] = ok ? ld_op<T>(p.q2, p.sq2, b, h, row0 + r, c) : 0.f;
-    }
-    for (int t = threadIdx.x; t < kRows * Dv; t += blockDim.x) {
-        const int r = t / Dv, c = t % Dv;
-        dow[t] = (row0 + r < p.N) ? p.d_o[row_index(p, b, h, row0 + r) * Dv + c] : 0.f;
-    }
+    stage_rows<T>(q1w, d, p.q1, p.sq1, b, h, row0, kRows, d, p.N, warp, lane);
+    stage_rows<T>(q2w, d, p.q2, p.sq2, b, h, row0, kRows, d, p.N, warp, lane);
+    stage_ws_rows(dow, Dv, p.d_o, p, b, h, row0, kRows, Dv, warp, lane);
     float lse1 = 0.f, lse2 = 0.f, D1 = 0.f, D2 = 0.f;
     if (i < p.N) {
         const float* st = p.stats + row_index(p, b, h, i) * 4;
@@ -368,27 +369,17 @@ __global__ void __launch_bounds__(kThreads) bwd_q_kernel(const BwdParams p) {
     const int kend = p.causal ? min(p.N, row0 + kRows) : p.N;
     for (int c0 = 0; c0 < kend; c0 += kChunk) {
         __syncthreads();
-        for (int t = threadIdx.x; t < kChunk * d; t += blockDim.x) {
-            const int r = t / d, c = t % d;
-            const bool ok = c0 + r < p.N;
-            k1c[r * dp + c] = ok ? ld_op<T>(p.k1, p.sk1, b, h, c0 + r, c) : 0.f;
-            k2c[r * dp + c] = ok ? ld_op<T>(p.k2, p.sk2, b, h, c0 + r, c) : 0.f;
-        }
-        for (int t = threadIdx.x; t < kChunk * Dv; t += blockDim.x) {
-            const int r = t / Dv, c = t % Dv;
-            vc[r * dvp + c] = (c0 + r < p.N) ? ld_op<T>(p.v, p.sv, b, h, c0 + r, c) : 0.f;
-        }
+        stage_rows<T>(k1c, dp, p.k1, p.sk1, b, h, c0, kChunk, d, p.N, warp, lane);
+        stage_rows<T>(k2c, dp, p.k2, p.sk2, b, h, c0, kChunk, d, p.N, warp, lane);
+        stage_rows<T>(vc, dvp, p.v, p.sv, b, h, c0, kChunk, Dv, p.N, warp, lane);
         __syncthreads();
         if (i >= p.N) continue;
 
         const int j = c0 + lane;  // this lane's key
         const bool visible = (j < p.N) && (!p.causal || j <= i);
-        float s1 = 0.f, s2 = 0.f, da = 0.f;
-        for (int c = 0; c < d; ++c) {
-            s1 = fmaf(q1w[warp * d + c], k1c[lane * dp + c], s1);
-            s2 = fmaf(q2w[warp * d + c], k2c[lane * dp + c], s2);
-        }
-        for (int c = 0; c < Dv; ++c) da = fmaf(dow[warp * Dv + c], vc[lane * dvp + c], da);
+        const float s1 = dot4(q1w + warp * d, k1c + lane * dp, d);
+        const float s2 = dot4(q2w + warp * d, k2c + lane * dp, d);
+        const float da = dot4(dow + warp * Dv, vc + lane * dvp, Dv);
         const float p1 = visible ? expf(s1 * scale - lse1) : 0.f;
         const float p2 = visible ? expf(s2 * scale - lse2) : 0.f;
         const float ds1 = p1 * (da - D1);
@@ -442,12 +433,12 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(const BwdParams p, int6
 template <typename T>
 cudaError_t launch_typed(const BwdParams& p, cudaStream_t stream) {
     const int d = p.d, Dv = p.Dv;
-    const size_t s_rows = sizeof(float) * (size_t)(2 * kRows * d + 2 * kChunk * (d + 1) + kChunk * Dv +
+    const size_t s_rows = sizeof(float) * (size_t)(2 * kRows * d + 2 * kChunk * (d + 4) + kChunk * Dv +
                                                    kRows * Dv + kRows);
-    const size_t s_kv = sizeof(float) * (size_t)(2 * kRows * d + kRows * Dv + 2 * kChunk * (d + 1) +
-                                                 kChunk * (Dv + 1) + kChunk * 4);
-    const size_t s_q = sizeof(float) * (size_t)(2 * kRows * d + kRows * Dv + 2 * kChunk * (d + 1) +
-                                                kChunk * (Dv + 1));
+    const size_t s_kv = sizeof(float) * (size_t)(2 * kRows * d + kRows * Dv + 2 * kChunk * (d + 4) +
+                                                 kChunk * (Dv + 4) + kChunk * 4);
+    const size_t s_q = sizeof(float) * (size_t)(2 * kRows * d + kRows * Dv + 2 * kChunk * (d + 4) +
+                                                kChunk * (Dv + 4));
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(bwd_rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_rows)) ||
         (e = cudaFuncSetAttribute(bwd_kv_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_kv)) ||
