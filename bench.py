@@ -137,19 +137,26 @@ class ClockSampler:
             self.max_mhz = mx.value
         return nv, h, getr
 
-    def _loop(self):
+    def _sample(self):
         import ctypes
         nv, h, getr = self.nvml
         mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
-        while not self.stop.is_set():
+        try:
             if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and getr(h, ctypes.byref(rs)) == 0:
                 self.samples.append((mhz.value, rs.value))
+        except (OSError, ctypes.ArgumentError):  # a failed read is a missing sample, not a failed run
+            pass
+
+    def _loop(self):
+        while not self.stop.is_set():
+            self._sample()
             time.sleep(0.001)
 
     def __enter__(self):
         import threading
         try:
             self.nvml = self._open_nvml()
+            self._sample()  # one sample at the start of the region, whatever the thread manages
             self.thread = threading.Thread(target=self._loop, daemon=True)
             self.thread.start()
         except (OSError, AttributeError):
@@ -170,6 +177,7 @@ class ClockSampler:
         if self.thread is not None:
             self.stop.set()
             self.thread.join(timeout=2)
+            self._sample()  # and one at its end, right after the closing synchronize
         if self.proc is not None:
             self.proc.terminate()
             self.proc.wait(timeout=5)

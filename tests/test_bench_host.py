@@ -56,3 +56,36 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"],
                        cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_clock_sampler_brackets_the_region_with_a_fake_nvml(monkeypatch):
+    """The NVML path on a stand-in library: samples at the start and end of the region
+    (plus whatever the thread adds), median clock, and throttle reasons decoded."""
+    import ctypes
+
+    class FakeNvml:
+        def __init__(self):
+            self.calls = 0
+
+        def nvmlDeviceGetClockInfo(self, h, kind, out):
+            self.calls += 1
+            ctypes.cast(out, ctypes.POINTER(ctypes.c_uint))[0] = 1900 + 10 * (self.calls % 3)
+            return 0
+
+    fake = FakeNvml()
+
+    def reasons(h, out):
+        ctypes.cast(out, ctypes.POINTER(ctypes.c_ulonglong))[0] = 0x4  # sw_power_cap
+        return 0
+
+    def fake_open(self):
+        self.max_mhz = 2070
+        return fake, None, reasons
+
+    monkeypatch.setattr(bench.ClockSampler, "_open_nvml", fake_open)
+    with bench.ClockSampler(0) as clk:
+        pass
+    out = clk.summary()
+    assert out["source"] == "nvml" and out["samples"] >= 2
+    assert out["sm_max_mhz"] == 2070 and 1900 <= out["sm_mhz"] <= 1920
+    assert out["reasons"] == ["sw_power_cap"]
