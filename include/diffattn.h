@@ -155,7 +155,9 @@ diffattn_status diffattn_decode(const void* q1, const void* q2,
                                 int num_splits, int out_dtype,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes for diffattn_decode with these sizes; num_splits as above. */
+/* Workspace bytes for diffattn_decode with these sizes; num_splits as above. Also
+ * large enough for diffattn_decode_paged and diffattn_decode_paged_fp8 with the
+ * same sizes (the fp8 decode may choose more splits; the larger count is used). */
 diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int Dv, int num_splits, size_t* bytes);
 
 /*
@@ -170,9 +172,9 @@ diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int D
  * Arguments are those of diffattn_decode without workspace/workspace_bytes.
  * Scratch: a file-scope device array of DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES
  * (8 MiB) that every GPU loading the library holds until process exit. Calls
- * whose partial states need more (diffattn_decode_workspace_size() for the same
- * arguments larger than the limit) are rejected with DIFFATTN_ERR_WORKSPACE
- * before anything is launched.
+ * whose partial states need more (the split states diffattn_decode would use for
+ * the same arguments larger than the limit) are rejected with
+ * DIFFATTN_ERR_WORKSPACE before anything is launched.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current), so make that first call
  * before any stream capture. No call allocates or frees device memory.
