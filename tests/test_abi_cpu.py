@@ -46,10 +46,17 @@ def test_header_is_plain_c_and_links_against_the_library(lib, tmp_path):
         pytest.skip("no C compiler")
     names = _declared_functions()
     src = tmp_path / "use_header.c"
+    # Besides referencing every entry point, the program calls the host-only ones: lambda for
+    # layer 1 from zero vectors is exp(0) - exp(0) + 0.2 = 0.2, and a status string.
     src.write_text('#include "diffattn.h"\n#include <stdio.h>\ntypedef void (*fn_t)(void);\n'
                    "int main(void) {\n    fn_t fns[] = {\n"
                    + "".join(f"        (fn_t)&{n},\n" for n in names)
-                   + "    };\n    printf(\"%d\\n\", (int)(sizeof fns / sizeof fns[0]));\n    return 0;\n}\n")
+                   + "    };\n"
+                   "    float z[4] = {0.f, 0.f, 0.f, 0.f}, lam = -1.f, lam_init = -1.f;\n"
+                   "    diffattn_status st = diffattn_lambda(z, z, z, z, 4, 1, -1.f, &lam, &lam_init);\n"
+                   "    printf(\"%d %d %.6f %.6f %s\\n\", (int)(sizeof fns / sizeof fns[0]), (int)st, lam, lam_init,\n"
+                   "           diffattn_status_string(DIFFATTN_ERR_WORKSPACE));\n"
+                   "    return 0;\n}\n")
     pkg = os.path.dirname(da.__file__)
     out = tmp_path / "use_header"
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
@@ -58,7 +65,11 @@ def test_header_is_plain_c_and_links_against_the_library(lib, tmp_path):
     assert r.returncode == 0, r.stderr
     # The library carries the CUDA runtime statically: the program loads it with nothing else.
     r = subprocess.run([str(out)], capture_output=True, text=True, env={**os.environ, "LD_LIBRARY_PATH": pkg})
-    assert r.returncode == 0 and r.stdout.strip() == str(len(names)), (r.stdout, r.stderr)
+    assert r.returncode == 0, r.stderr
+    count, status, lam, lam_init, text = r.stdout.split(maxsplit=4)
+    assert int(count) == len(names) and int(status) == da.OK
+    assert float(lam) == pytest.approx(0.2, abs=1e-6) and float(lam_init) == pytest.approx(0.2, abs=1e-6)
+    assert text.strip() == da.status_string(da.ERR_WORKSPACE)
 
 
 def test_status_strings(lib):
