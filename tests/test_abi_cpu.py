@@ -164,6 +164,23 @@ def test_decode_and_gemm_argument_validation(lib):
         assert g(N=250) == da.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("B,H,L,d", [(1, 1, 64, 64), (3, 4, 1000, 64), (64, 16, 8192, 64), (8, 16, 65536, 64),
+                                     (2, 8, 300, 128), (128, 32, 4096, 128)])
+def test_decode_auto_split_count_bounds(lib, B, H, L, d):
+    """The automatic split count (read back from the workspace size) is at least 1, keeps at
+    least 256 keys per split when it splits, and never exceeds 256."""
+    Dv = 2 * d
+    n = ctypes.c_size_t()
+    assert lib.diffattn_decode_workspace_size(B, H, L, d, Dv, 0, ctypes.byref(n)) == da.OK
+    per_split = B * H * (4 * 4 + 2 * Dv * 4)
+    S, rem = divmod(n.value - 256, per_split)
+    assert rem == 0 and 1 <= S <= 256
+    assert S == 1 or L // S >= 256  # a split of a longer cache keeps at least 256 keys
+    # an explicit count is taken as given (up to empty trailing splits)
+    assert lib.diffattn_decode_workspace_size(B, H, L, d, Dv, 1, ctypes.byref(n)) == da.OK
+    assert n.value == 256 + per_split
+
+
 def test_paged_decode_argument_validation(lib):
     t = _tensor(sb=2 * 64 * 64, sh=64 * 64, sn=64)  # [pages, H_kv=2, 64, 64]
     vp = ctypes.c_void_p
