@@ -24,7 +24,7 @@ EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffat
             "diffattn_gemm_workspace_size", "diffattn_read_error", "diffattn_decode_noalloc",
             "diffattn_decode_paged", "diffattn_kv_append_paged", "diffattn_add_rmsnorm", "diffattn_swiglu",
             "diffattn_bwd", "diffattn_bwd_workspace_size", "diffattn_lambda_bwd", "diffattn_decode_paged_fp8",
-            "diffattn_kv_append_paged_fp8",
+            "diffattn_kv_append_paged_fp8", "diffattn_decode_noalloc_read_error",
             "diffattn_selftest_timeout")
 
 
@@ -76,6 +76,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_decode_noalloc.restype = i32
     lib.diffattn_decode_noalloc.argtypes = [vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, vp, vp, i32, i32, i32, i32,
                                             f32, f32, f32, i32, i32, vp]
+    lib.diffattn_decode_noalloc_read_error.restype = i32
+    lib.diffattn_decode_noalloc_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.diffattn_decode_paged.restype = i32
     lib.diffattn_decode_paged.argtypes = [vp, vp, Tensor4, Tensor4, Tensor4, vp, i32, i32, vp, i32, vp, vp, i32, i32,
                                           i32, i32, i32, f32, f32, f32, i32, i32, vp, sz, vp]
@@ -419,24 +421,32 @@ gemm_bf16 = gemm
 
 
 def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float, eps: float = 1e-5,
-               norm_weight=None, ws=None, stream=None, out_dtype=torch.bfloat16):
+               norm_weight=None, ws=None, stream=None, out_dtype=torch.bfloat16, qkv_dtype=torch.float16):
     """Multi-head differential attention module: three projection GEMMs, the fused
     attention reading Q/K/V in place through strided views, and the W_O GEMM.
 
     x [B,N,d_model]; w_q, w_k [d_model, h*2d]; w_v [d_model, h*Dv]; w_o [h*Dv, d_model],
     all bf16 or all fp16. Head i uses Q[..., 2di:2di+d] as Q1 and Q[..., 2di+d:2d(i+1)] as Q2
-    (K likewise). The projections are written in fp16 (bf16 rounding of Q, K and V
-    alone would cost about 3e-3 relative error at the output); the attention output
-    that W_O multiplies has the operands' type.
+    (K likewise). The projections are written as qkv_dtype: fp16 by default (bf16
+    rounding of Q, K and V alone would cost about 3e-3 relative error at the output);
+    the attention output that W_O multiplies has the operands' type.
+
+    Range: fp16 holds projections up to 65504 in magnitude; an entry beyond that
+    overflows to infinity in the GEMM epilogue and the module's output is not
+    finite. Inputs normalised before the projections (as in the layer) stay far
+    inside it. For wider activations pass qkv_dtype=torch.bfloat16 (the range of
+    fp32, 8 significant bits instead of 11).
     """
+    if qkv_dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("qkv_dtype must be torch.float16 or torch.bfloat16")
     B, N, dm = x.shape
     h = n_heads
     d = w_q.shape[1] // (2 * h)
     Dv = w_v.shape[1] // h
     x2 = x.reshape(B * N, dm)
-    q = gemm(x2, w_q, out_dtype=torch.float16, ws=ws, stream=stream)
-    k = gemm(x2, w_k, out_dtype=torch.float16, ws=ws, stream=stream)
-    v = gemm(x2, w_v, out_dtype=torch.float16, ws=ws, stream=stream)
+    q = gemm(x2, w_q, out_dtype=qkv_dtype, ws=ws, stream=stream)
+    k = gemm(x2, w_k, out_dtype=qkv_dtype, ws=ws, stream=stream)
+    v = gemm(x2, w_v, out_dtype=qkv_dtype, ws=ws, stream=stream)
     # [B*N, h*2d] -> [B, h, N, 2d] views (no copies): strides (N*h*2d, 2d, h*2d, 1)
     q4 = q.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
     k4 = k.view(B, N, h, 2 * d).permute(0, 2, 1, 3)

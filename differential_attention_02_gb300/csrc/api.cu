@@ -254,11 +254,16 @@ diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int D
     return DIFFATTN_OK;
 }
 
-diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor k1_cache, diffattn_tensor k2_cache,
-                                diffattn_tensor v_cache, const int32_t* seq_lens, int L, void* out,
-                                const float* norm_weight, int B, int H, int d, int Dv, float lambda,
-                                float lambda_init, float eps, int num_splits, int out_dtype, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// Every host check of diffattn_decode except the workspace: sizes, dtypes,
+// scalars, pointers, alignment, operand strides and the (d, Dv) pair. With
+// B == 0 or H == 0 only the size, dtype and scalar checks apply (nothing runs).
+diffattn_status decode_check_args(const void* q1, const void* q2, const diffattn_tensor& k1_cache,
+                                  const diffattn_tensor& k2_cache, const diffattn_tensor& v_cache, int L,
+                                  const void* out, const float* norm_weight, int B, int H, int d, int Dv, float lambda,
+                                  float lambda_init, float eps, int num_splits, int out_dtype) {
     if (B < 0 || H < 0 || L < 1 || d < 1 || Dv < 1 || num_splits < 0 || num_splits > 256)
         return DIFFATTN_ERR_INVALID_ARG;
     if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16) return DIFFATTN_ERR_INVALID_ARG;
@@ -270,6 +275,20 @@ diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor 
         return DIFFATTN_ERR_INVALID_ARG;
     if (norm_weight != nullptr && !aligned16(norm_weight)) return DIFFATTN_ERR_INVALID_ARG;
     if (!((d == 64 && Dv == 128) || (d == 128 && Dv == 256))) return DIFFATTN_ERR_UNSUPPORTED;
+    return DIFFATTN_OK;
+}
+}  // namespace
+
+extern "C" {
+
+diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor k1_cache, diffattn_tensor k2_cache,
+                                diffattn_tensor v_cache, const int32_t* seq_lens, int L, void* out,
+                                const float* norm_weight, int B, int H, int d, int Dv, float lambda,
+                                float lambda_init, float eps, int num_splits, int out_dtype, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    const diffattn_status chk = decode_check_args(q1, q2, k1_cache, k2_cache, v_cache, L, out, norm_weight, B, H, d,
+                                                  Dv, lambda, lambda_init, eps, num_splits, out_dtype);
+    if (chk != DIFFATTN_OK || B == 0 || H == 0) return chk;
     DecodeParams p{};
     decode_geometry(B, H, L, d, num_splits, &p.num_splits, &p.keys_per_split);
     const size_t need = decode_ws_bytes(B, H, p.num_splits, Dv);
@@ -577,34 +596,33 @@ diffattn_status diffattn_decode_paged_fp8(const void* q1, const void* q2, diffat
 // symbol as an address; it looks the device address up per device.
 static __device__ __align__(256) uint8_t g_decode_scratch[DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES];
 
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+}  // extern "C"
 
-// Device address of g_decode_scratch on the current device (looked up once per device).
+namespace {
+// Device address of g_decode_scratch in the current device's context. It is
+// looked up on every call rather than cached: a device reset reloads the
+// module, and the array may then sit at another address. Once the module is
+// loaded on a device the lookup costs little; the first lookup on a device
+// loads it, which is why the first call must precede any stream capture.
 void* decode_scratch_address() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = ptr;
-    }
-    return g_scratch_addr[dev];
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) return nullptr;
+    return ptr;
 }
 }  // namespace
+
+extern "C" {
 
 diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2, diffattn_tensor k1_cache,
                                         diffattn_tensor k2_cache, diffattn_tensor v_cache, const int32_t* seq_lens,
                                         int L, void* out, const float* norm_weight, int B, int H, int d, int Dv,
                                         float lambda, float lambda_init, float eps, int num_splits, int out_dtype,
                                         void* stream) {
-    size_t need = 0;
-    const diffattn_status st = diffattn_decode_workspace_size(B, H, L, d, Dv, num_splits, &need);
-    if (st != DIFFATTN_OK) return st;
-    if (B == 0 || H == 0) return DIFFATTN_OK;
+    // The argument checks come first, so a bad call writes nothing to the shared
+    // scratch (whose error word a call in flight on another stream may own).
+    const diffattn_status chk = decode_check_args(q1, q2, k1_cache, k2_cache, v_cache, L, out, norm_weight, B, H, d,
+                                                  Dv, lambda, lambda_init, eps, num_splits, out_dtype);
+    if (chk != DIFFATTN_OK || B == 0 || H == 0) return chk;
     int S, kps;  // the bf16-cache geometry diffattn_decode will use
     decode_geometry(B, H, L, d, num_splits, &S, &kps, false);
     if (decode_ws_bytes(B, H, S, Dv) > sizeof(g_decode_scratch)) return DIFFATTN_ERR_WORKSPACE;
@@ -615,6 +633,13 @@ diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2, diffattn
         return DIFFATTN_ERR_CUDA;
     return diffattn_decode(q1, q2, k1_cache, k2_cache, v_cache, seq_lens, L, out, norm_weight, B, H, d, Dv, lambda,
                            lambda_init, eps, num_splits, out_dtype, scratch, sizeof(g_decode_scratch), stream);
+}
+
+diffattn_status diffattn_decode_noalloc_read_error(void* stream, int32_t* device_code) {
+    if (!device_code) return DIFFATTN_ERR_INVALID_ARG;
+    void* scratch = decode_scratch_address();
+    if (scratch == nullptr) return DIFFATTN_ERR_CUDA;
+    return diffattn_read_error(scratch, stream, device_code);
 }
 
 diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes) {

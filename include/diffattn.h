@@ -108,6 +108,14 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
  * accumulation (the probability tile P is rounded to the operand type for the
  * P.V product). out_dtype f32 or bf16 for every in_dtype; f16 as well for bf16
  * and f16 inputs.
+ * Range: scores, running maxima, row sums and accumulators are fp32 and every
+ *   P entry is at most 2^8 (the running maximum is refreshed whenever a row's
+ *   maximum grows by more than 8 in log2 units), so any finite input of the
+ *   operand type is in range, however large its scores. Precision: the output's
+ *   sensitivity to the rounding of Q and K grows with the scores' magnitude, as
+ *   for any softmax. An f16 out_dtype saturates nothing: |y| beyond 65504 would
+ *   be infinite, but y is RMS-normalised (|y| <= sqrt(Dv) * |weight| *
+ *   |1 - lambda_init|).
  * B, H or N equal to 0: nothing to do, returns DIFFATTN_OK.
  * workspace: at least diffattn_fwd_workspace_size() bytes, 256-byte aligned;
  *   its first 4 bytes are the device error word, which must be zero before the
@@ -175,16 +183,20 @@ diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int D
  * whose partial states need more (the split states diffattn_decode would use for
  * the same arguments larger than the limit) are rejected with
  * DIFFATTN_ERR_WORKSPACE before anything is launched.
- * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current), so make that first call
- * before any stream capture. No call allocates or frees device memory.
+ * Set-up: every call looks up the array's device address in the current
+ * device's context (cudaGetSymbolAddress). The first lookup on a device loads
+ * the library's device code there, so make the first call on each device before
+ * any stream capture. Looking the address up each time keeps it right after a
+ * device reset, which reloads the code and may move the array. No call
+ * allocates or frees device memory.
+ * Errors: the arguments are checked exactly as diffattn_decode checks them,
+ * before the scratch is touched, so a rejected call writes nothing to it.
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents; the error word is cleared (cudaMemsetAsync on `stream`) at
  * the start of each call. Calls that overlap on the GPU (different streams
  * without ordering) race on the array and give undefined results. A device-side
- * wait that gives up is recorded only in that private error word, which
- * diffattn_read_error cannot reach; use diffattn_decode when that report is
- * needed.
+ * wait that gives up is recorded in the array's error word: read it with
+ * diffattn_decode_noalloc_read_error before the next call clears it.
  */
 #define DIFFATTN_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
 diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2,
@@ -193,6 +205,15 @@ diffattn_status diffattn_decode_noalloc(const void* q1, const void* q2,
                                         void* out, const float* norm_weight,
                                         int B, int H, int d, int Dv, float lambda, float lambda_init, float eps,
                                         int num_splits, int out_dtype, void* stream);
+
+/* diffattn_decode_noalloc_read_error — host only: reads the error word of the
+ * no-allocation decode's scratch on the current device, after synchronising
+ * `stream`, and clears it when it is set, like diffattn_read_error does for a
+ * workspace. *device_code receives the raw device code (0 = no error).
+ * Returns DIFFATTN_OK when it was 0, DIFFATTN_ERR_TIMEOUT when a device-side
+ * wait gave up, DIFFATTN_ERR_CUDA if the copy or the address lookup failed,
+ * DIFFATTN_ERR_INVALID_ARG if device_code is NULL. No counterpart in the pages. */
+diffattn_status diffattn_decode_noalloc_read_error(void* stream, int32_t* device_code);
 
 /*
  * diffattn_decode_paged — diffattn_decode against a paged KV cache, with query

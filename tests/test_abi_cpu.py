@@ -164,6 +164,29 @@ def test_decode_and_gemm_argument_validation(lib):
         assert g(N=250) == da.ERR_INVALID_ARG
 
 
+def test_noalloc_decode_argument_validation(lib):
+    """The no-allocation decode checks its arguments like diffattn_decode before it
+    looks up or writes its scratch, so these return without touching a device."""
+    t = _tensor()
+    vp = ctypes.c_void_p
+    call = lambda **kw: lib.diffattn_decode_noalloc(
+        vp(kw.get("q1", 0x1000)), vp(0x1000), kw.get("k1", t), t, kw.get("v", _tensor(sn=128)), None,
+        kw.get("L", 64), vp(kw.get("out", 0x2000)), vp(kw.get("w")) if kw.get("w") else None, kw.get("B", 2), 2,
+        kw.get("d", 64), 128, kw.get("lam", 0.5), 0.2, 1e-5, kw.get("S", 0), kw.get("outd", da.F32), None)
+    assert call(B=0) == da.OK
+    assert call(L=0) == da.ERR_INVALID_ARG
+    assert call(S=300) == da.ERR_INVALID_ARG
+    assert call(q1=0) == da.ERR_INVALID_ARG
+    assert call(q1=0x1008) == da.ERR_INVALID_ARG                # misaligned
+    assert call(out=0) == da.ERR_INVALID_ARG
+    assert call(w=0x3004) == da.ERR_INVALID_ARG                 # misaligned norm weight
+    assert call(k1=_tensor(sn=60)) == da.ERR_INVALID_ARG        # row stride < d
+    assert call(outd=da.F16) == da.ERR_INVALID_ARG              # decode outputs fp32 or bf16
+    assert call(lam=float("inf")) == da.ERR_INVALID_ARG
+    assert call(d=32, k1=_tensor(sn=32)) == da.ERR_UNSUPPORTED
+    assert lib.diffattn_decode_noalloc_read_error(None, None) == da.ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("B,H,L,d", [(1, 1, 64, 64), (3, 4, 1000, 64), (64, 16, 8192, 64), (8, 16, 65536, 64),
                                      (2, 8, 300, 128), (128, 32, 4096, 128)])
 def test_decode_auto_split_count_bounds(lib, B, H, L, d):
