@@ -294,8 +294,9 @@ def run_e2e(args, da, w, host, lv, out_shape, dev, stream, world):
 
 
 def time_device(fn, steps, warmup, stream, flush=None):
-    """Mean CUDA-event time (ms) of fn() over `steps` calls after `warmup` calls;
-    with `flush`, L2 is evicted (untimed) before each timed call."""
+    """Median CUDA-event time (ms) of fn() over `steps` calls after `warmup` calls,
+    each call bracketed by its own pair of events on `stream`; with `flush`, L2 is
+    evicted (untimed) before each timed call."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -307,7 +308,12 @@ def time_device(fn, steps, warmup, stream, flush=None):
         fn()
         b.record(stream)
     torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in ev) / steps
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def extra_reps(args) -> int:
+    """Timed calls per extra workload: at least 20, more when the run asks for more steps."""
+    return max(20, args.steps)
 
 
 def run_long_prefill(args, da, gi, dev, stream, peaks, peak_kind):
@@ -320,7 +326,7 @@ def run_long_prefill(args, da, gi, dev, stream, peaks, peak_kind):
     ws = da.workspace(256, dev)
     fn = lambda: da.diffattn_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam, lam_init, w.eps,
                                  out_dtype=torch.bfloat16, out=out, ws=ws, stream=stream)
-    ms = time_device(fn, max(3, args.steps // 4), args.warmup, stream)
+    ms = time_device(fn, extra_reps(args), args.warmup, stream)
     assert da.read_error(ws) == 0
     tf = prefill_def_flops(w) / (ms * 1e-3) / 1e12
     return {"workload": "prefill B1 H16 N16384 d64 Dv128 causal, layer 12, bf16 in/out", "ms_per_step": ms,
@@ -340,7 +346,7 @@ def run_module(args, da, gi, dev, stream, peaks, peak_kind):
     ws = da.workspace(256, dev)
     fn = lambda: da.module_fwd(t["x"], t["w_q"], t["w_k"], t["w_v"], t["w_o"], w.H, lam, lam_init, w.eps, ws=ws,
                                stream=stream)
-    ms = time_device(fn, max(3, args.steps // 4), args.warmup, stream)
+    ms = time_device(fn, extra_reps(args), args.warmup, stream)
     assert da.read_error(ws) == 0
     n_pairs = w.N * (w.N + 1) / 2
     att = w.B * w.H * (4 * n_pairs * w.d + 2 * n_pairs * w.Dv)
@@ -368,7 +374,7 @@ def run_layer(args, da, gi, dev, stream, peaks, peak_kind):
     ws = da.workspace(256, dev)
     fn = lambda: da.layer_fwd(t["x"], t["w_q"], t["w_k"], t["w_v"], t["w_o"], wgu, t["w_down"], w.H, lam, lam_init,
                               w.eps, ws=ws, stream=stream)
-    ms = time_device(fn, max(3, args.steps // 4), args.warmup, stream)
+    ms = time_device(fn, extra_reps(args), args.warmup, stream)
     assert da.read_error(ws) == 0
     n_pairs = w.N * (w.N + 1) / 2
     att = w.B * w.H * (4 * n_pairs * w.d + 2 * n_pairs * w.Dv)
@@ -394,18 +400,22 @@ def run_backward(args, da, gi, dev, stream, peaks, peak_kind):
     ws = da.workspace(da.bwd_workspace_bytes(w.B, w.H, w.N, w.d, w.Dv), dev)
     fn = lambda: da.diffattn_bwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], dy, lam, lam_init, w.eps,
                                  want_dnorm_weight=True, ws=ws, stream=stream)
-    ms = time_device(fn, max(3, args.steps // 4), args.warmup, stream)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = time_device(fn, extra_reps(args), args.warmup, stream)
     n_pairs = w.N * (w.N + 1) / 2
     # Chain-rule FLOPs per (b, h): per map S recomputed, dQ and dK (2 Np d each); dV and dA (2 Np Dv each).
     flops = w.B * w.H * (12 * n_pairs * w.d + 4 * n_pairs * w.Dv)
     tf = flops / (ms * 1e-3) / 1e12
-    # CUDA-core fp32 peak: 152 SMs x 128 FMA lanes x 2 FLOP x the sampled SM clock.
-    sm_mhz = 2070.0
-    alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    # CUDA-core fp32 peak: SMs x 128 FMA lanes x 2 FLOP x the SM clock sampled while the backward ran
+    # (the maximum clock when no sample could be taken).
+    c = clk.summary()
+    sm_mhz = c["sm_mhz"] or c["sm_max_mhz"] or 2070.0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12
     return {"workload": "backward of the prefill workload B4 H16 N2048 d64 Dv128 causal, bf16 in, fp32 gradients",
             "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "flops_per_step": flops,
             "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
-                         "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 x 2070 MHz"},
+                         "peak_kind": f"derived: {sms} SMs x 128 fp32 lanes x 2 x {sm_mhz:.0f} MHz (sampled)"},
             "gpu_launches_per_step": 4}
 
 
@@ -438,7 +448,7 @@ def run_decode(args, da, gi, dev, stream, peaks, peak_kind):
         dev_ev[i][1].record(stream)
     torch.cuda.synchronize()
     assert da.read_error(dws) == 0
-    dms = sum(a.elapsed_time(b) for a, b in dev_ev) / args.steps
+    dms = statistics.median(a.elapsed_time(b) for a, b in dev_ev)
     kvb = decode_kv_bytes(wd)
     gbs = kvb / (dms * 1e-3) / 1e9
     per_seq = profiled_traffic("decode_split_per_sequence_H16L8192", ["decode_bf16.cu", "common.cuh", "kernels.h"])
@@ -477,7 +487,7 @@ def run_serving(args, da, wd, y, lam, lam_init, dev, stream, peaks, kvb):
         da.diffattn_decode_paged(y["q1"], y["q2"], pools["k1"], pools["k2"], pools["v"], table, lens, lam,
                                  lam_init, L=L, eps=wd.eps, out_dtype=torch.bfloat16, out=out, ws=ws, stream=stream)
 
-    ms = time_device(step, args.steps, max(3, args.warmup), stream)
+    ms = time_device(step, extra_reps(args), max(3, args.warmup), stream)
     assert da.read_error(ws) == 0
     gbs = kvb / (ms * 1e-3) / 1e9
     res = {"workload": f"decode {B} seqs, H{H}, L{L}: new token appended to a paged KV cache (64-token pages, "
@@ -501,7 +511,7 @@ def run_serving(args, da, wd, y, lam, lam_init, dev, stream, peaks, kvb):
         da.diffattn_decode_paged(y["q1"], y["q2"], q8["k1"], q8["k2"], q8["v"], table, lens, lam, lam_init, L=L,
                                  eps=wd.eps, out_dtype=torch.bfloat16, out=out, ws=ws, stream=stream, scales=scales)
 
-    ms8 = time_device(step8, args.steps, max(3, args.warmup), stream)
+    ms8 = time_device(step8, extra_reps(args), max(3, args.warmup), stream)
     assert da.read_error(ws) == 0
     gbs8 = kvb / 2 / (ms8 * 1e-3) / 1e9
     res["fp8_cache"] = {
@@ -565,6 +575,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     clocks = clk.summary()
     ms = [a.elapsed_time(b) for a, b in ev]
     ms_step = max_over_ranks(sum(ms) / len(ms), dev)
+    ms_median = max_over_ranks(statistics.median(ms), dev)
     flops = prefill_def_flops(w)
     value = job_throughput(flops, ms_step, world) / 1e12
     achieved = flops / (ms_step * 1e-3) / 1e12  # the prefill kernel is the whole step on the GPU
@@ -604,6 +615,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "l2": "flushed between timed steps (256 MB write, untimed)",
                    "flops": "algorithmic: 4*Np*d + 2*Np*Dv per (b,h), Np = N(N+1)/2",
                    "exec_tflops": world * prefill_exec_flops(w) / (ms_step * 1e-3) / 1e12,
+                   "ms_per_step_median": ms_median,
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} bf16 burst",
@@ -624,7 +636,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-decode", action="store_true")
