@@ -14,7 +14,8 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdiffattn.so")
+# DIFFATTN_LIBRARY selects another build of the library, e.g. libdiffattn_debug.so.
+LIB_PATH = os.environ.get("DIFFATTN_LIBRARY") or os.path.join(_PKG, "libdiffattn.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
 F32, BF16, F16 = 0, 1, 2

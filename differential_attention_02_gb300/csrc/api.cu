@@ -557,6 +557,7 @@ diffattn_status decode_paged(bool fp8, const float* scales, const void* q1, cons
     p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
     p.block_table = block_table;
     p.max_pages = max_pages;
+    p.num_pages = num_pages;
     p.kv_group = kv_group;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.err = err_word(workspace);

@@ -28,6 +28,29 @@ __device__ __forceinline__ void report_error(int32_t* err, int32_t site, int32_t
     if (err != nullptr) atomicCAS(err, 0, (site << 8) | kind);
 }
 
+// Device-side index checks of a debug build (compiled with DIFFATTN_DEBUG_CHECKS;
+// build(debug=True) makes libdiffattn_debug.so). A failed check records
+// (site << 8) | kErrIndex in the error word; it never traps. The checked accesses
+// are TMA coordinates, paged block-table entries and split ranges, all of which
+// the hardware or the kernel already makes safe (an out-of-range TMA load reads
+// zeros, a store past the tensor's end is clipped), so a failure is reported
+// rather than skipped. In a release build index_ok compiles to `true`.
+constexpr int32_t kErrIndex = 2;
+#ifdef DIFFATTN_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool index_ok(bool cond, int32_t* err, int32_t site) {
+    if constexpr (kDebugChecks) {
+        if (!cond) {
+            report_error(err, site, kErrIndex);
+            return false;
+        }
+    }
+    return true;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -131,7 +131,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                 // Coordinates (row, batch) of the stage: (key, b) in a contiguous cache,
                 // (0, page) in a paged one.
                 const int row = pages ? 0 : key_begin + t * kStageKeys;
-                const int bz = pages ? page : b;
+                // The stage lies inside this split's keys, and a paged stage's page inside the pool
+                // (a debug build that finds a page outside it reports it and reads page 0 instead).
+                index_ok(key_begin + t * kStageKeys < key_end && hk < p.H / p.kv_group, p.err, 0xA0);
+                const int bz = pages ? (index_ok(page >= 0 && page < p.num_pages, p.err, 0xA1) ? page : 0) : b;
                 mbar_arrive_expect_tx(&full[s], C::kStageBytes);
 #pragma unroll
                 for (int x = 0; x < C::kBoxesK; ++x) {  // fp8: one box, x = 0

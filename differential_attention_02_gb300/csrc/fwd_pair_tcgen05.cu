@@ -180,6 +180,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&p.tm_v);
             mbar_arrive_expect_tx(&bars->q_full, C::kQBytes);
 #pragma unroll
+            index_ok(q0 < p.N && h < p.H && b < p.B, p.err, 0x93);
             for (int x = 0; x < D / 64; ++x) tma_load_4d(qs + x * C::kBoxBytes, tm_q, &bars->q_full, x * 64, q0, h, b);
             // Issue order K(j), V(j): K tiles run ahead as soon as S frees them, V tiles
             // follow the PV products.
@@ -190,6 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 go = mbar_wait(&bars->k_empty[sk], ((j / C::kKStages) & 1) ^ 1, abort_flag, p.err, 0x51);
                 if (!go) break;
                 mbar_arrive_expect_tx(&bars->k_full[sk], C::kKBytes);
+                index_ok(j * BN < p.N, p.err, 0x94);
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x)
                     tma_load_4d(ks + sk * C::kKBytes + x * C::kBoxBytes, tm_k, &bars->k_full[sk], x * 64, j * BN, h,
@@ -474,6 +476,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 128);  // all four epilogue warps, on every path
         if (warp == 2 && lane == 0 && !*abort_flag) {
             const int bw = p.out_bf16 || p.out_f16 ? 64 : 32;  // elements per 128-byte box row
+            index_ok(q0 < p.N && own0 + H2 <= DV, p.err, 0x95);
             for (int i = 0; i < H2 / bw; ++i)
                 tma_store_3d(&p.tm_out, smem + C::kOffOut + i * (BM * 128), h * DV + own0 + i * bw, q0, b);
             tma_store_commit();

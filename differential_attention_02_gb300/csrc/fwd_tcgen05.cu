@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 tma_prefetch_desc(&p.tm_k2);
                 tma_prefetch_desc(&p.tm_v);
                 mbar_arrive_expect_tx(&bars->q_full, 2 * C::kQBytes);
+                index_ok(q0 < p.N && h < p.H && b < p.B, p.err, 0x90);
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x) {
                     tma_load_4d(q1s + x * C::kBoxBytes, &p.tm_q1, &bars->q_full, x * 64, q0, h, b);
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                     if (!mbar_wait(&bars->kv_empty[s], ((j / kKvStages) & 1) ^ 1, abort_flag, p.err, 0x31)) break;
                     uint8_t* st = stages + s * C::kStageBytes;
                     mbar_arrive_expect_tx(&bars->kv_full[s], C::kStageBytes);
+                    index_ok(j * BN < p.N, p.err, 0x91);
 #pragma unroll
                     for (int x = 0; x < D / 64; ++x) {
                         tma_load_4d(st + x * C::kBoxBytes, &p.tm_k1, &bars->kv_full[s], x * 64, j * BN, h, b);
@@ -462,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         named_bar_sync(1, 256);
         if (threadIdx.x == 0 && !*abort_flag) {
             const int bw = p.out_bf16 || p.out_f16 ? 64 : 32;  // elements per 128-byte box row
+            index_ok(q0 < p.N, p.err, 0x92);
             for (int i = 0; i < DV / bw; ++i) tma_store_3d(&p.tm_out, stage + i * (BM * 128), h * DV + i * bw, q0, b);
             tma_store_commit();
             tma_store_wait_read();

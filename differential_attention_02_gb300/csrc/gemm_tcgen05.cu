@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                     }
                     uint8_t* st = smem + s * kStageBytes;
                     mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
+                    index_ok(m0 < p.M && n0 < p.N && kb * BK < p.K, p.err, 0xB0);
                     tma_load_2d(st, &p.tm_a, &bars->full[s], kb * BK, m0);
 #pragma unroll
                     for (int c = 0; c < BN / 64; ++c)
@@ -209,8 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                 __syncwarp();
                 if (lane == 0) {
                     const int nbox = kOutCols / bw;
-                    for (int i = 0; i < nbox; ++i)
+                    for (int i = 0; i < nbox; ++i) {
+                        index_ok(m0 + lg * 32 < p.M && n0 + pass * kOutCols + i * bw < p.N, p.err, 0xB1);
                         tma_store_2d(&p.tm_c, stage + i * kOutBoxBytes, n0 + pass * kOutCols + i * bw, m0 + lg * 32);
+                    }
                     tma_store_commit();
                 }
             }

@@ -63,6 +63,7 @@ struct DecodeParams {
     int32_t* err;
     const int32_t* block_table;  // [B][max_pages] physical page of each 64-token page, or null (contiguous cache)
     int max_pages;
+    int num_pages = 0;           // pages in the pool (paged cache; checked in debug builds only)
     int kv_group;  // query heads per KV head (query head h reads KV head h / kv_group)
     int kv_fp8;    // cache of fp8 e4m3 values (1) or bf16 (0)
     float k1_scale = 1.f, k2_scale = 1.f, v_scale = 1.f;  // cache value = stored value * scale
