@@ -400,22 +400,20 @@ def run_backward(args, da, gi, dev, stream, peaks, peak_kind):
     ws = da.workspace(da.bwd_workspace_bytes(w.B, w.H, w.N, w.d, w.Dv), dev)
     fn = lambda: da.diffattn_bwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], dy, lam, lam_init, w.eps,
                                  want_dnorm_weight=True, ws=ws, stream=stream)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        ms = time_device(fn, extra_reps(args), args.warmup, stream)
+    ms = time_device(fn, extra_reps(args), args.warmup, stream)
+    assert da.read_error(ws) == 0
     n_pairs = w.N * (w.N + 1) / 2
     # Chain-rule FLOPs per (b, h): per map S recomputed, dQ and dK (2 Np d each); dV and dA (2 Np Dv each).
     flops = w.B * w.H * (12 * n_pairs * w.d + 4 * n_pairs * w.Dv)
+    # Executed on the tensor cores: the forward re-run (4 Np d + 4 Np Dv), then the key-side kernel
+    # (S1, S2, dA, dV, dK1, dK2: 8 Np d + 4 Np Dv) and the query-side one (S1, S2, dA, dQ1, dQ2: 8 Np d + 2 Np Dv).
+    exec_flops = w.B * w.H * n_pairs * (20 * w.d + 10 * w.Dv)
     tf = flops / (ms * 1e-3) / 1e12
-    # CUDA-core fp32 peak: SMs x 128 FMA lanes x 2 FLOP x the SM clock sampled while the backward ran
-    # (the maximum clock when no sample could be taken).
-    c = clk.summary()
-    sm_mhz = c["sm_mhz"] or c["sm_max_mhz"] or 2070.0
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12
     return {"workload": "backward of the prefill workload B4 H16 N2048 d64 Dv128 causal, bf16 in, fp32 gradients",
             "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "flops_per_step": flops,
-            "roofline": {"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
-                         "peak_kind": f"derived: {sms} SMs x 128 fp32 lanes x 2 x {sm_mhz:.0f} MHz (sampled)"},
+            "exec_tflops": exec_flops / (ms * 1e-3) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 burst"},
             "gpu_launches_per_step": 4}
 
 

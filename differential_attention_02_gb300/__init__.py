@@ -435,8 +435,10 @@ def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float,
     Range: fp16 holds projections up to 65504 in magnitude; an entry beyond that
     overflows to infinity in the GEMM epilogue and the module's output is not
     finite. Inputs normalised before the projections (as in the layer) stay far
-    inside it. For wider activations pass qkv_dtype=torch.bfloat16 (the range of
-    fp32, 8 significant bits instead of 11).
+    inside it. Projections that large would also put the scores past the
+    attention's own range (scaled scores below 2^28, see diffattn_fwd), so fp16 is
+    no narrower in practice; qkv_dtype=torch.bfloat16 selects bf16 Q, K and V
+    (8 significant bits instead of 11) for callers who want bf16 throughout.
     """
     if qkv_dtype not in (torch.float16, torch.bfloat16):
         raise ValueError("qkv_dtype must be torch.float16 or torch.bfloat16")

@@ -27,7 +27,7 @@ LIB = os.path.join(PKG, "libdiffattn.so")
 BUILD_DEBUG = os.path.join(PKG, "_build_debug")
 LIB_DEBUG = os.path.join(PKG, "libdiffattn_debug.so")
 SOURCES = ["api.cu", "fwd_simt_f32.cu", "decode_bf16.cu", "gemm_tcgen05.cu", "fwd_tcgen05.cu",
-           "fwd_pair_tcgen05.cu", "layer_ops.cu", "bwd_simt.cu",
+           "fwd_pair_tcgen05.cu", "layer_ops.cu", "bwd_simt.cu", "bwd_tcgen05.cu",
            "selftest.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"),
            os.path.join(ROOT, "include", "diffattn.h")]

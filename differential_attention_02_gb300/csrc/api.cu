@@ -70,6 +70,20 @@ bool encode_out_3d(CUtensorMap* m, void* ptr, int W, int N, int B, int elem_byte
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over the backward's per-row statistics [rows][4] fp32, boxes of 4 x 64
+// rows, unswizzled (the key-side gradient kernel loads one query step at a time).
+bool encode_stats_2d(CUtensorMap* m, const float* ptr, int64_t rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {4, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {16};
+    cuuint32_t box[2] = {4, 64};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_2d(CUtensorMap* m, const void* ptr, int inner, int outer, int64_t ld, int box_inner, int box_outer,
                bool f16) {
     auto enc = tensor_map_encoder();
@@ -367,6 +381,61 @@ diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     if (workspace == nullptr || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return DIFFATTN_ERR_WORKSPACE;
     BwdParams p{};
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.dlambda = dlambda;
+    p.dnorm_w = dnorm_weight;
+    p.Dv = Dv;
+    p.part_lam = reinterpret_cast<float*>(ws + lay.part_lam);
+    p.part_w = reinterpret_cast<float*>(ws + lay.part_w);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int dt = in_dtype == DIFFATTN_F32 ? 0 : in_dtype == DIFFATTN_BF16 ? 1 : 2;
+    if (bwd_tc_supported(d, Dv, dt)) {
+        // Tensor-core path: the forward re-run with the preparation epilogue (dO in
+        // the operand type, per-row statistics, dlambda and gain partials), the
+        // key-side and query-side gradient kernels, then the fixed-order reduction.
+        const CUtensorMapDataType tdt = dt == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+        void* d_o = ws + lay.d_o;
+        float* stats = reinterpret_cast<float*>(ws + lay.stats);
+        const diffattn_tensor dot{d_o, (int64_t)H * N * Dv, (int64_t)N * Dv, Dv};
+        FwdParams f{};
+        if (!encode_4d(&f.tm_q1, q1, d, N, H, B, 64, kFwdBM, sw, tdt) ||
+            !encode_4d(&f.tm_q2, q2, d, N, H, B, 64, kFwdBM, sw, tdt) ||
+            !encode_4d(&f.tm_k1, k1, d, N, H, B, 64, kFwdBN, sw, tdt) ||
+            !encode_4d(&f.tm_k2, k2, d, N, H, B, 64, kFwdBN, sw, tdt) ||
+            !encode_4d(&f.tm_v, v, Dv, N, H, B, 64, kFwdBN, sw, tdt))
+            return DIFFATTN_ERR_INVALID_ARG;
+        f.in_f16 = dt == 2;
+        f.norm_w = norm_weight;
+        f.B = B; f.H = H; f.N = N; f.d = d; f.Dv = Dv; f.causal = causal != 0;
+        f.lambda = lambda; f.lambda_init = lambda_init; f.eps = eps;
+        f.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+        f.err = err_word(workspace);
+        f.dy = dy;
+        f.d_o = d_o;
+        f.stats = stats;
+        f.part_lam = p.part_lam;
+        f.part_w = p.part_w;
+        BwdTcParams t{};
+        t.tm_q1 = f.tm_q1; t.tm_q2 = f.tm_q2; t.tm_k1 = f.tm_k1; t.tm_k2 = f.tm_k2; t.tm_v = f.tm_v;
+        if (!encode_4d(&t.tm_do, dot, Dv, N, H, B, 64, 128, sw, tdt) ||
+            !encode_4d(&t.tm_q1s, q1, d, N, H, B, 64, 64, sw, tdt) ||
+            !encode_4d(&t.tm_q2s, q2, d, N, H, B, 64, 64, sw, tdt) ||
+            !encode_4d(&t.tm_dos, dot, Dv, N, H, B, 64, 64, sw, tdt) ||
+            !encode_stats_2d(&t.tm_stats, stats, (int64_t)B * H * N))
+            return DIFFATTN_ERR_INVALID_ARG;
+        t.stats = stats;
+        t.dq1 = dq1; t.dq2 = dq2; t.dk1 = dk1; t.dk2 = dk2; t.dv = dv;
+        t.B = B; t.H = H; t.N = N; t.d = d; t.Dv = Dv; t.causal = causal != 0; t.in_f16 = dt == 2;
+        t.lambda = lambda;
+        t.scale_log2 = f.scale_log2;
+        t.scale = (float)(1.0 / sqrt((double)d));
+        t.err = err_word(workspace);
+        cudaError_t e = launch_bwd_prep(f, st);
+        if (e == cudaSuccess) e = launch_bwd_tc(t, st);
+        if (e == cudaSuccess) e = launch_bwd_reduce(p, (int64_t)((N + kFwdBM - 1) / kFwdBM) * B * H, st);
+        return cuda_status(e);
+    }
     p.q1 = q1.ptr; p.q2 = q2.ptr; p.k1 = k1.ptr; p.k2 = k2.ptr; p.v = v.ptr;
     const diffattn_tensor* ts[5] = {&q1, &q2, &k1, &k2, &v};
     int64_t* ss[5] = {p.sq1, p.sq2, p.sk1, p.sk2, p.sv};
@@ -378,17 +447,12 @@ diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     p.dy = dy;
     p.norm_w = norm_weight;
     p.dq1 = dq1; p.dq2 = dq2; p.dk1 = dk1; p.dk2 = dk2; p.dv = dv;
-    p.dlambda = dlambda;
-    p.dnorm_w = dnorm_weight;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.d_o = reinterpret_cast<float*>(ws + lay.d_o);
     p.stats = reinterpret_cast<float*>(ws + lay.stats);
-    p.part_lam = reinterpret_cast<float*>(ws + lay.part_lam);
-    p.part_w = reinterpret_cast<float*>(ws + lay.part_w);
-    p.B = B; p.H = H; p.N = N; p.d = d; p.Dv = Dv; p.causal = causal != 0;
-    p.in_dtype = in_dtype == DIFFATTN_F32 ? 0 : in_dtype == DIFFATTN_BF16 ? 1 : 2;
+    p.B = B; p.H = H; p.N = N; p.d = d; p.causal = causal != 0;
+    p.in_dtype = dt;
     p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
-    return cuda_status(launch_bwd_simt(p, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_bwd_simt(p, st));
 }
 
 diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2, int d,

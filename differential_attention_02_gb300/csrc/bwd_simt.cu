@@ -449,13 +449,17 @@ cudaError_t launch_typed(const BwdParams& p, cudaStream_t stream) {
     bwd_kv_kernel<T><<<grid, kThreads, s_kv, stream>>>(p);
     bwd_q_kernel<T><<<grid, kThreads, s_q, stream>>>(p);
     const int64_t n_part = (int64_t)grid.x * p.H * p.B;
-    bwd_reduce_kernel<<<p.dnorm_w ? 1 + Dv : 1, 256, 0, stream>>>(p, n_part);
-    return cudaGetLastError();
+    return launch_bwd_reduce(p, n_part, stream);
 }
 
 }  // namespace
 
 int64_t bwd_partial_count(int B, int H, int N) { return (int64_t)((N + kRows - 1) / kRows) * H * B; }
+
+cudaError_t launch_bwd_reduce(const BwdParams& p, int64_t n_part, cudaStream_t stream) {
+    bwd_reduce_kernel<<<p.dnorm_w ? 1 + p.Dv : 1, 256, 0, stream>>>(p, n_part);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_simt(const BwdParams& p, cudaStream_t stream) {
     if (p.d % 32 || p.d > 32 * kDL || p.Dv % 32 || p.Dv > 32 * kDVL) return cudaErrorInvalidValue;

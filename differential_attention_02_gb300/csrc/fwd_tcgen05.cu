@@ -39,6 +39,8 @@
 // execute in issue order, so the read completes before the overwrite.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -75,7 +77,8 @@ struct FwdCfg {
     // The epilogue's exchange buffer (4 x 128 floats) reuses the Q1 tile, which
     // is idle once the last MMA has completed.
     static constexpr int kOffEpi = kOffQ1;
-    static_assert(4 * BM * 4 <= kQBytes, "epilogue buffer fits in the Q1 tile");
+    static_assert(8 * BM * 4 <= kQBytes, "epilogue buffer fits in the Q1 tile");
+    static_assert(BM * (DV + 1) * 4 <= kKvStages * kStageBytes, "gain-gradient terms fit in the K/V ring");
     static constexpr size_t kSmem = 1024 + (size_t)kOffBar + kBarBytes;
     static_assert(kSmem <= 232448, "shared memory budget");
     static constexpr uint32_t kTmemCols = 512;
@@ -125,7 +128,171 @@ __device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, 
     }
 }
 
-template <int D, int DV, bool F16>
+// Epilogue of the backward preparation (PREP): instead of storing y, the two
+// softmax groups derive, per query row, what the tensor-core backward consumes.
+// With n = O/r, r = sqrt(mean(O^2) + eps), c = 1 - lambda_init, g = dy w c:
+//   dO = (g - n mean(g n)) / r          (gradient of the pre-norm output O)
+//   D1 = dO . (P1 V),  D2 = -lambda dO . (P2 V)
+//   L_m = max_m + log2(l_m)             (so that P_m = exp2(S_m log2(e)/sqrt(d) - L_m))
+// and, summed over the CTA's rows in a fixed order, dlambda = -sum dO . (P2 V)
+// and the gain's gradient sum_rows dy n c. Group g handles output columns
+// [g Dv/2, (g+1) Dv/2); row sums cross between the groups through `xch`.
+template <int DV, bool F16>
+__device__ __forceinline__ void prep_epilogue(const FwdParams& p, bool ok, int g, int r, int qrow, int b, int h,
+                                              uint32_t lane_base, uint32_t col_o, float l, float m_used, float* xch,
+                                              float* dwbuf) {
+    constexpr int kHalf = DV / 2;
+    using T16 = typename std::conditional<F16, __half, __nv_bfloat16>::type;
+    const bool live = ok && qrow < p.N;
+    // Row statistics of both maps.
+    xch[g * BM + r] = l;
+    xch[(2 + g) * BM + r] = m_used;
+    named_bar_sync(1, 256);
+    const float l1 = xch[r], l2 = xch[BM + r], mx1 = xch[2 * BM + r], mx2 = xch[3 * BM + r];
+    const float i1 = 1.0f / l1, i2 = 1.0f / l2, lam = p.lambda, cs = 1.0f - p.lambda_init;
+    const uint32_t t1 = lane_base + col_o + g * kHalf, t2 = lane_base + col_o + DV + g * kHalf;
+    // This row's slice of dy (kHalf 16-bit values) in fp32.
+    float dyv[kHalf];
+    if (live) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T16*>(p.dy) +
+                                                          (((int64_t)b * p.N + qrow) * p.H + h) * DV + g * kHalf);
+#pragma unroll
+        for (int c = 0; c < kHalf / 8; ++c) {
+            const uint4 v = src[c];
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if constexpr (F16) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                    dyv[c * 8 + 2 * e] = f.x;
+                    dyv[c * 8 + 2 * e + 1] = f.y;
+                } else {
+                    dyv[c * 8 + 2 * e] = bf16lo_to_f32(w4[e]);
+                    dyv[c * 8 + 2 * e + 1] = bf16hi_to_f32(w4[e]);
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < kHalf; ++c) dyv[c] = 0.f;
+    }
+    // Pass 1: sum of squares of O over the row.
+    float ss = 0.f;
+    if (ok) {
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c) {
+            uint32_t a[32], e[32];
+            tmem_ld32(t1 + c * 32, a);
+            tmem_ld32(t2 + c * 32, e);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float x = __uint_as_float(a[i]) * i1 - lam * (__uint_as_float(e[i]) * i2);
+                ss = fmaf(x, x, ss);
+            }
+        }
+    }
+    xch[(4 + g) * BM + r] = ss;
+    named_bar_sync(1, 256);
+    const float ir = 1.0f / sqrtf((xch[4 * BM + r] + xch[5 * BM + r]) / (float)DV + p.eps);
+    // Pass 2: mean(g n) over the row.
+    float gn = 0.f;
+    if (ok) {
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c) {
+            uint32_t a[32], e[32];
+            tmem_ld32(t1 + c * 32, a);
+            tmem_ld32(t2 + c * 32, e);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int col = g * kHalf + c * 32 + i;
+                const float n = (__uint_as_float(a[i]) * i1 - lam * (__uint_as_float(e[i]) * i2)) * ir;
+                const float gg = dyv[c * 32 + i] * (p.norm_w ? p.norm_w[col] : 1.f) * cs;
+                gn = fmaf(gg, n, gn);
+            }
+        }
+    }
+    xch[(6 + g) * BM + r] = gn;
+    named_bar_sync(1, 256);
+    gn = (xch[6 * BM + r] + xch[7 * BM + r]) / (float)DV;
+    // Pass 3: dO (stored in the operand type), D1/D2 partials, gain-gradient terms.
+    float x1 = 0.f, x2 = 0.f, x2e = 0.f;
+    T16* dorow = static_cast<T16*>(p.d_o) + (((int64_t)b * p.H + h) * p.N + qrow) * DV + g * kHalf;
+    float* dwrow = dwbuf + r * (DV + 1) + g * kHalf;
+#pragma unroll
+    for (int c = 0; c < kHalf / 32; ++c) {
+        uint32_t a[32], e[32];
+        if (ok) {
+            tmem_ld32(t1 + c * 32, a);
+            tmem_ld32(t2 + c * 32, e);
+            tmem_ld_wait();
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            float d2[2], o1v[2], o2v[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int col = g * kHalf + c * 32 + i + k;
+                const float o1 = ok ? __uint_as_float(a[i + k]) * i1 : 0.f;
+                const float o2 = ok ? __uint_as_float(e[i + k]) * i2 : 0.f;
+                const float n = (o1 - lam * o2) * ir;
+                const float dyc = dyv[c * 32 + i + k];
+                const float gg = dyc * (p.norm_w ? p.norm_w[col] : 1.f) * cs;
+                d2[k] = (gg - n * gn) * ir;
+                o1v[k] = o1;
+                o2v[k] = o2;
+                dwrow[c * 32 + i + k] = live ? dyc * n * cs : 0.f;
+            }
+            pk[i / 2] = pack_p<F16>(d2[0], d2[1]);
+            // D1, D2 from the rounded dO the gradient products will use, so that
+            // sum_j P_ij (dA_ij - D_i) stays zero for every row.
+            float r0, r1;
+            if constexpr (F16) {
+                const float2 rr = __half22float2(*reinterpret_cast<const __half2*>(&pk[i / 2]));
+                r0 = rr.x;
+                r1 = rr.y;
+            } else {
+                r0 = bf16lo_to_f32(pk[i / 2]);
+                r1 = bf16hi_to_f32(pk[i / 2]);
+            }
+            x1 = fmaf(r0, o1v[0], fmaf(r1, o1v[1], x1));
+            x2 = fmaf(r0, o2v[0], fmaf(r1, o2v[1], x2));
+            x2e = fmaf(d2[0], o2v[0], fmaf(d2[1], o2v[1], x2e));  // dlambda takes the unrounded dO
+        }
+        if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(dorow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+    }
+    named_bar_sync(1, 256);  // every read of the exchange slots above is done
+    xch[g * BM + r] = x1;
+    xch[(2 + g) * BM + r] = x2;
+    xch[(4 + g) * BM + r] = x2e;
+    named_bar_sync(1, 256);
+    const float X1 = xch[r] + xch[BM + r], X2 = xch[2 * BM + r] + xch[3 * BM + r];
+    const float X2e = xch[4 * BM + r] + xch[5 * BM + r];
+    if (g == 0 && live) {
+        float4* st = reinterpret_cast<float4*>(p.stats + (((int64_t)b * p.H + h) * p.N + qrow) * 4);
+        *st = make_float4(mx1 + __log2f(l1), mx2 + __log2f(l2), X1, -lam * X2);
+    }
+    if (g == 0) dwbuf[r * (DV + 1) + DV] = live ? -X2e : 0.f;  // this row's dlambda term
+    named_bar_sync(1, 256);
+    // Column sums over the CTA's rows, in row order: the gain's gradient and dlambda.
+    const int t = g * BM + r;  // 0..255
+    for (int col = t; col <= DV; col += 256) {
+        float acc = 0.f;
+        for (int row = 0; row < BM; ++row) acc += dwbuf[row * (DV + 1) + col];
+        if (col < DV)
+            p.part_w[(int64_t)blockIdx.x * DV + col] = acc;
+        else
+            p.part_lam[blockIdx.x] = acc;
+    }
+}
+
+template <int D, int DV, bool F16, bool PREP>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D, DV>;
     extern __shared__ uint8_t smem_raw[];
@@ -392,6 +559,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         }
         tc_fence_after();
         named_bar_sync(1, 256);  // both groups past their last PV: the Q1 tile is free
+        if constexpr (PREP) {
+            // The exchange slots take 8 x BM floats of the Q1 tile; the gain-gradient
+            // terms [BM][DV + 1] take the idle K/V ring.
+            prep_epilogue<DV, F16>(p, ok, g, r, qrow, b, h, lane_base, C::kColO, l, m_used, epi,
+                                   reinterpret_cast<float*>(smem + C::kOffStages));
+            tc_fence_before();
+            named_bar_sync(2, kThreads);
+            return;
+        }
         epi[g * BM + r] = (g == 0) ? 1.0f / l : p.lambda / l;
         named_bar_sync(1, 256);
         const float inv1 = epi[r], inv2 = epi[BM + r];
@@ -474,12 +650,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     }
 }
 
-template <int D, int DV, bool F16>
+template <int D, int DV, bool F16, bool PREP>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D, DV>;
-    auto k = fwd_bf16_kernel<D, DV, F16>;
+    auto k = fwd_bf16_kernel<D, DV, F16, PREP>;
     // The register split assumes the compiled per-thread count (see kRegsLaunch).
-    cudaError_t e = prepare_once<fwd_bf16_kernel<D, DV, F16>>((int)C::kSmem, kRegsLaunch);
+    cudaError_t e = prepare_once<fwd_bf16_kernel<D, DV, F16, PREP>>((int)C::kSmem, kRegsLaunch);
     if (e != cudaSuccess) return e;
     const int n_tiles = (p.N + BM - 1) / BM;
     k<<<n_tiles * p.B * p.H, kThreads, C::kSmem, stream>>>(p);
@@ -489,7 +665,14 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream) {
-    if (p.d == 64 && p.Dv == 128) return p.in_f16 ? launch_t<64, 128, true>(p, stream) : launch_t<64, 128, false>(p, stream);
+    if (p.d == 64 && p.Dv == 128)
+        return p.in_f16 ? launch_t<64, 128, true, false>(p, stream) : launch_t<64, 128, false, false>(p, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_prep(const FwdParams& p, cudaStream_t stream) {
+    if (p.d == 64 && p.Dv == 128 && p.dy && p.d_o && p.stats && p.part_lam && p.part_w)
+        return p.in_f16 ? launch_t<64, 128, true, true>(p, stream) : launch_t<64, 128, false, true>(p, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                 if (lane == 0) {
                     const int nbox = kOutCols / bw;
                     for (int i = 0; i < nbox; ++i) {
-                        index_ok(m0 + lg * 32 < p.M && n0 + pass * kOutCols + i * bw < p.N, p.err, 0xB1);
+                        // The tile starts inside C; boxes past its end are clipped by the store.
+                        index_ok(m0 < p.M && n0 < p.N && m0 >= 0 && n0 >= 0, p.err, 0xB1);
                         tma_store_2d(&p.tm_c, stage + i * kOutBoxBytes, n0 + pass * kOutCols + i * bw, m0 + lg * 32);
                     }
                     tma_store_commit();

@@ -45,6 +45,23 @@ struct BwdParams {
 };
 int64_t bwd_partial_count(int B, int H, int N);
 cudaError_t launch_bwd_simt(const BwdParams& p, cudaStream_t stream);
+// Block 0: *dlambda = sum of n_part partials; block 1 + c: dnorm_w[c] (fixed order).
+cudaError_t launch_bwd_reduce(const BwdParams& p, int64_t n_part, cudaStream_t stream);
+
+// Backward on tcgen05 (d = 64, Dv = 128, bf16 or fp16 operands), after launch_bwd_prep.
+struct BwdTcParams {
+    CUtensorMap tm_q1, tm_q2, tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H, N, width], boxes of 64 x 128 rows
+    CUtensorMap tm_do;                             // dO [B, H, N, Dv], boxes of 64 x 128 rows
+    CUtensorMap tm_q1s, tm_q2s, tm_dos;            // the same tensors in boxes of 64 x 64 rows (query steps)
+    CUtensorMap tm_stats;                          // 2-D map over the stats [B*H*N][4] fp32, boxes of 4 x 64
+    const float* stats;                            // [B, H, N, 4]: L1, L2, D1, D2
+    float *dq1, *dq2, *dk1, *dk2, *dv;             // fp32 gradients, contiguous
+    int B, H, N, d, Dv, causal, in_f16;
+    float lambda, scale_log2, scale;               // scale = 1/sqrt(d), scale_log2 = log2(e)/sqrt(d)
+    int32_t* err;
+};
+bool bwd_tc_supported(int d, int Dv, int in_dtype);  // in_dtype 1 bf16, 2 fp16
+cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream);
 
 // bf16 split-KV decode (+ merge).
 struct DecodeParams {
@@ -129,8 +146,16 @@ struct FwdParams {
     float lambda, lambda_init, eps;
     float scale_log2;  // log2(e) / sqrt(d)
     int32_t* err;
+    // Backward preparation (launch_bwd_prep): the same forward, whose epilogue
+    // writes what the tensor-core backward needs instead of the output.
+    const void* dy = nullptr;      // [B, N, H, Dv] output gradient, operand dtype
+    void* d_o = nullptr;           // [B, H, N, Dv] gradient of the pre-norm output, operand dtype
+    float* stats = nullptr;        // [B, H, N, 4]: log2 sum-exp of map 1, of map 2 (scaled-score units), D1, D2
+    float* part_lam = nullptr;     // [grid] per-CTA partial of dlambda
+    float* part_w = nullptr;       // [grid][Dv] per-CTA partial of the gain's gradient
 };
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);       // both maps in one CTA
+cudaError_t launch_bwd_prep(const FwdParams& p, cudaStream_t stream);       // d=64: forward + backward inputs
 cudaError_t launch_fwd_pair_bf16(const FwdParams& p, cudaStream_t stream);  // one map per CTA of a pair
 constexpr int kFwdBM = 128;
 constexpr int kFwdBN = 128;

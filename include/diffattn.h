@@ -108,14 +108,17 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
  * accumulation (the probability tile P is rounded to the operand type for the
  * P.V product). out_dtype f32 or bf16 for every in_dtype; f16 as well for bf16
  * and f16 inputs.
- * Range: scores, running maxima, row sums and accumulators are fp32 and every
- *   P entry is at most 2^8 (the running maximum is refreshed whenever a row's
- *   maximum grows by more than 8 in log2 units), so any finite input of the
- *   operand type is in range, however large its scores. Precision: the output's
+ * Range: scores, running maxima, row sums and accumulators are fp32 and P is
+ *   kept below 2^8 (the running maximum is refreshed whenever a row's maximum
+ *   grows by more than 8 in log2 units). The exponent S log2(e)/sqrt(d) - max is
+ *   one fused multiply-add whose rounding residual grows with the scores: up to
+ *   half an fp32 ulp of the row maximum, which stays below 1 for scaled scores
+ *   |S log2(e)/sqrt(d)| < 2^24 and below the 16-bit P range for < 2^28. Scores
+ *   beyond 2^28 (far past one-hot: a softmax saturates long before) are outside
+ *   the supported range and may give a non-finite row. Precision: the output's
  *   sensitivity to the rounding of Q and K grows with the scores' magnitude, as
- *   for any softmax. An f16 out_dtype saturates nothing: |y| beyond 65504 would
- *   be infinite, but y is RMS-normalised (|y| <= sqrt(Dv) * |weight| *
- *   |1 - lambda_init|).
+ *   for any softmax. y is RMS-normalised (|y| <= sqrt(Dv) * |weight| *
+ *   |1 - lambda_init|), so an f16 out_dtype cannot overflow.
  * B, H or N equal to 0: nothing to do, returns DIFFATTN_OK.
  * workspace: at least diffattn_fwd_workspace_size() bytes, 256-byte aligned;
  *   its first 4 bytes are the device error word, which must be zero before the
@@ -335,8 +338,19 @@ diffattn_status diffattn_kv_append_paged_fp8(const void* k1_new, const void* k2_
  * dnorm_weight: device f32[Dv] or NULL — the gradient with respect to the
  *   RMSNorm gain (of a unit gain when norm_weight is NULL).
  * d and Dv multiples of 32 with d <= 128 and Dv <= 256 (else UNSUPPORTED).
- * Every pointer 16-byte aligned. Arithmetic is fp32 on the CUDA cores; results
- * do not depend on scheduling (no atomics). B, H or N equal to 0: DIFFATTN_OK.
+ * Every pointer 16-byte aligned. Two paths, chosen by shape and type:
+ *   bf16 or f16 with (d, Dv) = (64, 128): tcgen05 tensor cores. The forward is
+ *     re-run with an epilogue that leaves dO (rounded to in_dtype), the per-row
+ *     log-sum-exps, D1 = dO.(P1 V), D2 = -lambda dO.(P2 V) and per-tile partial
+ *     sums of dlambda and dw; a key-side kernel forms dV and dK1, dK2 and a
+ *     query-side kernel dQ1, dQ2, both from S, P and dA recomputed on the tensor
+ *     cores with fp32 accumulation. dO, A and dS1, dS2 are rounded to in_dtype
+ *     as the left operands of their products (like P in the forward): about
+ *     2.5e-3 relative RMS per gradient for bf16 and 3e-4 for f16.
+ *   otherwise (f32 inputs, other widths): fp32 arithmetic on the CUDA cores.
+ * Results do not depend on scheduling (no atomics): every gradient row is
+ * written by one CTA and the partial sums are added in a fixed order.
+ * B, H or N equal to 0: DIFFATTN_OK.
  * workspace: diffattn_bwd_workspace_size() bytes, 256-byte aligned.
  */
 diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
@@ -348,7 +362,8 @@ diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes diffattn_bwd needs: the control block, dO and four per-row
- * statistics in f32, and per-block partial sums of dlambda and dw. */
+ * statistics (dO in f32, or in the 16-bit input type on the tensor-core path),
+ * and per-block partial sums of dlambda and dw. */
 diffattn_status diffattn_bwd_workspace_size(int B, int H, int N, int d, int Dv, size_t* bytes);
 
 /*
