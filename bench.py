@@ -535,6 +535,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     stream = torch.cuda.current_stream()
     peaks, peak_kind = load_peaks()
 
+    if args.only:  # one section alone (profiling): no headline line
+        fn = {"decode": run_decode, "long_prefill": run_long_prefill, "module": run_module, "layer": run_layer,
+              "backward": run_backward}[args.only]
+        res = fn(args, da, gi, dev, stream, peaks, peak_kind)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "result": res}), flush=True)
+        return
+
     # -------- inputs resident in HBM
     w = gi.WORKLOADS[PREFILL]
     host = gi.prefill_inputs(w)
@@ -641,6 +649,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-extra", action="store_true", help="skip the long-prefill and module lines")
     ap.add_argument("--decode-batch", type=int, default=0, help="override the decode workload's batch (profiling)")
+    ap.add_argument("--only", default="", choices=["", "decode", "long_prefill", "module", "layer", "backward"],
+                    help="run one section alone and print its result (profiling), not the bench line")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
