@@ -25,7 +25,10 @@
 // Transformer que cancela ruído de atenção", section "Resultados experimentais
 // e efeitos de aplicação"); here the cache is quantized to halve the bytes the
 // HBM-bound decode reads. The K scales are folded into the query, the V scale
-// into the merged output.
+// into the merged output. Per byte read the fp8 path has twice the arithmetic
+// of the bf16 one (every e4m3 pair is converted to fp16 and then fp32), so its
+// loop is kept lean: packed fp32 FMAs on element pairs for the scores and P.V,
+// the eight keys of a warp unrolled, and a lazily moved running maximum.
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -74,13 +77,18 @@ __device__ __forceinline__ const uint4* key_chunk(const uint8_t* tile, int r, in
     else return k_chunk(tile, r, c);
 }
 
-// Four e4m3 values packed in a 32-bit word (lowest byte first) as floats.
-__device__ __forceinline__ void fp8x4_to_f32(uint32_t w, float* f) {
+// Four e4m3 values packed in a 32-bit word (lowest byte first) as two float pairs.
+__device__ __forceinline__ void fp8x4_to_f32x4(uint32_t w, float2* f) {
     const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
     const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-    const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[0] = __half22float2(__half2(lo));
+    f[1] = __half22float2(__half2(hi));
 }
+
+// Stale-maximum threshold (log2 units): a running maximum moves only when a score exceeds it
+// by more than this, so the weights exp2(s - m) stay below 2^8 and most stages skip the
+// rescale of the accumulators. The stale maximum is exact: l and o use the same one.
+constexpr float kLazyMax = 8.f;
 
 template <int D, int DV, bool FP8>
 __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_constant__ DecodeParams p) {
@@ -152,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
         const int kq = lane >> 2;      // key within the warp's 8
         const int quarter = lane & 3;  // quarter of the d elements this lane dots
         // Query halves, pre-scaled so scores come out in log2 units.
-        float q1r[C::kQuarter], q2r[C::kQuarter];
+        float q1r[C::kQuarter], q2r[C::kQuarter];  // fp8: read in pairs by the packed FMAs
         {
             const __nv_bfloat16* q1 = reinterpret_cast<const __nv_bfloat16*>(p.q1) + ((int64_t)b * p.H + h) * D;
             const __nv_bfloat16* q2 = reinterpret_cast<const __nv_bfloat16*>(p.q2) + ((int64_t)b * p.H + h) * D;
@@ -184,17 +192,22 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                 const uint4 bb = *key_chunk<D, FP8>(st + C::kKBytes, r, chunk);
                 const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bb.x, bb.y, bb.z, bb.w};
                 if constexpr (FP8) {
+                    // packed fp32 FMAs on (even, odd) element pairs
+                    float2 t1 = make_float2(0.f, 0.f), t2 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float fa[4], fb[4];
-                        fp8x4_to_f32(aw[e], fa);
-                        fp8x4_to_f32(bw[e], fb);
+                        float2 fa[2], fb[2];
+                        fp8x4_to_f32x4(aw[e], fa);
+                        fp8x4_to_f32x4(bw[e], fb);
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            s1 = fmaf(q1r[c * 16 + 4 * e + u], fa[u], s1);
-                            s2 = fmaf(q2r[c * 16 + 4 * e + u], fb[u], s2);
+                        for (int u = 0; u < 2; ++u) {
+                            const int i = c * 16 + 4 * e + 2 * u;
+                            t1 = __ffma2_rn(make_float2(q1r[i], q1r[i + 1]), fa[u], t1);
+                            t2 = __ffma2_rn(make_float2(q2r[i], q2r[i + 1]), fb[u], t2);
                         }
                     }
+                    s1 += t1.x + t1.y;
+                    s2 += t2.x + t2.y;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -221,38 +234,68 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
             }
             const int nk = min(kKeysPerWarp, key_end - (key_begin + t * kStageKeys + warp * kKeysPerWarp));
             if (nk > 0) {
-                const float n1 = fmaxf(m1, c1), n2 = fmaxf(m2, c2);
-                const float a1 = fast_exp2(m1 - n1), a2 = fast_exp2(m2 - n2);
-                const float p1 = ok ? fast_exp2(s1 - n1) : 0.f;
-                const float p2 = ok ? fast_exp2(s2 - n2) : 0.f;
-                l1 = l1 * a1 + p1;  // per-lane partial; every key is counted by its 4 lanes
-                l2 = l2 * a2 + p2;
-                m1 = n1;
-                m2 = n2;
+                if constexpr (FP8) {
+                    // c1, c2 and the maxima are the same in every lane: the branch is warp-uniform
+                    if (c1 > m1 + kLazyMax || c2 > m2 + kLazyMax) {
+                        const float n1 = c1 > m1 + kLazyMax ? c1 : m1, n2 = c2 > m2 + kLazyMax ? c2 : m2;
+                        const float a1 = fast_exp2(m1 - n1), a2 = fast_exp2(m2 - n2);
+                        l1 *= a1;
+                        l2 *= a2;
+                        m1 = n1;
+                        m2 = n2;
 #pragma unroll
-                for (int u = 0; u < C::kDVL; ++u) {
-                    o1[u] *= a1;
-                    o2[u] *= a2;
+                        for (int u = 0; u < C::kDVL; ++u) {
+                            o1[u] *= a1;
+                            o2[u] *= a2;
+                        }
+                    }
+                }
+                float p1, p2;
+                if constexpr (FP8) {
+                    p1 = ok ? fast_exp2(s1 - m1) : 0.f;
+                    p2 = ok ? fast_exp2(s2 - m2) : 0.f;
+                    l1 += p1;  // per-lane partial; every key is counted by its 4 lanes
+                    l2 += p2;
+                } else {
+                    const float n1 = fmaxf(m1, c1), n2 = fmaxf(m2, c2);
+                    const float a1 = fast_exp2(m1 - n1), a2 = fast_exp2(m2 - n2);
+                    p1 = ok ? fast_exp2(s1 - n1) : 0.f;
+                    p2 = ok ? fast_exp2(s2 - n2) : 0.f;
+                    l1 = l1 * a1 + p1;  // per-lane partial; every key is counted by its 4 lanes
+                    l2 = l2 * a2 + p2;
+                    m1 = n1;
+                    m2 = n2;
+#pragma unroll
+                    for (int u = 0; u < C::kDVL; ++u) {
+                        o1[u] *= a1;
+                        o2[u] *= a2;
+                    }
                 }
                 const uint8_t* vt = st + 2 * C::kKBytes;
-                for (int kk = 0; kk < nk; ++kk) {
+                auto pv_key = [&](int kk) {
                     const float w1 = __shfl_sync(0xffffffffu, p1, kk * 4);
                     const float w2 = __shfl_sync(0xffffffffu, p2, kk * 4);
                     const uint8_t* vrow = vt + (size_t)(warp * kKeysPerWarp + kk) * DV * C::kEB;
                     if constexpr (FP8) {
                         // kDVL consecutive e4m3 values: columns lane * kDVL ...
-                        float f[C::kDVL];
+                        float2 f[C::kDVL / 2];
                         if constexpr (C::kDVL == 4) {
-                            fp8x4_to_f32(*reinterpret_cast<const uint32_t*>(vrow + lane * 4), f);
+                            fp8x4_to_f32x4(*reinterpret_cast<const uint32_t*>(vrow + lane * 4), f);
                         } else {
                             const uint2 vv = *reinterpret_cast<const uint2*>(vrow + lane * 8);
-                            fp8x4_to_f32(vv.x, f);
-                            fp8x4_to_f32(vv.y, f + 4);
+                            fp8x4_to_f32x4(vv.x, f);
+                            fp8x4_to_f32x4(vv.y, f + 2);
                         }
+                        // packed fp32 FMAs on column pairs, one weight broadcast to both halves
+                        const float2 ww1 = make_float2(w1, w1), ww2 = make_float2(w2, w2);
 #pragma unroll
-                        for (int u = 0; u < C::kDVL; ++u) {
-                            o1[u] = fmaf(w1, f[u], o1[u]);
-                            o2[u] = fmaf(w2, f[u], o2[u]);
+                        for (int u = 0; u < C::kDVL / 2; ++u) {
+                            const float2 r1 = __ffma2_rn(ww1, f[u], make_float2(o1[2 * u], o1[2 * u + 1]));
+                            const float2 r2 = __ffma2_rn(ww2, f[u], make_float2(o2[2 * u], o2[2 * u + 1]));
+                            o1[2 * u] = r1.x;
+                            o1[2 * u + 1] = r1.y;
+                            o2[2 * u] = r2.x;
+                            o2[2 * u + 1] = r2.y;
                         }
                     } else if constexpr (C::kDVL == 4) {
                         const uint2 vv = *reinterpret_cast<const uint2*>(vrow + lane * 8);
@@ -274,6 +317,12 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_con
                             o2[2 * u + 1] = fmaf(w2, bf16hi_to_f32(vw[u]), o2[2 * u + 1]);
                         }
                     }
+                };
+                if (nk == kKeysPerWarp) {  // warp-uniform: every key of the warp is in range
+#pragma unroll
+                    for (int kk = 0; kk < kKeysPerWarp; ++kk) pv_key(kk);
+                } else {
+                    for (int kk = 0; kk < nk; ++kk) pv_key(kk);
                 }
             }
             __syncwarp();

@@ -1,9 +1,12 @@
 """GPU checks of the serving decode over an fp8 (e4m3) KV cache.
 
-The decode reads e4m3 bytes and one scale per tensor; its arithmetic is fp32 on
-the dequantized values, so it is compared with the float64 oracle run on exactly
-those dequantized values (the same bar as the bf16 decode). The append must
-quantize like a plain round-to-nearest-even cast of x / scale."""
+The decode reads e4m3 bytes and one scale per tensor. Its dot products are exact
+f16 x f16 products (every e4m3 value is an f16 value; the query is held as f16
+scaled by a power of two) accumulated in fp32, and the softmax weights are
+rounded to f16 for the P.V products (a relative 2^-11, as the prefill rounds P),
+so it is compared with the float64 oracle run on exactly the dequantized values,
+at the bar of the bf16 decode. The append must quantize like a plain
+round-to-nearest-even cast of x / scale."""
 
 import numpy as np
 import pytest
@@ -66,6 +69,31 @@ def test_fp8_paged_decode_matches_oracle_on_dequantized_cache(d, Dv, group):
     expand = lambda x: x.repeat_interleave(group, dim=1)
     ref = orc.diffattn_decode(q1, q2, expand(deq["k1"]), expand(deq["k2"]), expand(deq["v"]), lens_l, lam, lam_init)
     assert_bf16_parity(got, ref, f"fp8 paged decode d{d} group{group}")
+
+
+@pytest.mark.parametrize("q_scale", [1e-5, 3e4])
+def test_fp8_decode_query_magnitudes(q_scale):
+    """Queries far from unit scale: 1e-5 (f16 subnormal range without the power-of-two
+    scaling) and 3e4 (elements past the f16 limit of 65504). Scores of order q_scale
+    give a flat softmax at 1e-5 and a nearly one-hot one at 3e4; both meet the oracle."""
+    g = torch.Generator().manual_seed(31)
+    B, H, L, d, Dv = 2, 3, 700, 64, 128
+    q1, q2 = ((torch.randn(B, H, d, generator=g) * q_scale).to(torch.bfloat16) for _ in range(2))
+    kv = {"k1": torch.randn(B, H, L, d, generator=g), "k2": torch.randn(B, H, L, d, generator=g),
+          "v": torch.randn(B, H, L, Dv, generator=g)}
+    scales = tuple(float(kv[k].abs().max()) / 448.0 for k in ("k1", "k2", "v"))
+    q8 = {k: _quant(kv[k], s) for k, s in zip(("k1", "k2", "v"), scales)}
+    deq = {k: q8[k].float() * s for k, s in zip(("k1", "k2", "v"), scales)}
+    lens_l = [700, 333]
+    lens = torch.tensor(lens_l, dtype=torch.int32, device="cuda")
+    pools, table = {}, None
+    for k in q8:
+        pools[k], table = _paged(q8[k], seed=8)
+    got = da.diffattn_decode_paged(q1.cuda(), q2.cuda(), pools["k1"].cuda(), pools["k2"].cuda(), pools["v"].cuda(),
+                                   table.cuda(), lens, 0.6, 0.3, L=L, scales=scales)
+    torch.cuda.synchronize()
+    ref = orc.diffattn_decode(q1, q2, deq["k1"], deq["k2"], deq["v"], lens_l, 0.6, 0.3)
+    assert_bf16_parity(got, ref, f"fp8 decode, queries x {q_scale}")
 
 
 def test_fp8_append_quantizes_like_a_cast_and_saturates():
