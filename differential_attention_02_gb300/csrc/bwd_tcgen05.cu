@@ -19,11 +19,13 @@
 // Each gradient row is written by exactly one CTA, so there are no atomics and
 // the result does not depend on scheduling.
 //
-// Both kernels keep S, dA and the gradient accumulators in TMEM; the products
+// Both kernels keep S, dA and the gradient accumulators in TMEM. The products
 // whose left operand is elementwise data (dS or A, rounded to the operand type)
-// read it from TMEM like the forward's P.V, so shared memory only serves the
-// tiles the copy engine loads.
+// read it from TMEM in bwd_dq, like the forward's P.V, and from shared memory in
+// bwd_dkdv, where that frees the score columns for the next step's products.
 #include <math.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -322,14 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 // ============================================================================
 // bwd_dkdv: one CTA per 128-key tile of one (b, h); query steps of 64 rows.
 // ============================================================================
-// TMEM (keys = lanes): S1^T [0,64), S2^T [64,128), dA^T [128,192) for the step's
-// 64 queries; dV [192,320), dK1 [320,384), dK2 [384,448). After the elementwise
-// pass, A^T = P1 - lambda P2 sits in S1^T's first 32 columns, dS1^T in S2^T's and
-// dS2^T in dA^T's (16-bit pairs), the left operands of
+// TMEM (keys = lanes): S1^T [0,64), S2^T [64,128), dA^T [128,192) for one step's
+// 64 queries; dV [192,320), dK1 [320,384), dK2 [384,448). The elementwise warps
+// write A^T = P1 - lambda P2, dS1^T and dS2^T (operand type) to shared memory as
+// K-major 128-byte-swizzled tiles, the left operands of
 //   dV += A^T dO,  dK1 += dS1^T Q1,  dK2 += dS2^T Q2.
+// The score columns are free as soon as the elementwise warps have loaded them,
+// so the products of step t+1's scores run while step t's elementwise work does:
+//   S/dA(0) ... [loads of S/dA(t)] S/dA(t+1) [elementwise t, stores] dV/dK(t) ...
 // Warps 0..3 handle the step's queries 0..31, warps 4..7 queries 32..63 (every
-// key row); the two groups meet at a named barrier between reading their inputs
-// and writing the 16-bit results, which overwrite columns the other group reads.
+// key row).
 namespace dkdv {
 constexpr int kSQ = 64;                        // queries per step
 constexpr int kStages = 3;
@@ -338,24 +342,44 @@ constexpr int kVBytes = BM * kDV * 2;          // V tile, 32 KB
 constexpr int kQBytes = kSQ * kD * 2;          // Q step, 8 KB
 constexpr int kOBytes = kSQ * kDV * 2;         // dO step, 16 KB
 constexpr int kSBytes = kSQ * 16;              // stats of the step, 1 KB
+constexpr int kPBytes = BM * kSQ * 2;          // one elementwise result tile, 16 KB
 constexpr int kStageBytes = 2 * kQBytes + kOBytes + 1024;  // + stats, padded to keep tiles 1024-aligned
-constexpr int kOffK1 = 0, kOffK2 = kKBytes, kOffV = 2 * kKBytes, kOffStages = 2 * kKBytes + kVBytes;
+constexpr int kOffK1 = 0, kOffK2 = kKBytes, kOffV = 2 * kKBytes, kOffP = 2 * kKBytes + kVBytes;
+constexpr int kOffStages = kOffP + 3 * kPBytes;
 constexpr int kOffBar = kOffStages + kStages * kStageBytes;
 constexpr size_t kSmem = 1024 + (size_t)kOffBar + 256;
 static_assert(kSmem <= 232448, "shared memory budget");
+static_assert(kOffP % 1024 == 0 && kOffStages % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled tiles");
 constexpr uint32_t kColS1 = 0, kColS2 = 64, kColA = 128, kColV = 192, kColK1 = 320, kColK2 = 384;
+// Register split: the MMA warp's loop (two waits and two groups of products per step) needs
+// more than 56 registers; the elementwise warps need far fewer than 216.
+constexpr int kRegsMathKV = 216, kRegsOtherKV = 72;
+static_assert(2 * 128 * kRegsMathKV + 128 * kRegsOtherKV <= kThreads * kRegsLaunch, "register split");
 
 struct Bars {
     uint64_t kv_full;
     uint64_t q_full[kStages], q_empty[kStages];
     uint64_t s_full;      // S1^T, S2^T, dA^T of the step in TMEM
-    uint64_t p_full;      // A^T, dS1^T, dS2^T of the step in TMEM (8 warps)
+    uint64_t s_free;      // every elementwise warp has loaded them (8 warps)
+    uint64_t p_full;      // A^T, dS1^T, dS2^T of the step in shared memory (8 warps)
+    uint64_t p_empty;     // the products that read them completed
     uint64_t acc_done;    // the last products completed
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 }  // namespace dkdv
+
+// D (+)= A[smem, K-major] * B[smem, MN-major]: one K=16 step advances 32 bytes in A's
+// 128-byte rows and 16 rows of 128 bytes in B.
+template <int KSTEPS>
+__device__ __forceinline__ void mma_kmajor_mn(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk)
+        umma_ss(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 128), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
 
 template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdTcParams p) {
@@ -365,14 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
     volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = (p.N + BM - 1) / BM;
     const int BH = p.B * p.H;
     const int kt = (int)(blockIdx.x / BH);  // key tile; the first ones see the most queries
     const int bh = blockIdx.x % BH, b = bh / p.H, h = bh % p.H;
     const int k0 = kt * BM;
     const int qs0 = p.causal ? k0 : 0;                 // first query that can see these keys
     const int nsteps = (p.N - qs0 + kSQ - 1) / kSQ;    // query steps of 64 rows
-    (void)n_tiles;
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->kv_full, 1);
@@ -381,7 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             mbar_init(&bars->q_empty[s], 1);
         }
         mbar_init(&bars->s_full, 1);
+        mbar_init(&bars->s_free, 8);
         mbar_init(&bars->p_full, 8);
+        mbar_init(&bars->p_empty, 1);
         mbar_init(&bars->acc_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -398,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     uint8_t* stages = smem + kOffStages;
 
     if (warp >= 8) {
-        setmaxnreg_dec<kRegsOther>();
+        setmaxnreg_dec<kRegsOtherKV>();
         if (warp == kWarpProducer) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars->kv_full, 2 * kKBytes + kVBytes);
@@ -427,12 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             }
         } else if (warp == kWarpMma) {
             const bool lead = elect_one();
-            const uint64_t dk1 = sdesc_sw128(smem_u32(smem + kOffK1), 16, 1024);
-            const uint64_t dk2 = sdesc_sw128(smem_u32(smem + kOffK2), 16, 1024);
-            const uint64_t dv = sdesc_sw128(smem_u32(smem + kOffV), 16, 1024);
-            const uint64_t dst0 = sdesc_sw128(smem_u32(stages), 16, 1024);          // K-major step tiles
+            // K-major descriptors differ only in the start address (bytes >> 4, far below the
+            // field's 2^14 limit for shared memory): one base plus constant offsets.
+            const uint64_t dk1 = sdesc_sw128(smem_u32(smem), 16, 1024);
+            const uint64_t dk2 = dk1 + (kOffK2 >> 4), dv = dk1 + (kOffV >> 4);
+            const uint64_t dpa = dk1 + (kOffP >> 4);                                // A^T, K-major
+            const uint64_t dst0 = dk1 + (kOffStages >> 4);                          // K-major step tiles
             const uint64_t dsn0 = sdesc_sw128(smem_u32(stages), kSQ * 128, 1024);   // MN-major step tiles
             constexpr uint64_t kStep = kStageBytes >> 4, kQ2 = kQBytes >> 4, kO = (2 * kQBytes) >> 4;
+            constexpr uint64_t kP = kPBytes >> 4;
             constexpr uint32_t id_s = idesc_kind_f16(BM, kSQ, 0, 0, F16);    // S^T, dA^T: 128 x 64
             constexpr uint32_t id_v = idesc_kind_f16(BM, kDV, 0, 1, F16);    // dV: 128 x 128, B MN-major
             constexpr uint32_t id_k = idesc_kind_f16(BM, kD, 0, 1, F16);     // dK: 128 x 64, B MN-major
@@ -454,17 +481,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 const int s = t % kStages, s1 = (t + 1) % kStages;
                 const bool more = t + 1 < nsteps;
                 const uint64_t st = (uint64_t)s * kStep;
-                ok = mbar_wait_warp(&bars->p_full, t & 1, abort_flag, p.err, 0xE7) &&
-                     (!more || mbar_wait_warp(&bars->q_full[s1], ((t + 1) / kStages) & 1, abort_flag, p.err, 0xE8));
+                if (more) {
+                    // step t+1's scores overwrite step t's once the elementwise warps hold them
+                    ok = mbar_wait_warp(&bars->s_free, t & 1, abort_flag, p.err, 0xE7) &&
+                         mbar_wait_warp(&bars->q_full[s1], ((t + 1) / kStages) & 1, abort_flag, p.err, 0xE8);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lead) issue_scores(s1);
+                    __syncwarp();
+                }
+                ok = mbar_wait_warp(&bars->p_full, t & 1, abort_flag, p.err, 0xEA);
                 if (!ok) break;
                 tc_fence_after();
                 if (lead) {
-                    mma_tmem_a<kSQ / 16>(tmem + kColV, tmem + kColS1, dsn0 + st + kO, id_v, t > 0);
-                    mma_tmem_a<kSQ / 16>(tmem + kColK1, tmem + kColS2, dsn0 + st, id_k, t > 0);
-                    mma_tmem_a<kSQ / 16>(tmem + kColK2, tmem + kColA, dsn0 + st + kQ2, id_k, t > 0);
+                    mma_kmajor_mn<kSQ / 16>(tmem + kColV, dpa, dsn0 + st + kO, id_v, t > 0);
+                    mma_kmajor_mn<kSQ / 16>(tmem + kColK1, dpa + kP, dsn0 + st, id_k, t > 0);
+                    mma_kmajor_mn<kSQ / 16>(tmem + kColK2, dpa + 2 * kP, dsn0 + st + kQ2, id_k, t > 0);
                     umma_commit(&bars->q_empty[s]);
-                    if (more) issue_scores(s1);
-                    else umma_commit(&bars->acc_done);
+                    umma_commit(&bars->p_empty);
+                    if (!more) umma_commit(&bars->acc_done);
                 }
                 __syncwarp();
             }
@@ -482,30 +517,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     }
 
     // ---------------------------------------------------------------- elementwise
-    setmaxnreg_inc<kRegsMath>();
+    setmaxnreg_inc<kRegsMathKV>();
     const int g = warp >> 2, lg = warp & 3;
     const int r = lg * 32 + lane;  // key row within the tile
     const int key = k0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
     const float sl2 = p.scale_log2, lam = p.lambda;
     constexpr int kHQ = kSQ / 2;  // queries per group and step
-    // Every warp runs every step, so both groups reach each named barrier the same
-    // number of times; after an abort (a wait that gave up, *abort raised) the waits
-    // return at once and the steps only pass the barrier.
+    // This thread's row of each result tile: 128 bytes, 16-byte chunk c at c ^ (r % 8).
+    uint8_t* prow = smem + kOffP + r * 128;
     bool ok = true;
-    for (int t = 0; t < nsteps; ++t) {
+    for (int t = 0; ok && t < nsteps; ++t) {
         const int s = t % kStages;
-        ok = ok && mbar_wait_warp(&bars->s_full, t & 1, abort_flag, p.err, 0xF0);
+        ok = mbar_wait_warp(&bars->s_full, t & 1, abort_flag, p.err, 0xF0);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s1[kHQ], s2[kHQ], a[kHQ];
+        tmem_ld32(lane_base + kColS1 + g * kHQ, s1);
+        tmem_ld32(lane_base + kColS2 + g * kHQ, s2);
+        tmem_ld32(lane_base + kColA + g * kHQ, a);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free);
+
+        const float4* stats = reinterpret_cast<const float4*>(stages + s * kStageBytes + 2 * kQBytes + kOBytes);
+        const int qbase = qs0 + t * kSQ + g * kHQ;  // first query of this group's columns
+        // Every (query, key) pair of the group visible: no masks (warp-uniform).
+        const bool full = (!p.causal || qbase >= k0 + BM - 1) && qbase + kHQ <= p.N;
         uint32_t pa[kHQ / 2], p1[kHQ / 2], p2[kHQ / 2];
-        if (ok) {
-            tc_fence_after();
-            const float4* stats = reinterpret_cast<const float4*>(stages + s * kStageBytes + 2 * kQBytes + kOBytes);
-            const int qbase = qs0 + t * kSQ + g * kHQ;  // first query of this group's columns
-            uint32_t s1[kHQ], s2[kHQ], a[kHQ];
-            tmem_ld32(lane_base + kColS1 + g * kHQ, s1);
-            tmem_ld32(lane_base + kColS2 + g * kHQ, s2);
-            tmem_ld32(lane_base + kColA + g * kHQ, a);
-            tmem_ld_wait();
+        auto elementwise = [&](auto masked) {
 #pragma unroll
             for (int i = 0; i < kHQ; i += 2) {
                 float va[2], v1[2], v2[2];
@@ -513,30 +554,46 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 for (int k = 0; k < 2; ++k) {
                     const int q = qbase + i + k;
                     const float4 st = stats[g * kHQ + i + k];  // L1, L2, D1, D2 of query q (broadcast read)
-                    const bool vis = q < p.N && (!p.causal || key <= q);
-                    const float e1 = vis ? fast_exp2(fmaf(__uint_as_float(s1[i + k]), sl2, -st.x)) : 0.f;
-                    const float e2 = vis ? fast_exp2(fmaf(__uint_as_float(s2[i + k]), sl2, -st.y)) : 0.f;
+                    float e1 = fast_exp2(fmaf(__uint_as_float(s1[i + k]), sl2, -st.x));
+                    float e2 = fast_exp2(fmaf(__uint_as_float(s2[i + k]), sl2, -st.y));
                     const float da = __uint_as_float(a[i + k]);
+                    float d1 = da - st.z, d2 = fmaf(-lam, da, -st.w);
+                    if constexpr (decltype(masked)::value) {
+                        // a query past N reads another row's statistics: every result is zeroed
+                        const bool vis = q < p.N && (!p.causal || key <= q);
+                        e1 = vis ? e1 : 0.f;
+                        e2 = vis ? e2 : 0.f;
+                        d1 = vis ? d1 : 0.f;
+                        d2 = vis ? d2 : 0.f;
+                    }
                     va[k] = fmaf(-lam, e2, e1);
-                    v1[k] = vis ? e1 * (da - st.z) : 0.f;   // a query past N reads another row's statistics
-                    v2[k] = vis ? e2 * fmaf(-lam, da, -st.w) : 0.f;
+                    v1[k] = e1 * d1;
+                    v2[k] = e2 * d2;
                 }
                 pa[i / 2] = pack_p<F16>(va[0], va[1]);
                 p1[i / 2] = pack_p<F16>(v1[0], v1[1]);
                 p2[i / 2] = pack_p<F16>(v2[0], v2[1]);
             }
+        };
+        if (full) elementwise(std::false_type{});
+        else elementwise(std::true_type{});
+
+        // the previous step's products have read the tiles this step overwrites
+        if (t > 0) ok = mbar_wait_warp(&bars->p_empty, (t - 1) & 1, abort_flag, p.err, 0xF2);
+        if (!ok) break;
+#pragma unroll
+        for (int j = 0; j < kHQ / 8; ++j) {
+            const int c = g * (kHQ / 8) + j;  // 16-byte chunk: queries 8c .. 8c+7 of the step
+            const uint32_t off = (uint32_t)((c ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(prow + off) = make_uint4(pa[4 * j], pa[4 * j + 1], pa[4 * j + 2], pa[4 * j + 3]);
+            *reinterpret_cast<uint4*>(prow + kPBytes + off) =
+                make_uint4(p1[4 * j], p1[4 * j + 1], p1[4 * j + 2], p1[4 * j + 3]);
+            *reinterpret_cast<uint4*>(prow + 2 * kPBytes + off) =
+                make_uint4(p2[4 * j], p2[4 * j + 1], p2[4 * j + 2], p2[4 * j + 3]);
         }
-        // Both groups have read their inputs before either overwrites the other's columns.
-        named_bar_sync(1, 256);
-        if (ok) {
-            tmem_st16(lane_base + kColS1 + g * (kHQ / 2), pa);
-            tmem_st16(lane_base + kColS2 + g * (kHQ / 2), p1);
-            tmem_st16(lane_base + kColA + g * (kHQ / 2), p2);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full);
-        }
+        fence_proxy_async_shared();  // the tensor core reads these through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
     }
     // ---------------------------------------------------------------- epilogue: dV, dK rows
     if (ok && nsteps > 0) ok = mbar_wait_warp(&bars->acc_done, 0, abort_flag, p.err, 0xF1);
