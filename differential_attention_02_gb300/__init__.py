@@ -26,7 +26,7 @@ EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffat
             "diffattn_decode_paged", "diffattn_kv_append_paged", "diffattn_add_rmsnorm", "diffattn_swiglu",
             "diffattn_bwd", "diffattn_bwd_workspace_size", "diffattn_lambda_bwd", "diffattn_decode_paged_fp8",
             "diffattn_kv_append_paged_fp8", "diffattn_decode_noalloc_read_error",
-            "diffattn_selftest_timeout")
+            "diffattn_selftest_timeout", "diffattn_gemm_residual", "diffattn_gemm_swiglu")
 
 
 class DiffAttnError(RuntimeError):
@@ -72,6 +72,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_gemm_bf16.argtypes = [vp, vp, vp, i32, i32, i32, i64, i64, i64, i32, vp, sz, vp]
     lib.diffattn_gemm_f16.restype = i32
     lib.diffattn_gemm_f16.argtypes = lib.diffattn_gemm_bf16.argtypes
+    lib.diffattn_gemm_residual.restype = i32
+    lib.diffattn_gemm_residual.argtypes = [vp] * 7 + [i32] * 3 + [i64] * 5 + [i32] * 3 + [vp, sz, vp]
+    lib.diffattn_gemm_swiglu.restype = i32
+    lib.diffattn_gemm_swiglu.argtypes = [vp, vp, vp, vp, i32, f32, f32, i32, i32, i32, i64, i64, i64, i32, i32, vp, sz,
+                                         vp]
     lib.diffattn_gemm_workspace_size.restype = i32
     lib.diffattn_gemm_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
     lib.diffattn_decode_noalloc.restype = i32
@@ -375,27 +380,92 @@ def swiglu(gate_up, out_dtype=torch.bfloat16, stream=None):
     return h
 
 
-def layer_fwd(x, w_q, w_k, w_v, w_o, w_gate_up, w_down, n_heads: int, lam: float, lam_init: float,
-              eps: float = 1e-5, norm1_weight=None, norm2_weight=None, head_weight=None, ws=None, stream=None):
+def interleave_gate_up(w_gate, w_up):
+    """[K, F] gate and up weights -> [K, 2F] with 128-column blocks interleaved: columns
+    256 t .. 256 t + 127 hold w_gate[:, 128 t : 128 t + 128], the next 128 w_up's (the layout
+    gemm_swiglu reads). F a multiple of 128. A one-time weight transform."""
+    K, F = w_gate.shape
+    if w_up.shape != (K, F) or F % 128:
+        raise ValueError("w_gate and w_up [K, F] with F a multiple of 128")
+    return torch.stack([w_gate.reshape(K, F // 128, 128), w_up.reshape(K, F // 128, 128)], dim=2).reshape(
+        K, 2 * F).contiguous()
+
+
+def layer_fwd(x, w_q, w_k, w_v, w_o, w_gu, w_down, n_heads: int, lam: float, lam_init: float,
+              eps: float = 1e-5, norm1_weight=None, norm2_weight=None, head_weight=None, ws=None, stream=None,
+              w_qkv=None):
     """One DIFF Transformer layer: Y = MultiHead(RMSNorm(X)) + X, X' = SwiGLU(RMSNorm(Y)) + Y.
 
-    x: [B, N, d_model] bf16 or fp32; module weights as in module_fwd; w_gate_up: [d_model, 2*d_ff]
-    = [W_gate | W_up]; w_down: [d_ff, d_model]; every weight bf16, or every weight fp16, and the
-    GEMM operands (the RMSNorm outputs, the attention output, the SwiGLU output) take that type;
-    norm weights fp32 [d_model], head_weight fp32 [Dv] (the per-head RMSNorm's gain). Returns
-    X' [B, N, d_model] fp32 (the residual stream is kept in fp32; the gate/up output is fp16)."""
+    x: [B, N, d_model] bf16 or fp32; module weights as in module_fwd (w_qkv, if given, is
+    torch.cat([w_q, w_k, w_v], 1): one projection GEMM instead of three); w_gu: [d_model, 2*d_ff]
+    gate and up weights interleaved by interleave_gate_up; w_down: [d_ff, d_model]; every weight
+    bf16, or every weight fp16, and the GEMM operands take that type; norm weights fp32 [d_model],
+    head_weight fp32 [Dv] (the per-head RMSNorm's gain). d_model a multiple of 256, d_ff of 128.
+    Returns X' [B, N, d_model] fp32 (the residual stream is kept in fp32).
+
+    Six launches: RMSNorm of X; the QKV projection; the fused attention; W_O with the residual
+    add in its epilogue, which also writes Y (times norm2's gain) as the next operand and the row
+    sums of Y^2; gate/up with SwiGLU in its epilogue, scaled by 1/RMS(Y) per row
+    (RMSNorm(Y) W = (Y W) / r); W_down with the second residual add.
+
+    Range: the 16-bit operand copy of Y (times norm2's gain) is taken before the
+    normalisation, so fp16 weights need |Y * g| <= 65504; bf16 weights have fp32's range."""
     B, N, dm = x.shape
     M = B * N
-    op = w_q.dtype
+    op = (w_qkv if w_qkv is not None else w_q).dtype
     _, n1 = add_rmsnorm(x, weight=norm1_weight, eps=eps, n_dtype=op, stream=stream)
-    a = module_fwd(n1, w_q, w_k, w_v, w_o, n_heads, lam, lam_init, eps, norm_weight=head_weight, ws=ws,
-                   stream=stream, out_dtype=torch.float32)
-    y, n2 = add_rmsnorm(x, a, weight=norm2_weight, eps=eps, want_y=True, n_dtype=op, stream=stream)
-    gu = gemm(n2.view(M, dm), w_gate_up, out_dtype=torch.float16, ws=ws, stream=stream)
-    h = swiglu(gu, out_dtype=op, stream=stream)
-    f = gemm(h, w_down, out_dtype=torch.float32, ws=ws, stream=stream)
-    out, _ = add_rmsnorm(y, f.view(B, N, dm), eps=eps, want_y=True, want_n=False, stream=stream)
-    return out
+    att = _module_attention(n1, w_q, w_k, w_v, n_heads, lam, lam_init, eps, head_weight, ws, stream, op, w_qkv)
+    y, y16, sq = gemm_residual(att, w_o, x.reshape(M, dm), c16_dtype=op, c16_gain=norm2_weight, want_row_sq=True,
+                               ws=ws, stream=stream)
+    h = gemm_swiglu(y16, w_gu, row_sq=sq, sq_count=dm, eps=eps, out_dtype=op, ws=ws, stream=stream)
+    out, _, _ = gemm_residual(h, w_down, y, ws=ws, stream=stream)
+    return out.view(B, N, dm)
+
+
+def gemm_residual(a, w, r, c16_dtype=None, c16_gain=None, want_row_sq=False, out=None, ws=None, stream=None):
+    """C = a @ w + r in fp32: a [M, K] and w [K, N] both bf16 or both fp16 (contiguous rows),
+    r [M, N] fp32, bf16 or fp16; N a multiple of 256. Optionally the 16-bit copy C * c16_gain
+    (c16_dtype; c16_gain fp32 [N] or None) and row_sq [M, N // 256] (row sums of C^2 per
+    256-column tile). Returns (C, C16 or None, row_sq or None)."""
+    M, K = a.shape
+    K2, N = w.shape
+    if K2 != K or a.stride(1) != 1 or w.stride(1) != 1 or r.shape != (M, N) or r.stride(1) != 1:
+        raise ValueError("a [M,K], w [K,N], r [M,N] with contiguous rows")
+    if a.dtype != w.dtype or a.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("a and w must both be bf16 or both fp16")
+    c = torch.empty((M, N), dtype=torch.float32, device=a.device) if out is None else out
+    c16 = torch.empty((M, N), dtype=c16_dtype, device=a.device) if c16_dtype is not None else None
+    sq = torch.empty((M, N // 256), dtype=torch.float32, device=a.device) if want_row_sq else None
+    ws = workspace(256, a.device) if ws is None else ws
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    _check(load_library().diffattn_gemm_residual(
+        ptr(a), ptr(w), ptr(r), ptr(c), ptr(c16), ptr(c16_gain), ptr(sq), M, N, K, a.stride(0), w.stride(0),
+        r.stride(0), c.stride(0), c16.stride(0) if c16 is not None else 0, _dtype_code(a.dtype), _dtype_code(r.dtype),
+        _dtype_code(c16_dtype) if c16_dtype is not None else 0, ptr(ws), ws.numel(), _stream_ptr(stream)),
+        "diffattn_gemm_residual")
+    return c, c16, sq
+
+
+def gemm_swiglu(a, w_gu, row_sq=None, sq_count=None, eps: float = 1e-5, out_dtype=torch.float16, ws=None,
+                stream=None):
+    """H = SiLU(g / r) * (u / r): g, u the gate and up columns of a @ w_gu (w_gu [K, 2F] from
+    interleave_gate_up), r = sqrt(sum(row_sq[m]) / sq_count + eps) per row (1 without row_sq).
+    a and w_gu both bf16 or both fp16. Returns H [M, F] of out_dtype (bf16 or fp16)."""
+    M, K = a.shape
+    K2, F2 = w_gu.shape
+    if K2 != K or a.stride(1) != 1 or w_gu.stride(1) != 1:
+        raise ValueError("a [M,K] and w_gu [K,2F] with contiguous rows")
+    h = torch.empty((M, F2 // 2), dtype=out_dtype, device=a.device)
+    ws = workspace(256, a.device) if ws is None else ws
+    n_sq = 0 if row_sq is None else row_sq.shape[1]
+    if row_sq is not None and (row_sq.shape[0] != M or not row_sq.is_contiguous() or sq_count is None):
+        raise ValueError("row_sq [M, n] contiguous, with sq_count")
+    _check(load_library().diffattn_gemm_swiglu(
+        ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(w_gu.data_ptr()), ctypes.c_void_p(h.data_ptr()),
+        None if row_sq is None else ctypes.c_void_p(row_sq.data_ptr()), n_sq, float(sq_count or 1.0), float(eps), M,
+        F2 // 2, K, a.stride(0), w_gu.stride(0), h.stride(0), _dtype_code(a.dtype), _dtype_code(out_dtype),
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream)), "diffattn_gemm_swiglu")
+    return h
 
 
 def gemm(a: torch.Tensor, w: torch.Tensor, out_dtype=torch.bfloat16, out=None, ws=None, stream=None):
@@ -422,8 +492,10 @@ gemm_bf16 = gemm
 
 
 def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float, eps: float = 1e-5,
-               norm_weight=None, ws=None, stream=None, out_dtype=torch.bfloat16, qkv_dtype=torch.float16):
-    """Multi-head differential attention module: three projection GEMMs, the fused
+               norm_weight=None, ws=None, stream=None, out_dtype=torch.bfloat16, qkv_dtype=torch.float16,
+               w_qkv=None):
+    """Multi-head differential attention module: the projection GEMMs (one against
+    w_qkv = torch.cat([w_q, w_k, w_v], 1) when it is given, else three), the fused
     attention reading Q/K/V in place through strided views, and the W_O GEMM.
 
     x [B,N,d_model]; w_q, w_k [d_model, h*2d]; w_v [d_model, h*Dv]; w_o [h*Dv, d_model],
@@ -440,24 +512,46 @@ def module_fwd(x, w_q, w_k, w_v, w_o, n_heads: int, lam: float, lam_init: float,
     no narrower in practice; qkv_dtype=torch.bfloat16 selects bf16 Q, K and V
     (8 significant bits instead of 11) for callers who want bf16 throughout.
     """
+    att = _module_attention(x, w_q, w_k, w_v, n_heads, lam, lam_init, eps, norm_weight, ws, stream, x.dtype, w_qkv,
+                            qkv_dtype)
+    B, N, dm = x.shape
+    y = gemm(att, w_o, out_dtype=out_dtype, ws=ws, stream=stream)
+    return y.view(B, N, dm)
+
+
+def _module_attention(x, w_q, w_k, w_v, n_heads, lam, lam_init, eps, norm_weight, ws, stream, att_dtype, w_qkv=None,
+                      qkv_dtype=torch.float16):
+    """The projections and the fused attention of module_fwd: returns concat(heads) [B*N, h*Dv]
+    of att_dtype, the operand W_O multiplies."""
     if qkv_dtype not in (torch.float16, torch.bfloat16):
         raise ValueError("qkv_dtype must be torch.float16 or torch.bfloat16")
     B, N, dm = x.shape
     h = n_heads
-    d = w_q.shape[1] // (2 * h)
-    Dv = w_v.shape[1] // h
     x2 = x.reshape(B * N, dm)
-    q = gemm(x2, w_q, out_dtype=qkv_dtype, ws=ws, stream=stream)
-    k = gemm(x2, w_k, out_dtype=qkv_dtype, ws=ws, stream=stream)
-    v = gemm(x2, w_v, out_dtype=qkv_dtype, ws=ws, stream=stream)
-    # [B*N, h*2d] -> [B, h, N, 2d] views (no copies): strides (N*h*2d, 2d, h*2d, 1)
-    q4 = q.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
-    k4 = k.view(B, N, h, 2 * d).permute(0, 2, 1, 3)
-    v4 = v.view(B, N, h, Dv).permute(0, 2, 1, 3)
+    if w_qkv is not None:
+        # one GEMM against [W_Q | W_K | W_V]; Q, K, V are column blocks of its output
+        if w_q is not None:
+            d, Dv = w_q.shape[1] // (2 * h), w_v.shape[1] // h
+        else:
+            raise ValueError("w_qkv also needs w_q and w_v (or their shapes) to split the heads")
+        qkv = gemm(x2, w_qkv, out_dtype=qkv_dtype, ws=ws, stream=stream)
+        c = qkv.shape[1]
+        q, k, v = qkv[:, : 2 * d * h], qkv[:, 2 * d * h: 4 * d * h], qkv[:, 4 * d * h:]
+        if c != 4 * d * h + Dv * h:
+            raise ValueError("w_qkv must be torch.cat([w_q, w_k, w_v], 1)")
+    else:
+        d = w_q.shape[1] // (2 * h)
+        Dv = w_v.shape[1] // h
+        q = gemm(x2, w_q, out_dtype=qkv_dtype, ws=ws, stream=stream)
+        k = gemm(x2, w_k, out_dtype=qkv_dtype, ws=ws, stream=stream)
+        v = gemm(x2, w_v, out_dtype=qkv_dtype, ws=ws, stream=stream)
+    # [B*N, h*2d] (column blocks, any row stride) -> [B, h, N, 2d] views, no copies
+    q4 = q.unflatten(0, (B, N)).unflatten(2, (h, 2 * d)).permute(0, 2, 1, 3)
+    k4 = k.unflatten(0, (B, N)).unflatten(2, (h, 2 * d)).permute(0, 2, 1, 3)
+    v4 = v.unflatten(0, (B, N)).unflatten(2, (h, Dv)).permute(0, 2, 1, 3)
     att = diffattn_fwd(q4[..., :d], q4[..., d:], k4[..., :d], k4[..., d:], v4, lam, lam_init, eps, norm_weight,
-                       out_dtype=x.dtype, ws=ws, stream=stream)
-    y = gemm(att.view(B * N, h * Dv), w_o, out_dtype=out_dtype, ws=ws, stream=stream)
-    return y.view(B, N, dm)
+                       out_dtype=att_dtype, ws=ws, stream=stream)
+    return att.view(B * N, h * Dv)
 
 
 _side_streams = {}

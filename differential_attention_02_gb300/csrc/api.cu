@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "../../include/diffattn.h"
@@ -714,18 +715,20 @@ diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes)
 }
 
 namespace {
-diffattn_status gemm_16bit(bool ab_f16, const void* A, const void* W, void* C, int M, int N, int K, int64_t lda,
-                           int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+// Checks shared by the GEMM entry points; fills the operand maps and the map of the
+// output C, which has out_cols columns (N, or N / 2 for the SwiGLU epilogue).
+diffattn_status gemm_setup(GemmParams& p, bool ab_f16, const void* A, const void* W, void* C, int M, int N, int K,
+                           int out_cols, int64_t lda, int64_t ldw, int64_t ldc, int out_dtype, void* workspace,
+                           size_t workspace_bytes) {
     if (M < 1 || N < 1 || K < 1) return DIFFATTN_ERR_INVALID_ARG;
     if (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16 && out_dtype != DIFFATTN_F16)
         return DIFFATTN_ERR_INVALID_ARG;
     if (!A || !W || !C || !aligned16(A) || !aligned16(W) || !aligned16(C)) return DIFFATTN_ERR_INVALID_ARG;
     const int cq = out_dtype == DIFFATTN_F32 ? 4 : 8;
-    if (lda < K || lda % 8 || ldw < N || ldw % 8 || ldc < N || ldc % cq || N % 8) return DIFFATTN_ERR_INVALID_ARG;
+    if (lda < K || lda % 8 || ldw < N || ldw % 8 || ldc < out_cols || ldc % cq || N % 8 || out_cols % 8)
+        return DIFFATTN_ERR_INVALID_ARG;
     if (workspace == nullptr || workspace_bytes < kControlBytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return DIFFATTN_ERR_WORKSPACE;
-    GemmParams p{};
     if (!encode_2d(&p.tm_a, A, K, M, lda, kGemmBK, kGemmBM, ab_f16) ||
         !encode_2d(&p.tm_w, W, N, K, ldw, 64, kGemmBK, ab_f16))
         return DIFFATTN_ERR_INVALID_ARG;
@@ -736,7 +739,7 @@ diffattn_status gemm_16bit(bool ab_f16, const void* A, const void* W, void* C, i
         const CUtensorMapDataType dt = out_dtype == DIFFATTN_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                        : out_dtype == DIFFATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-        cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+        cuuint64_t dims[2] = {(cuuint64_t)out_cols, (cuuint64_t)M};
         cuuint64_t strides[1] = {(cuuint64_t)(ldc * eb)};
         cuuint32_t box[2] = {(cuuint32_t)(128 / eb), 32};
         cuuint32_t es[2] = {1, 1};
@@ -752,9 +755,68 @@ diffattn_status gemm_16bit(bool ab_f16, const void* A, const void* W, void* C, i
     p.out_f16 = out_dtype == DIFFATTN_F16;
     p.ab_f16 = ab_f16;
     p.err = err_word(workspace);
+    return DIFFATTN_OK;
+}
+
+diffattn_status gemm_16bit(bool ab_f16, const void* A, const void* W, void* C, int M, int N, int K, int64_t lda,
+                           int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    GemmParams p{};
+    const diffattn_status st =
+        gemm_setup(p, ab_f16, A, W, C, M, N, K, N, lda, ldw, ldc, out_dtype, workspace, workspace_bytes);
+    if (st != DIFFATTN_OK) return st;
     return cuda_status(launch_gemm_bf16(p, static_cast<cudaStream_t>(stream)));
 }
+
+bool is16(int dtype) { return dtype == DIFFATTN_BF16 || dtype == DIFFATTN_F16; }
 }  // namespace
+
+diffattn_status diffattn_gemm_residual(const void* A, const void* W, const void* R, float* C, void* C16,
+                                       const float* c16_gain, float* row_sq, int M, int N, int K, int64_t lda,
+                                       int64_t ldw, int64_t ldr, int64_t ldc, int64_t ldc16, int ab_dtype,
+                                       int r_dtype, int c16_dtype, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+    if (!is16(ab_dtype) || !(r_dtype == DIFFATTN_F32 || is16(r_dtype))) return DIFFATTN_ERR_INVALID_ARG;
+    if (N % kGemmBN) return DIFFATTN_ERR_INVALID_ARG;
+    const int rq = r_dtype == DIFFATTN_F32 ? 4 : 8;
+    if (!R || !aligned16(R) || ldr < N || ldr % rq) return DIFFATTN_ERR_INVALID_ARG;
+    if (C16 && (!is16(c16_dtype) || !aligned16(C16) || ldc16 < N || ldc16 % 8)) return DIFFATTN_ERR_INVALID_ARG;
+    if (c16_gain && !C16) return DIFFATTN_ERR_INVALID_ARG;
+    GemmParams p{};
+    const diffattn_status st = gemm_setup(p, ab_dtype == DIFFATTN_F16, A, W, C, M, N, K, N, lda, ldw, ldc,
+                                          DIFFATTN_F32, workspace, workspace_bytes);
+    if (st != DIFFATTN_OK) return st;
+    p.mode = 1;
+    p.resid = R;
+    p.ld_r = ldr;
+    p.r_dtype = r_dtype == DIFFATTN_F32 ? 0 : (r_dtype == DIFFATTN_BF16 ? 1 : 2);
+    p.c16 = C16;
+    p.ld_c16 = ldc16;
+    p.c16_f16 = c16_dtype == DIFFATTN_F16;
+    p.c16_gain = c16_gain;
+    p.row_sq = row_sq;
+    return cuda_status(launch_gemm_bf16(p, static_cast<cudaStream_t>(stream)));
+}
+
+diffattn_status diffattn_gemm_swiglu(const void* A, const void* W_gu, void* H, const float* row_sq, int n_sq,
+                                     float sq_count, float eps, int M, int F, int K, int64_t lda, int64_t ldw,
+                                     int64_t ldh, int ab_dtype, int h_dtype, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+    if (!is16(ab_dtype) || !is16(h_dtype)) return DIFFATTN_ERR_INVALID_ARG;
+    if (F < 1 || F % (kGemmBN / 2)) return DIFFATTN_ERR_INVALID_ARG;
+    if (row_sq && (n_sq < 1 || !(sq_count > 0.f) || !(eps >= 0.f) || !std::isfinite(sq_count) || !std::isfinite(eps)))
+        return DIFFATTN_ERR_INVALID_ARG;
+    GemmParams p{};
+    const diffattn_status st = gemm_setup(p, ab_dtype == DIFFATTN_F16, A, W_gu, H, M, 2 * F, K, F, lda, ldw, ldh,
+                                          h_dtype, workspace, workspace_bytes);
+    if (st != DIFFATTN_OK) return st;
+    p.mode = 2;
+    p.row_sq_in = row_sq;
+    p.n_sq = row_sq ? n_sq : 0;
+    p.sq_count = sq_count;
+    p.eps = eps;
+    return cuda_status(launch_gemm_bf16(p, static_cast<cudaStream_t>(stream)));
+}
 
 diffattn_status diffattn_gemm_bf16(const void* A, const void* W, void* C, int M, int N, int K, int64_t lda,
                                    int64_t ldw, int64_t ldc, int out_dtype, void* workspace, size_t workspace_bytes,

@@ -16,6 +16,14 @@
 // warps 2..5 = epilogue: warp w owns TMEM lanes (tile rows) 32*(w%4)..+31 and
 // writes them through 128-byte-swizzled shared-memory boxes with TMA stores,
 // 64 columns per pass.
+//
+// Epilogue modes for the DIFF Transformer layer ("The Overall Architecture Of The
+// Multi-Head Differential Transformer", intoai.pub; "Estrutura multi-head e
+// arquitetura completa", hada): the residual add Y = X + MultiHead(.) with the
+// row sums of Y^2 its RMSNorm needs and a 16-bit copy of Y (times the norm's gain)
+// as the next GEMM's operand, since RMSNorm(Y) W = (Y (g W)) / r row by row; and
+// the SwiGLU of the gate/up product, scaled by 1/r, so that neither the
+// normalised activations nor the gate/up output make a round trip through HBM.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -167,6 +175,62 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
             tc_fence_after();
             const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
             const uint32_t t_row = tmem + buf * BN + ((uint32_t)(lg * 32) << 16);
+            const int row = m0 + lg * 32 + lane;  // this lane's output row
+            const bool row_ok = row < p.M;
+            if (p.mode == 2) {
+                // SwiGLU: gate columns [0,128) and up columns [128,256) of the tile give output
+                // columns n0/2 + [0,128), 64 per pass. The row scale 1/r from the partial sums.
+                float ir = 1.f;
+                if (p.row_sq_in) {
+                    float ssum = 0.f;
+                    if (row_ok)
+                        for (int i = 0; i < p.n_sq; ++i) ssum += p.row_sq_in[(int64_t)row * p.n_sq + i];
+                    ir = row_ok ? 1.0f / sqrtf(ssum / p.sq_count + p.eps) : 0.f;
+                }
+#pragma unroll 1
+                for (int pass = 0; pass < 2; ++pass) {
+                    if (lane == 0) tma_store_wait_read();
+                    __syncwarp();
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t g[32], u[32];
+                        tmem_ld32(t_row + pass * 64 + c * 32, g);
+                        tmem_ld32(t_row + 128 + pass * 64 + c * 32, u);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float hv[2];
+#pragma unroll
+                                for (int k = 0; k < 2; ++k) {
+                                    const int i = 8 * j + 2 * e + k;
+                                    const float gs = __uint_as_float(g[i]) * ir, us = __uint_as_float(u[i]) * ir;
+                                    hv[k] = gs / (1.0f + expf(-gs)) * us;  // silu(g) * u
+                                }
+                                w4[e] = pack_16x2(hv[0], hv[1], p.out_f16 != 0);
+                            }
+                            *reinterpret_cast<uint4*>(stage + sw128_offset(lane, c * 4 + j)) =
+                                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                    if (pass == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->acc_empty[buf]);
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        index_ok(m0 < p.M && n0 < p.N && m0 >= 0 && n0 >= 0, p.err, 0xB2);
+                        tma_store_2d(&p.tm_c, stage, n0 / 2 + pass * 64, m0 + lg * 32);
+                        tma_store_commit();
+                    }
+                }
+                continue;
+            }
+            float sq = 0.f;  // mode 1: this row's sum of C^2 over the tile
 #pragma unroll 1
             for (int pass = 0; pass < BN / kOutCols; ++pass) {
                 // The staging boxes of this warp must be free (its previous stores read them).
@@ -176,7 +240,68 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                 for (int c = 0; c < kOutCols / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(t_row + pass * kOutCols + c * 32, r);
+                    const int col0 = n0 + pass * kOutCols + c * 32;  // first of these 32 columns
+                    float res[32];
+                    if (p.mode == 1) {
+                        // residual row slice, fetched while the TMEM load is in flight
+                        if (row_ok) {
+                            if (p.r_dtype == 0) {
+                                const float4* src =
+                                    reinterpret_cast<const float4*>(static_cast<const float*>(p.resid) + row * p.ld_r + col0);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const float4 v = src[q];
+                                    res[4 * q] = v.x; res[4 * q + 1] = v.y; res[4 * q + 2] = v.z; res[4 * q + 3] = v.w;
+                                }
+                            } else {
+                                const uint4* src = reinterpret_cast<const uint4*>(
+                                    static_cast<const uint16_t*>(p.resid) + row * p.ld_r + col0);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const uint4 v = src[q];
+                                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        float2 f2;
+                                        if (p.r_dtype == 2) f2 = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                                        else f2 = make_float2(bf16lo_to_f32(w4[e]), bf16hi_to_f32(w4[e]));
+                                        res[8 * q + 2 * e] = f2.x;
+                                        res[8 * q + 2 * e + 1] = f2.y;
+                                    }
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) res[i] = 0.f;
+                        }
+                    }
                     tmem_ld_wait();
+                    if (p.mode == 1) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float y = __uint_as_float(r[i]) + res[i];
+                            r[i] = __float_as_uint(y);
+                            sq = fmaf(y, y, sq);
+                        }
+                        if (p.c16 && row_ok) {
+                            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.c16) + row * p.ld_c16 + col0);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int i = 8 * q + 2 * e;
+                                    float a0 = __uint_as_float(r[i]), a1 = __uint_as_float(r[i + 1]);
+                                    if (p.c16_gain) {
+                                        a0 *= p.c16_gain[col0 + i];
+                                        a1 *= p.c16_gain[col0 + i + 1];
+                                    }
+                                    w4[e] = pack_16x2(a0, a1, p.c16_f16 != 0);
+                                }
+                                dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            }
+                        }
+                    }
                     if (eb == 2) {
                         // 32 columns = half a box row: 16-byte chunks c*4 .. c*4+3 of the one box.
 #pragma unroll
@@ -218,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                     tma_store_commit();
                 }
             }
+            if (p.mode == 1 && p.row_sq && row_ok) p.row_sq[(int64_t)row * tiles_n + n0 / BN] = sq;
         }
         if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         __syncwarp();

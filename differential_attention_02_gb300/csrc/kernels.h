@@ -128,6 +128,23 @@ struct GemmParams {
     int M, N, K, out_bf16, out_f16;  // output bf16, fp16, or fp32 when both are 0
     int ab_f16;                      // operands A and W fp16 (1) or bf16 (0)
     int32_t* err;
+    // Epilogue. mode 0: C = A.W. mode 1 (residual): C = A.W + R in fp32 (N a multiple of
+    // 256); optionally a 16-bit copy C * gain and per-tile row sums of C^2. mode 2
+    // (SwiGLU): the columns of W are gate and up blocks of 128 interleaved per 256-column
+    // tile; C[m, j] = silu(g / r) * (u / r), C has N / 2 columns, r the row's RMS from
+    // the partial sums of squares row_sq_in (r = 1 without them).
+    int mode = 0;
+    const void* resid = nullptr;     // mode 1: R [M, N], row stride ld_r elements
+    int64_t ld_r = 0;
+    int r_dtype = 0;                 // 0 fp32, 1 bf16, 2 fp16
+    void* c16 = nullptr;             // mode 1 (optional): 16-bit copy, row stride ld_c16 elements
+    int64_t ld_c16 = 0;
+    int c16_f16 = 0;                 // copy fp16 (1) or bf16 (0)
+    const float* c16_gain = nullptr; // mode 1 (optional): per-column factor of the copy
+    float* row_sq = nullptr;         // mode 1 (optional): [M, N / 256] sums of C^2 per 256-column tile
+    const float* row_sq_in = nullptr;  // mode 2 (optional): [M, n_sq] partial sums of squares
+    int n_sq = 0;
+    float sq_count = 1.f, eps = 0.f; // mode 2: r = sqrt(sum / sq_count + eps)
 };
 cudaError_t launch_gemm_bf16(const GemmParams& p, cudaStream_t stream);
 constexpr int kGemmBM = 128;

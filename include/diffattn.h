@@ -440,6 +440,51 @@ diffattn_status diffattn_gemm_f16(const void* A, const void* W, void* C, int M, 
 diffattn_status diffattn_gemm_workspace_size(int M, int N, int K, size_t* bytes);
 
 /*
+ * diffattn_gemm_residual — C = A . W + R in fp32 (tcgen05 GEMM with a fused
+ * epilogue), for the DIFF Transformer layer's residual connections
+ * Y = MultiHead(RMSNorm(X)) + X and X' = SwiGLU(RMSNorm(Y)) + Y ("The Overall
+ * Architecture Of The Multi-Head Differential Transformer", intoai.pub;
+ * "Estrutura multi-head e arquitetura completa", hada).
+ * A [M, K] (lda) and W [K, N] (ldw) row-major, both ab_dtype (bf16 or f16);
+ * R [M, N] row-major (ldr), r_dtype f32, bf16 or f16; C [M, N] fp32 (ldc).
+ * Optional outputs (NULL to skip):
+ *   C16 [M, N] (ldc16), c16_dtype bf16 or f16: C times c16_gain[N] (per column;
+ *     NULL = 1), rounded — the next GEMM's operand, RMSNorm(C) W being
+ *     (C (g W)) / r row by row;
+ *   row_sq [M, N / 256] fp32: row m's sum of C^2 over columns 256 t .. 256 t + 255
+ *     in entry m * (N / 256) + t (the partial sums of the RMSNorm's mean square).
+ * N a multiple of 256; M, K >= 1; pointers 16-byte aligned (row_sq 4-byte);
+ * lda, ldw, ldc16 multiples of 8, ldc a multiple of 4, ldr a multiple of 4
+ * (fp32 R) or 8; c16_gain only with C16. Workspace as diffattn_gemm_bf16.
+ * Errors: DIFFATTN_ERR_INVALID_ARG / _WORKSPACE before anything is launched.
+ */
+diffattn_status diffattn_gemm_residual(const void* A, const void* W, const void* R, float* C, void* C16,
+                                       const float* c16_gain, float* row_sq, int M, int N, int K,
+                                       int64_t lda, int64_t ldw, int64_t ldr, int64_t ldc, int64_t ldc16,
+                                       int ab_dtype, int r_dtype, int c16_dtype,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * diffattn_gemm_swiglu — the feed-forward block's first product and SwiGLU in
+ * one launch (same sections; "Feed-forward network (FFN) (applying the SwiGLU
+ * activation function)"): H[m, j] = SiLU(g / r) * (u / r), SiLU(t) = t / (1 + e^-t),
+ * where g and u are the gate and up columns of A . W_gu and r the RMS of row m of
+ * the RMSNorm input: r = sqrt(sum_{t < n_sq} row_sq[m * n_sq + t] / sq_count + eps)
+ * (r = 1 when row_sq is NULL). With A the unnormalised rows and the RMSNorm's gain
+ * folded into A (diffattn_gemm_residual's c16_gain), this is SwiGLU(RMSNorm(.) W).
+ * W_gu [K, 2F] row-major (ldw): gate and up blocks of 128 columns interleaved,
+ * columns 256 t .. 256 t + 127 = W_gate columns 128 t .., 256 t + 128 .. 256 t + 255
+ * = W_up columns 128 t ..; F a multiple of 128. A [M, K] (lda), ab_dtype bf16 or
+ * f16 as W_gu; H [M, F] (ldh), h_dtype bf16 or f16. sq_count > 0 and eps >= 0
+ * finite when row_sq is given, n_sq >= 1. Alignment, workspace and errors as
+ * diffattn_gemm_bf16.
+ */
+diffattn_status diffattn_gemm_swiglu(const void* A, const void* W_gu, void* H, const float* row_sq, int n_sq,
+                                     float sq_count, float eps, int M, int F, int K, int64_t lda, int64_t ldw,
+                                     int64_t ldh, int ab_dtype, int h_dtype, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * diffattn_read_error — reads and clears the device error word at the start of
  * a workspace used by an earlier call. Synchronises `stream` (the one place the
  * library blocks). *device_code (host pointer) receives the raw code: 0 = none;

@@ -234,6 +234,49 @@ def test_kv_append_argument_validation(lib):
     assert call(k2=_tensor(sb=4 * 64 * 64, sh=64 * 64, sn=64)) == da.ERR_INVALID_ARG  # K1/K2 strides differ
 
 
+def test_fused_gemm_argument_validation(lib):
+    """The layer's GEMMs with residual and SwiGLU epilogues reject bad arguments before any launch."""
+    vp = ctypes.c_void_p
+    res = lambda **kw: lib.diffattn_gemm_residual(
+        vp(kw.get("A", 0x1000)), vp(0x2000), vp(kw.get("R", 0x3000)), vp(0x4000), vp(kw.get("C16", None)),
+        vp(kw.get("gain", None)), None, kw.get("M", 128), kw.get("N", 256), 64, 64, 256, kw.get("ldr", 256), 256,
+        kw.get("ldc16", 256), kw.get("ab", da.F16), kw.get("rd", da.F32), kw.get("c16d", da.F16), vp(0x8000),
+        kw.get("wsb", 256), None)
+    assert res(N=128) == da.ERR_INVALID_ARG          # N a multiple of 256
+    assert res(ab=da.F32) == da.ERR_INVALID_ARG      # operands are 16-bit
+    assert res(R=0) == da.ERR_INVALID_ARG
+    assert res(R=0x3004) == da.ERR_INVALID_ARG       # 16-byte alignment
+    assert res(ldr=200) == da.ERR_INVALID_ARG        # row stride below N
+    assert res(gain=0x5000) == da.ERR_INVALID_ARG    # a gain without the copy
+    assert res(C16=0x6000, c16d=da.F32) == da.ERR_INVALID_ARG
+    assert res(C16=0x6000, ldc16=12) == da.ERR_INVALID_ARG
+    assert res(M=0) == da.ERR_INVALID_ARG
+    assert res(wsb=16) == da.ERR_WORKSPACE
+    glu = lambda **kw: lib.diffattn_gemm_swiglu(
+        vp(0x1000), vp(0x2000), vp(0x3000), vp(kw.get("sq", None)), kw.get("nsq", 8), kw.get("cnt", 512.0),
+        kw.get("eps", 1e-5), 128, kw.get("F", 256), 64, 64, 512, 256, kw.get("ab", da.BF16), kw.get("hd", da.BF16),
+        vp(0x8000), 256, None)
+    assert glu(F=192) == da.ERR_INVALID_ARG          # F a multiple of 128
+    assert glu(hd=da.F32) == da.ERR_INVALID_ARG      # H is 16-bit
+    assert glu(sq=0x5000, nsq=0) == da.ERR_INVALID_ARG
+    assert glu(sq=0x5000, cnt=0.0) == da.ERR_INVALID_ARG
+    assert glu(sq=0x5000, eps=float("nan")) == da.ERR_INVALID_ARG
+
+
+def test_interleave_gate_up_layout():
+    """Columns 256t..256t+127 of the interleaved weight are gate columns 128t.., the next 128 up's."""
+    K, F = 4, 384
+    wg = torch.arange(K * F, dtype=torch.float32).view(K, F)
+    wu = -wg - 1
+    w = da.interleave_gate_up(wg, wu)
+    assert w.shape == (K, 2 * F)
+    for t in range(F // 128):
+        assert torch.equal(w[:, 256 * t: 256 * t + 128], wg[:, 128 * t: 128 * t + 128])
+        assert torch.equal(w[:, 256 * t + 128: 256 * t + 256], wu[:, 128 * t: 128 * t + 128])
+    with pytest.raises(ValueError):
+        da.interleave_gate_up(wg[:, :100], wu[:, :100])
+
+
 def test_layer_elementwise_argument_validation(lib):
     vp = ctypes.c_void_p
     norm = lambda **kw: lib.diffattn_add_rmsnorm(

@@ -82,28 +82,32 @@ def test_swiglu_saturates_cleanly():
 
 
 # ------------------------------------------------------------------- layer
-def _layer(w, t, op_dtype=torch.float16):
+def _layer(w, t, op_dtype=torch.float16, fused_qkv=True):
     """Runs the layer with every weight as op_dtype. fp16 copies of the bf16 weights are exact
     above 2^-14 in magnitude; the smaller values (about 0.3%) move by at most 2^-25, and the
     oracle sees the bf16 values."""
     lam, lam_init = _lam(w)
     dev = {k: (v.cuda().to(op_dtype) if k.startswith("w_") else v.cuda()) for k, v in t.items()}
     ws = da.workspace(256)
-    wgu = torch.cat([dev["w_gate"], dev["w_up"]], dim=1).contiguous()
+    wgu = da.interleave_gate_up(dev["w_gate"], dev["w_up"])
+    wqkv = torch.cat([dev["w_q"], dev["w_k"], dev["w_v"]], dim=1).contiguous() if fused_qkv else None
     out = da.layer_fwd(dev["x"], dev["w_q"], dev["w_k"], dev["w_v"], dev["w_o"], wgu, dev["w_down"], w.H, lam,
-                       lam_init, w.eps, norm1_weight=dev.get("norm1_w"), norm2_weight=dev.get("norm2_w"), ws=ws)
+                       lam_init, w.eps, norm1_weight=dev.get("norm1_w"), norm2_weight=dev.get("norm2_w"), ws=ws,
+                       w_qkv=wqkv)
     torch.cuda.synchronize()
     assert da.read_error(ws) == 0
     assert out.dtype == torch.float32 and out.shape == t["x"].shape
     return out, lam, lam_init
 
 
-@pytest.mark.parametrize("norm_weights", [False, True])
-def test_layer_small_all_elements(norm_weights):
-    """X [1, 256, 512], h=2, d=128, Dv=256, d_ff=1536: every output element."""
+@pytest.mark.parametrize("norm_weights,fused_qkv", [(False, True), (True, True), (False, False)])
+def test_layer_small_all_elements(norm_weights, fused_qkv):
+    """X [1, 256, 512], h=2, d=128, Dv=256, d_ff=1536: every output element, with and without
+    RMSNorm gains (norm2's folded into the W_O epilogue's operand copy) and with one or three
+    projection GEMMs."""
     w = gi.WORKLOADS["layer_small_bf16"]
     t = gi.layer_inputs(w, norm_weights=norm_weights)
-    out, lam, lam_init = _layer(w, t)
+    out, lam, lam_init = _layer(w, t, fused_qkv=fused_qkv)
     ref = orc.layer_fwd(t["x"], t["w_q"], t["w_k"], t["w_v"], t["w_o"], t["w_gate"], t["w_up"], t["w_down"], w.H,
                         lam, lam_init, w.eps, t.get("norm1_w"), t.get("norm2_w"))
     ma, rr = errors(out, ref)

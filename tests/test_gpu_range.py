@@ -110,7 +110,7 @@ def test_layer_large_activations():
     t["x"] = _with_outliers(t["x"], 300.0)
     lam, lam_init = _lam(w)
     dev = {k: (v.cuda().half() if k.startswith("w_") else v.cuda()) for k, v in t.items()}
-    wgu = torch.cat([dev["w_gate"], dev["w_up"]], dim=1).contiguous()
+    wgu = da.interleave_gate_up(dev["w_gate"], dev["w_up"])
     ws = da.workspace(256)
     out = da.layer_fwd(dev["x"], dev["w_q"], dev["w_k"], dev["w_v"], dev["w_o"], wgu, dev["w_down"], w.H, lam,
                        lam_init, w.eps, ws=ws)
