@@ -62,7 +62,8 @@ CSRC = os.path.join(ROOT, "differential_attention_02_gb300", "csrc")
 
 def profiled_traffic(key, files):
     """DRAM bytes per launch recorded from an ncu capture in profiles/traffic.json,
-    or None when the kernel sources have changed since that capture."""
+    or None when the kernel sources (its .cu file and common.cuh) have changed since
+    that capture."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
@@ -417,7 +418,10 @@ def run_backward(args, da, gi, dev, stream, peaks, peak_kind):
             "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "flops_per_step": flops,
             "exec_tflops": exec_flops / (ms * 1e-3) / 1e12,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": tf / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 burst"},
+                         "frac": tf / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 burst",
+                         "traffic_dominant_kernel": {
+                             "kernel": "bwd_dkdv_kernel",
+                             "bytes": profiled_traffic("bwd_dkdv_prefill_B4H16N2048", ["bwd_tcgen05.cu", "common.cuh"])}},
             "gpu_launches_per_step": 4}
 
 
@@ -453,7 +457,7 @@ def run_decode(args, da, gi, dev, stream, peaks, peak_kind):
     dms = statistics.median(a.elapsed_time(b) for a, b in dev_ev)
     kvb = decode_kv_bytes(wd)
     gbs = kvb / (dms * 1e-3) / 1e9
-    per_seq = profiled_traffic("decode_split_per_sequence_H16L8192", ["decode_bf16.cu", "common.cuh", "kernels.h"])
+    per_seq = profiled_traffic("decode_split_per_sequence_H16L8192", ["decode_bf16.cu", "common.cuh"])
     traffic = per_seq * wd.B if (per_seq is not None and wd.H == 16 and wd.N == 8192) else None
     serving = run_serving(args, da, wd, y, lam, lam_init, dev, stream, peaks, kvb)
     return {"workload": f"decode {wd.B} seqs x 1 token, H{wd.H}, L{wd.N}, d{wd.d}, Dv{wd.Dv}, layer {wd.layer}",
@@ -516,12 +520,14 @@ def run_serving(args, da, wd, y, lam, lam_init, dev, stream, peaks, kvb):
     ms8 = time_device(step8, extra_reps(args), max(3, args.warmup), stream)
     assert da.read_error(ws) == 0
     gbs8 = kvb / 2 / (ms8 * 1e-3) / 1e9
+    per_seq8 = profiled_traffic("decode_split_fp8_per_sequence_H16L8192", ["decode_bf16.cu", "common.cuh"])
     res["fp8_cache"] = {
         "workload": "the same serving step with the K1, K2, V pages in fp8 e4m3 (one scale per tensor)",
         "ms_per_step": ms8, "value": gbs8, "unit": "GB/s", "kv_bytes_per_step": kvb // 2,
         "speedup_vs_bf16_cache": ms / ms8,
         "roofline": {"bound": "hbm", "achieved": gbs8, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs8 / peaks["hbm_gbs"]},
+                     "frac": gbs8 / peaks["hbm_gbs"],
+                     "traffic": per_seq8 * B if (per_seq8 is not None and H == 16 and L == 8192) else None},
         "gpu_launches_per_step": 3}
     del q8
     return res
@@ -629,8 +635,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} bf16 burst",
-                     "traffic": profiled_traffic("fwd_bf16_prefill_B4H16N2048",
-                                                 ["fwd_tcgen05.cu", "common.cuh", "kernels.h"]),
+                     "traffic": profiled_traffic("fwd_bf16_prefill_B4H16N2048", ["fwd_tcgen05.cu", "common.cuh"]),
                      "algorithmic_bytes": prefill_bytes(w)},
         "cpu_baseline": cpu,
         "e2e": e2e,

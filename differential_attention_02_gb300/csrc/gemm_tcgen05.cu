@@ -231,34 +231,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                 continue;
             }
             float sq = 0.f;  // mode 1: this row's sum of C^2 over the tile
+            // Mode 1: this row's residual slice of a 64-column pass as raw 16-byte words (16 for
+            // fp32, 8 for 16-bit R), loaded one pass ahead so a load's latency overlaps the
+            // previous pass's work instead of stalling every 32-column chunk.
+            uint4 rcur[16], rnext[16];
+            auto load_resid = [&](int pass, uint4* dst) {
+                if (p.mode != 1 || !row_ok) return;
+                const int col0 = n0 + pass * kOutCols;
+                if (p.r_dtype == 0) {
+                    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const float*>(p.resid) + row * p.ld_r + col0);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) dst[q] = src[q];
+                } else {
+                    const uint4* src =
+                        reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.resid) + row * p.ld_r + col0);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) dst[q] = src[q];
+                }
+            };
+            load_resid(0, rcur);
 #pragma unroll 1
             for (int pass = 0; pass < BN / kOutCols; ++pass) {
+                if (pass + 1 < BN / kOutCols) load_resid(pass + 1, rnext);
                 // The staging boxes of this warp must be free (its previous stores read them).
                 if (lane == 0) tma_store_wait_read();
                 __syncwarp();
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < kOutCols / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(t_row + pass * kOutCols + c * 32, r);
                     const int col0 = n0 + pass * kOutCols + c * 32;  // first of these 32 columns
                     float res[32];
                     if (p.mode == 1) {
-                        // residual row slice, fetched while the TMEM load is in flight
                         if (row_ok) {
                             if (p.r_dtype == 0) {
-                                const float4* src =
-                                    reinterpret_cast<const float4*>(static_cast<const float*>(p.resid) + row * p.ld_r + col0);
 #pragma unroll
                                 for (int q = 0; q < 8; ++q) {
-                                    const float4 v = src[q];
-                                    res[4 * q] = v.x; res[4 * q + 1] = v.y; res[4 * q + 2] = v.z; res[4 * q + 3] = v.w;
+                                    const uint4 v = rcur[c * 8 + q];
+                                    res[4 * q] = __uint_as_float(v.x); res[4 * q + 1] = __uint_as_float(v.y);
+                                    res[4 * q + 2] = __uint_as_float(v.z); res[4 * q + 3] = __uint_as_float(v.w);
                                 }
                             } else {
-                                const uint4* src = reinterpret_cast<const uint4*>(
-                                    static_cast<const uint16_t*>(p.resid) + row * p.ld_r + col0);
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) {
-                                    const uint4 v = src[q];
+                                    const uint4 v = rcur[c * 4 + q];
                                     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
@@ -342,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
                     }
                     tma_store_commit();
                 }
+#pragma unroll
+                for (int q = 0; q < 16; ++q) rcur[q] = rnext[q];
             }
             if (p.mode == 1 && p.row_sq && row_ok) p.row_sq[(int64_t)row * tiles_n + n0 / BN] = sq;
         }
