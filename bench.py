@@ -290,8 +290,36 @@ def run_e2e(args, da, w, host, lv, out_shape, dev, stream, world):
     e2e_ms = e0.elapsed_time(e1) / args.steps
     h2d = sum(pin[k].numel() * pin[k].element_size() for k in NAMES)
     d2h = out_host.numel() * out_host.element_size()
+    # The copies alone, on one stream, with the same pinned buffers: what the host link allows.
+    dbuf = {k: torch.empty_like(pin[k], device=dev) for k in NAMES}
+    dout = torch.empty(out_shape, dtype=torch.bfloat16, device=dev)
+
+    def copies(h2d_on, d2h_on):
+        for _ in range(max(3, args.steps)):
+            if h2d_on:
+                for k in NAMES:
+                    dbuf[k].copy_(pin[k], non_blocking=True)
+            if d2h_on:
+                out_host.copy_(dout, non_blocking=True)
+
+    timing = {}
+    for name, a, b in (("h2d", True, False), ("d2h", False, True), ("both", True, True)):
+        copies(a, b)  # warm-up
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        copies(a, b)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        timing[name] = c0.elapsed_time(c1) / max(3, args.steps)
     return {"value": world * prefill_def_flops(w) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies_alone": {
+                "note": "the step's host<->device copies alone, one stream, same pinned buffers",
+                "h2d_ms": timing["h2d"], "h2d_gbs": h2d / (timing["h2d"] * 1e-3) / 1e9,
+                "d2h_ms": timing["d2h"], "d2h_gbs": d2h / (timing["d2h"] * 1e-3) / 1e9,
+                "h2d_then_d2h_ms": timing["both"],
+                "e2e_over_copies": e2e_ms / timing["both"]}}
 
 
 def time_device(fn, steps, warmup, stream, flush=None):

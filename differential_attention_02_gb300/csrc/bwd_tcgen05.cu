@@ -97,6 +97,7 @@ struct Bars {
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block fits the 256 bytes past kOffBar");
 }  // namespace dq
 
 template <bool F16>
@@ -368,6 +369,7 @@ struct Bars {
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block fits the 256 bytes past kOffBar");
 }  // namespace dkdv
 
 // D (+)= A[smem, K-major] * B[smem, MN-major]: one K=16 step advances 32 bytes in A's

@@ -50,7 +50,8 @@ struct PairCfg {
     static constexpr int kOffV = kOffK + kKStages * kKBytes;
     static constexpr int kOffStages = kOffK;
     static constexpr int kOffBar = kOffV + kVStages * kVBytes;
-    static constexpr size_t kSmem = 1024 + (size_t)kOffBar + 256;
+    static constexpr int kBarBytes = 320;             // PairBars, rounded up
+    static constexpr size_t kSmem = 1024 + (size_t)kOffBar + kBarBytes;
     static constexpr int kHalf = DV / 2;              // output columns finished by each CTA
     static constexpr int kXStride = kHalf + 4;        // padded row of the exchange buffer (floats)
     static constexpr int kOffX = kOffStages;          // exchange buffer reuses the K/V rings
@@ -83,6 +84,8 @@ struct PairBars {
     uint32_t tmem_base;
     int abort;
 };
+
+static_assert(sizeof(PairBars) <= PairCfg<128, 256>::kBarBytes, "barrier block");
 
 template <int D, bool F16>
 __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t q_desc, uint64_t k_desc) {
@@ -179,8 +182,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(tm_k);
             tma_prefetch_desc(&p.tm_v);
             mbar_arrive_expect_tx(&bars->q_full, C::kQBytes);
-#pragma unroll
             index_ok(q0 < p.N && h < p.H && b < p.B, p.err, 0x93);
+#pragma unroll
             for (int x = 0; x < D / 64; ++x) tma_load_4d(qs + x * C::kBoxBytes, tm_q, &bars->q_full, x * 64, q0, h, b);
             // Issue order K(j), V(j): K tiles run ahead as soon as S frees them, V tiles
             // follow the PV products.

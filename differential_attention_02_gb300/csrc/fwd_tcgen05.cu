@@ -99,6 +99,7 @@ struct Bars {
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= FwdCfg<64, 128>::kBarBytes, "barrier block fits its reserve");
 
 // The MMA issuer shares its SM sub-partition with two softmax warps, so each
 // MMA costs as few instructions as possible: descriptors are built once and

@@ -55,6 +55,7 @@ struct GemmBars {
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(GemmBars) <= 256, "barrier block fits the 256 bytes past kOffBar");
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
