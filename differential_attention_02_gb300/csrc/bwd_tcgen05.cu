@@ -169,10 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             }
         } else if (warp == kWarpMma) {
             const bool lead = elect_one();
-            const uint64_t dq1 = sdesc_sw128(smem_u32(smem + kOffQ1), 16, 1024);
-            const uint64_t dq2 = sdesc_sw128(smem_u32(smem + kOffQ2), 16, 1024);
-            const uint64_t ddo = sdesc_sw128(smem_u32(smem + kOffO), 16, 1024);
-            const uint64_t dk0 = sdesc_sw128(smem_u32(stages), 16, 1024);            // K-major K / V tiles
+            // K-major descriptors differ only in the start address: one base plus offsets.
+            const uint64_t dq1 = sdesc_sw128(smem_u32(smem), 16, 1024);
+            const uint64_t dq2 = dq1 + (kOffQ2 >> 4), ddo = dq1 + (kOffO >> 4);
+            const uint64_t dk0 = dq1 + (kOffStages >> 4);                            // K-major K / V tiles
             const uint64_t dkn0 = sdesc_sw128(smem_u32(stages), BM * 128, 1024);      // K as an MN-major operand
             constexpr uint64_t kStep = kStageBytes >> 4, kK2 = kKBytes >> 4, kV = (2 * kKBytes) >> 4;
             constexpr uint32_t id_s = idesc_kind_f16(BM, BM, 0, 0, F16);    // S, dA: 128 x 128
@@ -256,12 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         Dg = g ? st.w : st.z;
     }
     const int lim = p.causal ? min(qrow + 1, p.N) : p.N;  // visible keys: key < lim
+    const float ca = g ? -lam : 1.0f;                     // dA's factor in dP_g
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
         if (!(ok = mbar_wait_warp(&bars->s_full[g], j & 1, abort_flag, p.err, 0xD0 + g))) break;
         tc_fence_after();
         const int kbase = j * BM;
-        const bool need_mask = kbase + BM > lim || kbase + BM > p.N;
+        // Masks only where some row of the tile may not see every key of the tile (the
+        // causal diagonal, or keys past N): a warp-uniform test.
+        const bool need_mask = (p.causal && kbase + BM > q0 + 1) || kbase + BM > p.N;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             uint32_t s[64], a[64];
@@ -276,19 +279,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 if (lane == 0) mbar_arrive(&bars->da_free);
             }
             uint32_t pk[32];
+            // dS_g = P_g (c dA - D_g) with c = 1 (map 1) or -lambda (map 2)
+            auto elementwise = [&](auto masked) {
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                float ds[2];
+                for (int i = 0; i < 64; i += 2) {
+                    float ds[2];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int key = kbase + hf * 64 + i + k;
-                    float pr = fast_exp2(fmaf(__uint_as_float(s[i + k]), sl2, -L));
-                    if (need_mask && key >= lim) pr = 0.f;
-                    const float da = __uint_as_float(a[i + k]);
-                    ds[k] = g ? pr * fmaf(-lam, da, -Dg) : pr * (da - Dg);
+                    for (int k = 0; k < 2; ++k) {
+                        float pr = fast_exp2(fmaf(__uint_as_float(s[i + k]), sl2, -L));
+                        if constexpr (decltype(masked)::value) {
+                            if (kbase + hf * 64 + i + k >= lim) pr = 0.f;
+                        }
+                        ds[k] = pr * fmaf(ca, __uint_as_float(a[i + k]), -Dg);
+                    }
+                    pk[i / 2] = pack_p<F16>(ds[0], ds[1]);
                 }
-                pk[i / 2] = pack_p<F16>(ds[0], ds[1]);
-            }
+            };
+            if (need_mask) elementwise(std::true_type{});
+            else elementwise(std::false_type{});
             tmem_st32(tS + hf * 32, pk);
         }
         tmem_st_wait();
