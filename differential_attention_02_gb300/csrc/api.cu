@@ -404,7 +404,8 @@ diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
             !encode_4d(&f.tm_q2, q2, d, N, H, B, 64, kFwdBM, sw, tdt) ||
             !encode_4d(&f.tm_k1, k1, d, N, H, B, 64, kFwdBN, sw, tdt) ||
             !encode_4d(&f.tm_k2, k2, d, N, H, B, 64, kFwdBN, sw, tdt) ||
-            !encode_4d(&f.tm_v, v, Dv, N, H, B, 64, kFwdBN, sw, tdt))
+            !encode_4d(&f.tm_v, v, Dv, N, H, B, 64, kFwdBN, sw, tdt) ||
+            !encode_out_3d(&f.tm_dy, const_cast<void*>(dy), H * Dv, N, B, 2, kFwdBM))
             return DIFFATTN_ERR_INVALID_ARG;
         f.in_f16 = dt == 2;
         f.norm_w = norm_weight;

@@ -78,7 +78,7 @@ struct FwdCfg {
     // is idle once the last MMA has completed.
     static constexpr int kOffEpi = kOffQ1;
     static_assert(8 * BM * 4 <= kQBytes, "epilogue buffer fits in the Q1 tile");
-    static_assert(BM * (DV + 1) * 4 <= kKvStages * kStageBytes, "gain-gradient terms fit in the K/V ring");
+    static_assert(BM * DV * 4 <= kStageBytes && BM * DV * 2 <= kStageBytes, "gain-gradient terms and dy fit a stage");
     static constexpr size_t kSmem = 1024 + (size_t)kOffBar + kBarBytes;
     static_assert(kSmem <= 232448, "shared memory budget");
     static constexpr uint32_t kTmemCols = 512;
@@ -96,6 +96,7 @@ struct Bars {
     uint64_t p_full[2];
     uint64_t o_done[2];
     uint64_t drain;
+    uint64_t dy_full;  // backward preparation: this tile's dy rows in shared memory
     uint32_t tmem_base;
     int abort;
 };
@@ -141,7 +142,7 @@ __device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, 
 template <int DV, bool F16>
 __device__ __forceinline__ void prep_epilogue(const FwdParams& p, bool ok, int g, int r, int qrow, int b, int h,
                                               uint32_t lane_base, uint32_t col_o, float l, float m_used, float* xch,
-                                              float* dwbuf) {
+                                              const uint8_t* dybuf, float* dwbuf, float* dlbuf) {
     constexpr int kHalf = DV / 2;
     using T16 = typename std::conditional<F16, __half, __nv_bfloat16>::type;
     const bool live = ok && qrow < p.N;
@@ -152,14 +153,14 @@ __device__ __forceinline__ void prep_epilogue(const FwdParams& p, bool ok, int g
     const float l1 = xch[r], l2 = xch[BM + r], mx1 = xch[2 * BM + r], mx2 = xch[3 * BM + r];
     const float i1 = 1.0f / l1, i2 = 1.0f / l2, lam = p.lambda, cs = 1.0f - p.lambda_init;
     const uint32_t t1 = lane_base + col_o + g * kHalf, t2 = lane_base + col_o + DV + g * kHalf;
-    // This row's slice of dy (kHalf 16-bit values) in fp32.
+    // This row's slice of dy (kHalf 16-bit values) in fp32, from the tile the producer
+    // staged: box g of [128 rows][64 values], 128-byte swizzled (rows past N are zeros).
     float dyv[kHalf];
-    if (live) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T16*>(p.dy) +
-                                                          (((int64_t)b * p.N + qrow) * p.H + h) * DV + g * kHalf);
+    static_assert(kHalf == 64, "one 64-column box per group");
+    if (ok) {
 #pragma unroll
         for (int c = 0; c < kHalf / 8; ++c) {
-            const uint4 v = src[c];
+            const uint4 v = *reinterpret_cast<const uint4*>(dybuf + g * (128 * 128) + sw128_offset(r, c));
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -220,7 +221,10 @@ __device__ __forceinline__ void prep_epilogue(const FwdParams& p, bool ok, int g
     // Pass 3: dO (stored in the operand type), D1/D2 partials, gain-gradient terms.
     float x1 = 0.f, x2 = 0.f, x2e = 0.f;
     T16* dorow = static_cast<T16*>(p.d_o) + (((int64_t)b * p.H + h) * p.N + qrow) * DV + g * kHalf;
-    float* dwrow = dwbuf + r * (DV + 1) + g * kHalf;
+    // [BM][DV] with column c of row r at c ^ (r % 32): row-per-thread writes and
+    // column-per-thread reads both hit 32 distinct banks.
+    float* dwrow = dwbuf + r * DV;
+    const int swz = r & 31;
 #pragma unroll
     for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t a[32], e[32];
@@ -244,7 +248,7 @@ __device__ __forceinline__ void prep_epilogue(const FwdParams& p, bool ok, int g
                 d2[k] = (gg - n * gn) * ir;
                 o1v[k] = o1;
                 o2v[k] = o2;
-                dwrow[c * 32 + i + k] = live ? dyc * n * cs : 0.f;
+                dwrow[(g * kHalf + c * 32 + i + k) ^ swz] = live ? dyc * n * cs : 0.f;
             }
             pk[i / 2] = pack_p<F16>(d2[0], d2[1]);
             // D1, D2 from the rounded dO the gradient products will use, so that
@@ -279,17 +283,28 @@ __device__ __forceinline__ void prep_epilogue(const FwdParams& p, bool ok, int g
         float4* st = reinterpret_cast<float4*>(p.stats + (((int64_t)b * p.H + h) * p.N + qrow) * 4);
         *st = make_float4(mx1 + __log2f(l1), mx2 + __log2f(l2), X1, -lam * X2);
     }
-    if (g == 0) dwbuf[r * (DV + 1) + DV] = live ? -X2e : 0.f;  // this row's dlambda term
+    if (g == 0) dlbuf[r] = live ? -X2e : 0.f;  // this row's dlambda term
     named_bar_sync(1, 256);
-    // Column sums over the CTA's rows, in row order: the gain's gradient and dlambda.
+    // Column sums over the CTA's rows in a fixed order: thread t sums column t % DV over
+    // rows 64 (t / DV) .. +63, then the two halves are added (256 threads, DV = 128).
+    static_assert(2 * DV == 256, "two threads per column");
     const int t = g * BM + r;  // 0..255
-    for (int col = t; col <= DV; col += 256) {
-        float acc = 0.f;
-        for (int row = 0; row < BM; ++row) acc += dwbuf[row * (DV + 1) + col];
-        if (col < DV)
-            p.part_w[(int64_t)blockIdx.x * DV + col] = acc;
-        else
-            p.part_lam[blockIdx.x] = acc;
+    const int col = t % DV, half = t / DV;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int row = half * 64; row < half * 64 + 64; ++row) acc += dwbuf[row * DV + (col ^ (row & 31))];
+    float* hsum = xch;  // the exchange slots are free again
+    named_bar_sync(1, 256);  // every read of the exchange slots above is done
+    if (half == 1) hsum[col] = acc;
+    named_bar_sync(1, 256);
+    if (half == 0) p.part_w[(int64_t)blockIdx.x * DV + col] = acc + hsum[col];
+    // dlambda over the rows: warp 0 (group 0's first warp) adds four rows per lane, then
+    // a fixed butterfly.
+    if (t < 32) {
+        float s4 = ((dlbuf[4 * t] + dlbuf[4 * t + 1]) + dlbuf[4 * t + 2]) + dlbuf[4 * t + 3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s4 += __shfl_xor_sync(0xffffffffu, s4, o);
+        if (t == 0) p.part_lam[blockIdx.x] = s4;
     }
 }
 
@@ -324,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
             mbar_init(&bars->o_done[g], 1);
         }
         mbar_init(&bars->drain, 1);
+        mbar_init(&bars->dy_full, 1);
         bars->abort = 0;
         fence_mbarrier_init();
     }
@@ -378,10 +394,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                         tma_load_4d(st + 2 * C::kKBytes + x * C::kBoxBytes, &p.tm_v, &bars->kv_full[s], x * 64, j * BN,
                                     h, b);
                 }
+                // Backward preparation: this tile's dy rows ([128 rows][DV], boxes of 64 columns)
+                // into the stage the ring frees next, so they land during the last tiles' work
+                // (the epilogue reads them; out-of-range rows read zeros).
+                bool dy_loaded = false;
+                if constexpr (PREP) {
+                    const int s = nkv % kKvStages;
+                    if (j == nkv &&
+                        mbar_wait(&bars->kv_empty[s], ((nkv / kKvStages) & 1) ^ 1, abort_flag, p.err, 0x3e)) {
+                        mbar_arrive_expect_tx(&bars->dy_full, BM * DV * 2);
+#pragma unroll
+                        for (int x = 0; x < DV / 64; ++x)
+                            tma_load_3d(stages + s * C::kStageBytes + x * C::kBoxBytes, &p.tm_dy, &bars->dy_full,
+                                        h * DV + x * 64, q0, b);
+                        dy_loaded = true;
+                    }
+                }
                 // Drain: no copy may still be landing in shared memory when the CTA exits.
                 mbar_wait(&bars->q_full, 0, nullptr, p.err, 0x32);
                 for (int u = max(0, j - kKvStages); u < j; ++u)
                     mbar_wait(&bars->kv_full[u % kKvStages], (u / kKvStages) & 1, nullptr, p.err, 0x33);
+                if (dy_loaded) mbar_wait(&bars->dy_full, 0, nullptr, p.err, 0x3f);
             }
         } else if (warp == kWarpMma) {
             // ------------------------------------------------------------ MMA issuer
@@ -563,8 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         if constexpr (PREP) {
             // The exchange slots take 8 x BM floats of the Q1 tile; the gain-gradient
             // terms [BM][DV + 1] take the idle K/V ring.
-            prep_epilogue<DV, F16>(p, ok, g, r, qrow, b, h, lane_base, C::kColO, l, m_used, epi,
-                                   reinterpret_cast<float*>(smem + C::kOffStages));
+            // dy is in stage nkv % 3 (the producer's last load); the gain-gradient terms take the
+            // next stage and the dlambda terms the idle Q2 tile.
+            const int sdy = nkv % kKvStages;
+            const bool dy_ok = ok && mbar_wait_warp(&bars->dy_full, 0, abort_flag, p.err, 0x47);
+            prep_epilogue<DV, F16>(p, dy_ok, g, r, qrow, b, h, lane_base, C::kColO, l, m_used, epi,
+                                   stages + sdy * C::kStageBytes,
+                                   reinterpret_cast<float*>(stages + ((sdy + 1) % kKvStages) * C::kStageBytes),
+                                   reinterpret_cast<float*>(q2s));
             tc_fence_before();
             named_bar_sync(2, kThreads);
             return;

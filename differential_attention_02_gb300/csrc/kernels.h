@@ -155,6 +155,7 @@ constexpr int kGemmBK = 64;
 struct FwdParams {
     CUtensorMap tm_q1, tm_q2, tm_k1, tm_k2, tm_v;  // 4-D maps over [B, H, N, width]
     CUtensorMap tm_out;                            // 3-D map over the output [B, N, H*Dv], 128-byte boxes
+    CUtensorMap tm_dy;                             // backward preparation: dy [B, N, H*Dv], boxes as tm_out
     void* out;                                     // [B, N, H, Dv]
     int out_bf16, out_f16;                         // output bf16, fp16, or fp32 when both are 0
     int in_f16;                                    // operands fp16 (1) or bf16 (0)
