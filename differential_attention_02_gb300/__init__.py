@@ -26,7 +26,8 @@ EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffat
             "diffattn_decode_paged", "diffattn_kv_append_paged", "diffattn_add_rmsnorm", "diffattn_swiglu",
             "diffattn_bwd", "diffattn_bwd_workspace_size", "diffattn_lambda_bwd", "diffattn_decode_paged_fp8",
             "diffattn_kv_append_paged_fp8", "diffattn_decode_noalloc_read_error",
-            "diffattn_selftest_timeout", "diffattn_gemm_residual", "diffattn_gemm_swiglu")
+            "diffattn_selftest_timeout", "diffattn_gemm_residual", "diffattn_gemm_swiglu", "diffattn_fwd_host",
+            "diffattn_fwd_host_buffer_size")
 
 
 class DiffAttnError(RuntimeError):
@@ -77,6 +78,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_gemm_swiglu.restype = i32
     lib.diffattn_gemm_swiglu.argtypes = [vp, vp, vp, vp, i32, f32, f32, i32, i32, i32, i64, i64, i64, i32, i32, vp, sz,
                                          vp]
+    lib.diffattn_fwd_host.restype = i32
+    lib.diffattn_fwd_host.argtypes = [vp] * 7 + [i32] * 6 + [f32] * 3 + [i32] * 3 + [vp, sz, vp]
+    lib.diffattn_fwd_host_buffer_size.restype = i32
+    lib.diffattn_fwd_host_buffer_size.argtypes = [i32] * 7 + [ctypes.POINTER(sz)]
     lib.diffattn_gemm_workspace_size.restype = i32
     lib.diffattn_gemm_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
     lib.diffattn_decode_noalloc.restype = i32
@@ -554,57 +559,49 @@ def _module_attention(x, w_q, w_k, w_v, n_heads, lam, lam_init, eps, norm_weight
     return att.view(B * N, h * Dv)
 
 
-_side_streams = {}
-
-
-def _streams_for(device):
-    """Three side streams per device (copies in, compute, copies out), created once."""
-    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
-    if key not in _side_streams:
-        _side_streams[key] = tuple(torch.cuda.Stream(device=key) for _ in range(3))
-    return _side_streams[key]
+_host_buffers = {}
 
 
 def diffattn_fwd_host(q1, q2, k1, k2, v, lam, lam_init, eps=1e-5, out_dtype=torch.float32, device="cuda",
-                      stream=None, out_host=None, chunks=None):
-    """End-to-end call from pinned HOST tensors [B,H,N,*]; returns the host output [B,N,H,Dv].
-
-    The batch is processed in `chunks` pieces (default: up to 4) on three streams, so the
-    host-to-device copies of one piece overlap the prefill of another and the copy back of
-    a third. (Two streams for the copies in were measured slower than one.) Device buffers are allocated on the caller's stream (default: the current one),
-    and that stream waits for all three before the call returns, so work enqueued on it
-    afterwards, including reuse of those buffers, is ordered after this call.
-    """
-    caller = torch.cuda.current_stream(device) if stream is None else stream
+                      stream=None, out_host=None, chunks=None, norm_weight=None, causal=True):
+    """End-to-end call from pinned HOST tensors [B,H,N,*] (contiguous); returns the host output
+    [B,N,H,Dv]. One C-ABI call (diffattn_fwd_host): the work in `chunks` pieces (head ranges of
+    one batch entry; default 4), each piece's copies in, prefill and copy back on three library
+    streams, so the copies of one piece overlap the prefill and copies of others. The device staging buffer is allocated
+    once per device and size, and reused; its first 256 bytes are the workspace, whose error word
+    read_error(host_buffer_workspace(...)) reads. `stream` (default: the current one) waits for the
+    last copy back, so synchronising it makes `out_host` valid."""
     names = (q1, q2, k1, k2, v)
+    if any(t.is_cuda or not t.is_contiguous() or t.dtype != q1.dtype for t in names):
+        raise ValueError("q1, q2, k1, k2, v: contiguous host tensors of one dtype")
     B, H, N, d = q1.shape
     Dv = v.shape[-1]
-    n = max(1, min(B, chunks or 4))
-    bounds = [(B * i) // n for i in range(n + 1)]
-    s_in, s_run, s_out = _streams_for(device)
-    with torch.cuda.stream(caller):
-        dev = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in names]
-        out = torch.empty((B, N, H, Dv), dtype=out_dtype, device=device)
-        nbytes = ctypes.c_size_t()
-        _check(load_library().diffattn_fwd_workspace_size(B, H, N, d, Dv, ctypes.byref(nbytes)),
-               "diffattn_fwd_workspace_size")
-        ws = workspace(nbytes.value, device)
+    dev = torch.device(device)
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     if out_host is None:
-        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    for s in (s_in, s_run, s_out):
-        s.wait_stream(caller)
-    for i in range(n):
-        lo, hi = bounds[i], bounds[i + 1]
-        if lo == hi:
-            continue
-        with torch.cuda.stream(s_in):
-            for dst, src in zip(dev, names):
-                dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
-        s_run.wait_stream(s_in)
-        diffattn_fwd(*(t[lo:hi] for t in dev), lam, lam_init, eps, out_dtype=out_dtype, out=out[lo:hi], ws=ws,
-                     stream=s_run)
-        s_out.wait_stream(s_run)
-        with torch.cuda.stream(s_out):
-            out_host[lo:hi].copy_(out[lo:hi], non_blocking=True)
-    caller.wait_stream(s_out)
+        out_host = torch.empty((B, N, H, Dv), dtype=out_dtype, pin_memory=True)
+    if out_host.shape != (B, N, H, Dv) or out_host.dtype != out_dtype or not out_host.is_contiguous():
+        raise ValueError("out_host: contiguous [B, N, H, Dv] of out_dtype")
+    buf = host_buffer_workspace(B, H, N, d, Dv, q1.dtype, out_dtype, dev)
+    st = torch.cuda.current_stream(dev) if stream is None else stream
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    _check(load_library().diffattn_fwd_host(
+        *(ptr(t) for t in names), ptr(out_host), ptr(norm_weight), B, H, N, d, Dv, int(bool(causal)), float(lam),
+        float(lam_init), float(eps), _dtype_code(q1.dtype), _dtype_code(out_dtype), int(chunks or 0), ptr(buf),
+        buf.numel(), _stream_ptr(st)), "diffattn_fwd_host")
     return out_host
+
+
+def host_buffer_workspace(B, H, N, d, Dv, in_dtype, out_dtype, device):
+    """The device staging buffer of diffattn_fwd_host for these sizes (cached per device: one
+    buffer, regrown when a call needs more). Its first 256 bytes are the call's workspace."""
+    n = ctypes.c_size_t()
+    _check(load_library().diffattn_fwd_host_buffer_size(B, H, N, d, Dv, _dtype_code(in_dtype), _dtype_code(out_dtype),
+                                                        ctypes.byref(n)), "diffattn_fwd_host_buffer_size")
+    key = torch.device(device).index
+    buf = _host_buffers.get(key)
+    if buf is None or buf.numel() < n.value:
+        buf = torch.zeros(n.value, dtype=torch.uint8, device=device)
+        _host_buffers[key] = buf
+    return buf

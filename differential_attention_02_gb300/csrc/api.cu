@@ -831,6 +831,148 @@ diffattn_status diffattn_gemm_f16(const void* A, const void* W, void* C, int M, 
     return gemm_16bit(true, A, W, C, M, N, K, lda, ldw, ldc, out_dtype, workspace, workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------------------
+// End-to-end prefill from host buffers: the batch in pieces, each piece's copies
+// in, prefill and copy back on three library streams so that they overlap.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+namespace {
+constexpr int kMaxHostChunks = 16;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_run = nullptr, s_out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in_done[kMaxHostChunks], run_done[kMaxHostChunks];
+};
+std::mutex g_pipe_mu;  // one pipelined call at a time (the streams and events are shared)
+HostPipe g_pipe[64];
+
+// The streams and events of the current device, created on first use.
+HostPipe* host_pipe() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    HostPipe& hp = g_pipe[dev];
+    if (!hp.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.s_run, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.start, ef) != cudaSuccess || cudaEventCreateWithFlags(&hp.done, ef) != cudaSuccess)
+            return nullptr;
+        for (int i = 0; i < kMaxHostChunks; ++i)
+            if (cudaEventCreateWithFlags(&hp.in_done[i], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.run_done[i], ef) != cudaSuccess)
+                return nullptr;
+        hp.ready = true;
+    }
+    return &hp;
+}
+
+// Byte offsets of the pieces of the device buffer: the workspace (error word) first,
+// then Q1, Q2, K1, K2, V ([B, H, N, width] contiguous) and the output [B, N, H, Dv].
+struct HostLayout {
+    size_t in[5], out, total;
+};
+HostLayout host_layout(int B, int H, int N, int d, int Dv, int in_eb, int out_eb) {
+    HostLayout L{};
+    size_t off = round256(kControlBytes);
+    for (int i = 0; i < 5; ++i) {
+        L.in[i] = off;
+        off += round256((size_t)B * H * N * (i == 4 ? Dv : d) * in_eb);
+    }
+    L.out = off;
+    off += round256((size_t)B * N * H * Dv * out_eb);
+    L.total = off;
+    return L;
+}
+int dtype_bytes(int dt) { return dt == DIFFATTN_F32 ? 4 : 2; }
+}  // namespace
+extern "C" {
+
+diffattn_status diffattn_fwd_host_buffer_size(int B, int H, int N, int d, int Dv, int in_dtype, int out_dtype,
+                                              size_t* bytes) {
+    if (!bytes || B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if ((in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16 && in_dtype != DIFFATTN_F16) ||
+        (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16 && out_dtype != DIFFATTN_F16))
+        return DIFFATTN_ERR_INVALID_ARG;
+    *bytes = host_layout(B, H, N, d, Dv, dtype_bytes(in_dtype), dtype_bytes(out_dtype)).total;
+    return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_fwd_host(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
+                                  void* out, const float* norm_weight, int B, int H, int N, int d, int Dv, int causal,
+                                  float lambda, float lambda_init, float eps, int in_dtype, int out_dtype, int chunks,
+                                  void* device_buffer, size_t device_buffer_bytes, void* stream) {
+    if (!q1 || !q2 || !k1 || !k2 || !v || !out || B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1 || chunks < 0 ||
+        chunks > kMaxHostChunks)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if ((in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16 && in_dtype != DIFFATTN_F16) ||
+        (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16 && out_dtype != DIFFATTN_F16))
+        return DIFFATTN_ERR_INVALID_ARG;
+    const int ieb = dtype_bytes(in_dtype), oeb = dtype_bytes(out_dtype);
+    const HostLayout L = host_layout(B, H, N, d, Dv, ieb, oeb);
+    if (device_buffer == nullptr || device_buffer_bytes < L.total || (reinterpret_cast<uintptr_t>(device_buffer) & 255u))
+        return DIFFATTN_ERR_WORKSPACE;
+    if (B == 0 || H == 0 || N == 0) return DIFFATTN_OK;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe* hp = host_pipe();
+    if (!hp) return DIFFATTN_ERR_CUDA;
+    cudaStream_t caller = static_cast<cudaStream_t>(stream);
+    uint8_t* dev = static_cast<uint8_t*>(device_buffer);
+    const void* host_in[5] = {q1, q2, k1, k2, v};
+    // Pieces are head ranges within one batch entry: (b, h0 .. h1). Their inputs are contiguous
+    // in the [B, H, N, *] buffers; each piece's output goes to its own contiguous [N, h1-h0, Dv]
+    // slice of the device output region and back with one pitched copy into [B, N, H, Dv].
+    // Default 4 pieces: smaller ones were measured slower (each pays its tensor-map encodes and
+    // launch, and pitched copies of short rows), so head ranges only split small batches.
+    const int want = chunks > 0 ? chunks : 4;
+    const int per_b = std::max(1, std::min(H, (want + B - 1) / B));  // pieces per batch entry
+    const int hg = (H + per_b - 1) / per_b;                           // heads per piece
+    // Everything is ordered after the caller's earlier work, and the caller's later work after it.
+    if (cudaEventRecord(hp->start, caller) != cudaSuccess || cudaStreamWaitEvent(hp->s_in, hp->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->s_run, hp->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->s_out, hp->start, 0) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    int i = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int h0 = 0; h0 < H; h0 += hg, ++i) {
+            const int h1 = std::min(H, h0 + hg), nh = h1 - h0;
+            // Events are reused after 16 pieces: a stream wait binds to the record current when the
+            // wait is enqueued, so recording the event again later does not affect it.
+            const int ev = i % kMaxHostChunks;
+            const int64_t unit0 = (int64_t)b * H + h0;  // first (b, h) of the piece
+            diffattn_tensor ts[5];
+            for (int t = 0; t < 5; ++t) {
+                const int w = t == 4 ? Dv : d;
+                const size_t per_h = (size_t)N * w * ieb;
+                if (cudaMemcpyAsync(dev + L.in[t] + unit0 * per_h, static_cast<const uint8_t*>(host_in[t]) + unit0 * per_h,
+                                    nh * per_h, cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess)
+                    return DIFFATTN_ERR_CUDA;
+                ts[t] = diffattn_tensor{dev + L.in[t] + unit0 * per_h, (int64_t)H * N * w, (int64_t)N * w, w};
+            }
+            if (cudaEventRecord(hp->in_done[ev], hp->s_in) != cudaSuccess ||
+                cudaStreamWaitEvent(hp->s_run, hp->in_done[ev], 0) != cudaSuccess)
+                return DIFFATTN_ERR_CUDA;
+            uint8_t* dout = dev + L.out + (size_t)unit0 * N * Dv * oeb;  // [N, nh, Dv]
+            const diffattn_status st = diffattn_fwd(ts[0], ts[1], ts[2], ts[3], ts[4], dout, norm_weight, 1, nh, N, d,
+                                                    Dv, causal, lambda, lambda_init, eps, in_dtype, out_dtype, dev,
+                                                    kControlBytes, hp->s_run);
+            if (st != DIFFATTN_OK) return st;
+            const size_t row = (size_t)nh * Dv * oeb;
+            if (cudaEventRecord(hp->run_done[ev], hp->s_run) != cudaSuccess ||
+                cudaStreamWaitEvent(hp->s_out, hp->run_done[ev], 0) != cudaSuccess ||
+                cudaMemcpy2DAsync(static_cast<uint8_t*>(out) + ((size_t)b * N * H + h0) * Dv * oeb,
+                                  (size_t)H * Dv * oeb, dout, row, row, N, cudaMemcpyDeviceToHost,
+                                  hp->s_out) != cudaSuccess)
+                return DIFFATTN_ERR_CUDA;
+        }
+    }
+    // The last copy back follows every prefill, which follows every copy in.
+    if (cudaEventRecord(hp->done, hp->s_out) != cudaSuccess || cudaStreamWaitEvent(caller, hp->done, 0) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    return DIFFATTN_OK;
+}
+
 diffattn_status diffattn_selftest_timeout(void* workspace, size_t workspace_bytes, void* stream) {
     if (workspace == nullptr || workspace_bytes < kControlBytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return DIFFATTN_ERR_WORKSPACE;

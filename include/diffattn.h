@@ -409,6 +409,39 @@ diffattn_status diffattn_add_rmsnorm(const void* x, int x_dtype, const float* z,
 diffattn_status diffattn_swiglu(const void* gate_up, void* h_out, int h_dtype, int M, int H, void* stream);
 
 /*
+ * diffattn_fwd_host — diffattn_fwd end to end from HOST buffers: the work is
+ * split into pieces, each a range of heads of one batch entry (`chunks` asks for
+ * that many pieces, 0 = 4, at most 16; every batch entry gets ceil(chunks / B)
+ * head ranges); each piece's inputs are copied to the device, its prefill runs,
+ * and its output is copied back, on three streams owned by the library, so that
+ * the copies of one piece overlap the prefill and copies of others. One
+ * cudaMemcpyAsync per input tensor piece (contiguous in [B, H, N, *]) and one
+ * pitched cudaMemcpy2DAsync per output piece (a head range of [B, N, H, Dv]).
+ * q1, q2, k1, k2: host [B, H, N, d] contiguous; v: host [B, H, N, Dv]
+ * contiguous; out: host [B, N, H, Dv] contiguous; in_dtype / out_dtype, the
+ * arguments from norm_weight (a DEVICE pointer or NULL) to eps, and the
+ * supported shapes as for diffattn_fwd. Host buffers should be pinned (pageable
+ * memory works, without overlap).
+ * device_buffer: at least diffattn_fwd_host_buffer_size() bytes of device
+ * memory, 256-byte aligned; its first 256 bytes are the workspace (the error
+ * word, zero before the first call: diffattn_read_error(device_buffer, ...)),
+ * the rest holds the device copies. Owned by the caller; one call at a time
+ * per buffer.
+ * Ordering: the call waits for work already enqueued on `stream` and makes
+ * `stream` wait for its last copy back, so work enqueued on `stream` afterwards
+ * (and a stream synchronisation) sees `out` filled. Concurrent calls from
+ * several host threads are serialised (the library's streams are shared).
+ * Errors: DIFFATTN_ERR_INVALID_ARG / _WORKSPACE before anything is enqueued;
+ * those of diffattn_fwd; DIFFATTN_ERR_CUDA if a copy or stream call fails.
+ */
+diffattn_status diffattn_fwd_host(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
+                                  void* out, const float* norm_weight, int B, int H, int N, int d, int Dv, int causal,
+                                  float lambda, float lambda_init, float eps, int in_dtype, int out_dtype, int chunks,
+                                  void* device_buffer, size_t device_buffer_bytes, void* stream);
+diffattn_status diffattn_fwd_host_buffer_size(int B, int H, int N, int d, int Dv, int in_dtype, int out_dtype,
+                                              size_t* bytes);
+
+/*
  * diffattn_gemm_bf16 — C[M, N] = A[M, K] . W[K, N], bf16 operands, fp32
  * accumulation, tcgen05 tensor cores. The module's projections: [Q|K|V] = X W
  * and Y = concat(heads) W_O ("A Simple Principle From Noise-Cancelling

@@ -263,6 +263,27 @@ def test_fused_gemm_argument_validation(lib):
     assert glu(sq=0x5000, eps=float("nan")) == da.ERR_INVALID_ARG
 
 
+def test_host_prefill_argument_validation(lib):
+    """diffattn_fwd_host rejects bad arguments before enqueuing anything; its buffer size is the
+    workspace plus the device copies, each rounded up to 256 bytes."""
+    vp = ctypes.c_void_p
+    n = ctypes.c_size_t()
+    assert lib.diffattn_fwd_host_buffer_size(2, 3, 100, 64, 128, da.BF16, da.BF16, ctypes.byref(n)) == da.OK
+    r = lambda x: (x + 255) // 256 * 256
+    assert n.value == 256 + 4 * r(2 * 3 * 100 * 64 * 2) + r(2 * 3 * 100 * 128 * 2) + r(2 * 100 * 3 * 128 * 2)
+    assert lib.diffattn_fwd_host_buffer_size(2, 3, 100, 64, 128, 7, da.BF16, ctypes.byref(n)) == da.ERR_INVALID_ARG
+    call = lambda **kw: lib.diffattn_fwd_host(
+        vp(kw.get("q1", 0x1000)), vp(0x1000), vp(0x1000), vp(0x1000), vp(0x1000), vp(kw.get("out", 0x2000)), None,
+        2, 3, 100, 64, 128, 1, 0.5, 0.2, 1e-5, da.BF16, da.BF16, kw.get("chunks", 0), vp(kw.get("buf", 0x100000)),
+        kw.get("bytes", 1 << 24), None)
+    assert call(q1=0) == da.ERR_INVALID_ARG
+    assert call(out=0) == da.ERR_INVALID_ARG
+    assert call(chunks=17) == da.ERR_INVALID_ARG
+    assert call(chunks=-1) == da.ERR_INVALID_ARG
+    assert call(bytes=1024) == da.ERR_WORKSPACE
+    assert call(buf=0x100010) == da.ERR_WORKSPACE  # 256-byte alignment
+
+
 def test_interleave_gate_up_layout():
     """Columns 256t..256t+127 of the interleaved weight are gate columns 128t.., the next 128 up's."""
     K, F = 4, 384

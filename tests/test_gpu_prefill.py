@@ -195,17 +195,32 @@ def test_f16_operands(d, Dv, N):
 
 
 def test_host_entry_point_matches_device_call():
-    """diffattn_fwd_host (pinned host buffers, batch pipelined over copy/compute/copy
-    streams, uneven chunks) returns exactly what one device call returns, and meets the
-    oracle."""
+    """diffattn_fwd_host (one C-ABI call: pinned host buffers, the batch pipelined over
+    copy/compute/copy streams, uneven pieces) returns exactly what one device call returns,
+    meets the oracle, and leaves the error word of its staging buffer at zero."""
     w = gi.WORKLOADS["prefill_bf16"]
     host = gi.prefill_inputs(w, B=3, H=2, N=300)
     pin = [host[k].pin_memory() for k in NAMES]
     lam, lam_init = 0.45, 0.47
-    for chunks in (2, 3):
+    for chunks in (None, 1, 2, 3, 6):  # 6: head ranges within each batch entry
         got = da.diffattn_fwd_host(*pin, lam, lam_init, out_dtype=torch.bfloat16, chunks=chunks)
         torch.cuda.synchronize()
         want = da.diffattn_fwd(*(t.cuda() for t in pin), lam, lam_init, out_dtype=torch.bfloat16)
         assert torch.equal(got, want.cpu()), f"chunks={chunks}"
+    buf = da.host_buffer_workspace(3, 2, 300, 64, 128, torch.bfloat16, torch.bfloat16, torch.device("cuda", 0))
+    assert da.read_error(buf) == 0
     ref = orc.diffattn_fwd(*(host[k] for k in NAMES), lam, lam_init)
     assert_bf16_out_parity(got, ref, "host entry point B3 H2 N300")
+
+
+def test_host_entry_point_gain_noncausal_fp32_out():
+    """The host entry point with a gain (device pointer), the non-causal mask and fp32 output,
+    against the device call on the same inputs."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    host = gi.prefill_inputs(w, B=2, H=3, N=200)
+    pin = [host[k].pin_memory() for k in NAMES]
+    gain = torch.linspace(0.5, 1.5, 128, device="cuda")
+    got = da.diffattn_fwd_host(*pin, 0.6, 0.2, out_dtype=torch.float32, chunks=2, norm_weight=gain, causal=False)
+    torch.cuda.synchronize()
+    want = da.diffattn_fwd(*(t.cuda() for t in pin), 0.6, 0.2, 1e-5, gain, out_dtype=torch.float32, causal=False)
+    assert torch.equal(got, want.cpu())
