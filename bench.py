@@ -663,7 +663,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} bf16 burst",
-                     "traffic": profiled_traffic("fwd_bf16_prefill_B4H16N2048", ["fwd_tcgen05.cu", "common.cuh"]),
+                     "kernel": "fwd_persist_kernel<64, 128> (one CTA per SM walking the query tiles)",
+                     "traffic": profiled_traffic("fwd_persist_prefill_B4H16N2048", ["fwd_tcgen05.cu", "common.cuh"]),
                      "algorithmic_bytes": prefill_bytes(w)},
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -37,6 +37,13 @@
 // while the tensor core works for the other map. S_m(j+1) overwrites the TMEM
 // columns PV_m(j) reads P from; tcgen05.mma operations issued by one thread
 // execute in issue order, so the read completes before the overwrite.
+//
+// Two launch forms share these roles. The per-tile kernel (one CTA per query
+// tile) serves long sequences, fp32 output and the backward preparation. The
+// persistent kernel (one CTA per SM walking a list of query tiles) serves
+// 16-bit output of short sequences, where each CTA's start and tail (first
+// loads and scores, epilogue, store, the next CTA's launch) are a large share
+// of a tile's time: it overlaps them with the neighbouring tiles' work.
 #include <math.h>
 
 #include <type_traits>
@@ -128,6 +135,92 @@ __device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, 
         const int kk = half * (BN / 32) + k;
         umma_ts(o_tmem, p_tmem + kk * 8, v_desc + (uint64_t)(kk * 128), idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
+}
+
+// One key tile of map g's online softmax, by the group's four warps (thread =
+// query row = TMEM lane): waits for the scores, masks keys past the causal
+// diagonal or past N, updates the running max (O is rescaled in TMEM only when
+// the max grew by more than the threshold; the stale max is exact because the
+// final division uses the same max), and writes P = exp2(S * scale - max) as
+// 16-bit pairs (lower key in the low half) into the first BN/2 columns of S,
+// row sum in fp32. The first half of the keys is handed to the MMA warp before
+// the second half is exponentiated, so the first half of PV overlaps the rest.
+// `ph` is the parity of this tile's phase of the map's barriers. Returns false
+// if a wait gave up.
+template <int DV, bool F16>
+__device__ __forceinline__ bool softmax_tile(const FwdParams& p, int g, uint64_t* s_full, uint64_t* o_done,
+                                             uint64_t* p_half, uint64_t* p_full, volatile int* abort_flag,
+                                             uint32_t tS, uint32_t tO, int q0, int qrow, int kbase, bool first,
+                                             uint32_t ph, float& m_used, float& l) {
+    const int lane = threadIdx.x & 31;
+    const float sl2 = p.scale_log2;
+    if (!mbar_wait_warp(s_full, ph, abort_flag, p.err, 0x40 + g)) return false;
+    tc_fence_after();
+    uint32_t sr[BN];
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
+    tmem_ld_wait();
+
+    const bool need_mask = (p.causal && kbase + BN - 1 > q0) || (kbase + BN > p.N);
+    if (need_mask) {
+        const int lim = p.causal ? min(qrow + 1, p.N) : p.N;  // visible keys: kbase + i < lim
+#pragma unroll
+        for (int i = 0; i < BN; ++i)
+            if (kbase + i >= lim) sr[i] = __float_as_uint(-INFINITY);
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < BN; i += 8) {
+        mx0 = fmax3(mx0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+        mx2 = fmax3(mx2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+        mx3 = fmax3(mx3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+    }
+    const float m_new = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
+    float alpha = 1.f;
+    bool rescale = false;
+    if (first) {
+        m_used = m_new;
+    } else if (m_new > m_used + kRescaleThreshold) {
+        alpha = fast_exp2(m_used - m_new);
+        m_used = m_new;
+        rescale = true;
+    }
+    // O must hold the previous tile's PV before it is rescaled; S landing already
+    // implies that (MMAs complete in issue order), so this wait returns at once.
+    if (!first && __any_sync(0xffffffffu, rescale)) {
+        if (!mbar_wait_warp(o_done, ph ^ 1u, abort_flag, p.err, 0x42 + g)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+        }
+    }
+    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[BN / 4];
+#pragma unroll
+        for (int i = 0; i < BN / 2; i += 2) {
+            const int k = hf * (BN / 2) + i;
+            const float e0 = fast_exp2(fmaf(__uint_as_float(sr[k]), sl2, -m_used));
+            const float e1 = fast_exp2(fmaf(__uint_as_float(sr[k + 1]), sl2, -m_used));
+            rs[(i >> 1) & 3] += e0 + e1;
+            pk[i / 2] = pack_p<F16>(e0, e1);
+        }
+        tmem_st32(tS + hf * (BN / 4), pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(hf == 0 ? p_half : p_full);
+    }
+    l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+    return true;
 }
 
 // Epilogue of the backward preparation (PREP): instead of storing y, the two
@@ -702,11 +795,414 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Persistent form, 16-bit output. One CTA per SM walks a static list of query
+// tiles (heaviest causal tiles first, dealt to the CTAs round by round in a
+// snake order: c, then G-1-c, ...), with the per-tile kernel's warp roles,
+// shared-memory ring and inner loops. What it saves is the start and the tail
+// of every tile: the next tile's Q tiles and first K/V stages load during the
+// current tile's last key tiles, its first score tiles are computed as soon as
+// the current tile's last PV products have consumed P (so they are ready when
+// the epilogue ends), the output tile's store drains while the next tile runs,
+// and there is no CTA launch, barrier setup or TMEM allocation between tiles.
+//
+// The epilogue stages the output tile in the ring stage that held the tile's
+// last (K1, K2, V) tiles. The producer, before it refills that stage, issues
+// the tile's TMA store from it and waits until the store has read it.
+constexpr int kPStages = 3;
+// Dispatch: the persistent form runs when a query tile has at most this many key
+// tiles on average (measured on B*H*N = 2^17 rows: 14%, 9% and 7% faster than the
+// per-tile kernel at N = 512, 1024, 2048 causal, even at 4096, 5% slower at 8192).
+constexpr double kPersistMaxMeanKv = 12.0;
+
+template <int D, int DV>
+struct PersistCfg {
+    static constexpr int kQBytes = BM * D * 2;
+    static constexpr int kKBytes = BN * D * 2;
+    static constexpr int kVBytes = BN * DV * 2;
+    static constexpr int kBoxBytes = 128 * 128;
+    static constexpr int kStageBytes = 2 * kKBytes + kVBytes;
+    static constexpr int kOffQ1 = 0;
+    static constexpr int kOffQ2 = kQBytes;
+    static constexpr int kOffStages = 2 * kQBytes;
+    static constexpr int kOffX = kOffStages + kPStages * kStageBytes;  // [2][BM] floats
+    static constexpr int kOffBar = kOffX + 2 * BM * 4;
+    static constexpr int kBarBytes = 256;
+    static constexpr size_t kSmem = 1024 + (size_t)kOffBar + kBarBytes;
+    static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(BM * DV * 2 <= kStageBytes, "a 16-bit output tile fits a stage");
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0;
+    static constexpr uint32_t kColO = 2 * BN;
+    static_assert(2 * BN + 2 * DV <= 512, "TMEM budget");
+};
+
+struct PersistBars {
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[kPStages], kv_empty[kPStages];
+    uint64_t out_full[kPStages];  // a query tile's output is staged in this stage
+    uint64_t s_full[2], p_half[2], p_full[2], o_done[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(PersistBars) <= PersistCfg<64, 128>::kBarBytes, "barrier block fits its reserve");
+
+struct QTile {
+    int q0, b, h, nkv;
+};
+
+template <int D, int DV, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) fwd_persist_kernel(const __grid_constant__ FwdParams p) {
+    using C = PersistCfg<D, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PersistBars* bars = reinterpret_cast<PersistBars*>(smem + C::kOffBar);
+    float* xch = reinterpret_cast<float*>(smem + C::kOffX);
+    volatile int* abort_flag = &bars->abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = (p.N + BM - 1) / BM;
+    const int BH = p.B * p.H;
+    const int total = n_tiles * BH;
+    const int G = (int)gridDim.x, cta = (int)blockIdx.x;
+    // k-th query tile of this CTA, or -1.
+    auto tile_at = [&](int k) -> int {
+        const int i = k * G + ((k & 1) ? (G - 1 - cta) : cta);
+        return i < total ? i : -1;
+    };
+    auto decode = [&](int i) -> QTile {
+        const int qt = n_tiles - 1 - i / BH;
+        const int bh = i % BH;
+        return QTile{qt * BM, bh / p.H, bh % p.H, p.causal ? min(qt + 1, n_tiles) : n_tiles};
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->out_full[s], 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&bars->s_full[g], 1);
+            mbar_init(&bars->p_half[g], 4);  // one arrival per softmax warp
+            mbar_init(&bars->p_full[g], 4);
+            mbar_init(&bars->o_done[g], 1);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(&bars->tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    uint8_t* q1s = smem + C::kOffQ1;
+    uint8_t* q2s = smem + C::kOffQ2;
+    uint8_t* stages = smem + C::kOffStages;
+
+    if (warp >= 8) {
+        setmaxnreg_dec<kRegsOther>();
+        if (warp == kWarpProducer) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                tma_prefetch_desc(&p.tm_q1);
+                tma_prefetch_desc(&p.tm_q2);
+                tma_prefetch_desc(&p.tm_k1);
+                tma_prefetch_desc(&p.tm_k2);
+                tma_prefetch_desc(&p.tm_v);
+                tma_prefetch_desc(&p.tm_out);
+                int it = 0, nq = 0;                 // stages filled, Q tiles loaded
+                int pend[kPStages];                 // query tile whose output is staged in stage s, or -1
+                for (int s = 0; s < kPStages; ++s) pend[s] = -1;
+                uint32_t oph = 0;                   // parity of each stage's next out_full phase
+                bool go = true;
+                // Writes the output tile staged in stage s (if any) and waits until the
+                // store has read it, so that the stage can be refilled.
+                auto flush = [&](int s) -> bool {
+                    if (pend[s] < 0) return true;
+                    const QTile t = decode(pend[s]);
+                    pend[s] = -1;
+                    if (!mbar_wait(&bars->out_full[s], (oph >> s) & 1u, abort_flag, p.err, 0x78)) return false;
+                    oph ^= 1u << s;
+                    if (!*abort_flag) {
+                        index_ok(t.q0 < p.N, p.err, 0x98);
+                        for (int x = 0; x < DV / 64; ++x)
+                            tma_store_3d(&p.tm_out, stages + s * C::kStageBytes + x * (BM * 128), t.h * DV + x * 64,
+                                         t.q0, t.b);
+                        tma_store_commit();
+                    }
+                    tma_store_wait_read();
+                    return true;
+                };
+                for (int k = 0; go; ++k) {
+                    const int ti = tile_at(k);
+                    if (ti < 0) break;
+                    const QTile t = decode(ti);
+                    // Q of tile k replaces Q of tile k-1 once its last score tiles are done.
+                    if (k > 0 && !(go = mbar_wait(&bars->q_empty, (k - 1) & 1, abort_flag, p.err, 0x70))) break;
+                    mbar_arrive_expect_tx(&bars->q_full, 2 * C::kQBytes);
+                    index_ok(t.q0 < p.N && t.h < p.H && t.b < p.B, p.err, 0x96);
+#pragma unroll
+                    for (int x = 0; x < D / 64; ++x) {
+                        tma_load_4d(q1s + x * C::kBoxBytes, &p.tm_q1, &bars->q_full, x * 64, t.q0, t.h, t.b);
+                        tma_load_4d(q2s + x * C::kBoxBytes, &p.tm_q2, &bars->q_full, x * 64, t.q0, t.h, t.b);
+                    }
+                    nq = k + 1;
+                    for (int j = 0; j < t.nkv; ++j, ++it) {
+                        const int s = it % kPStages;
+                        if (!(go = mbar_wait(&bars->kv_empty[s], ((it / kPStages) & 1) ^ 1, abort_flag, p.err, 0x71)))
+                            break;
+                        if (!(go = flush(s))) break;
+                        uint8_t* st = stages + s * C::kStageBytes;
+                        mbar_arrive_expect_tx(&bars->kv_full[s], C::kStageBytes);
+                        index_ok(j * BN < p.N, p.err, 0x97);
+#pragma unroll
+                        for (int x = 0; x < D / 64; ++x) {
+                            tma_load_4d(st + x * C::kBoxBytes, &p.tm_k1, &bars->kv_full[s], x * 64, j * BN, t.h, t.b);
+                            tma_load_4d(st + C::kKBytes + x * C::kBoxBytes, &p.tm_k2, &bars->kv_full[s], x * 64,
+                                        j * BN, t.h, t.b);
+                        }
+#pragma unroll
+                        for (int x = 0; x < DV / 64; ++x)
+                            tma_load_4d(st + 2 * C::kKBytes + x * C::kBoxBytes, &p.tm_v, &bars->kv_full[s], x * 64,
+                                        j * BN, t.h, t.b);
+                        if (j + 1 == t.nkv) pend[s] = ti;  // this stage will hold the tile's output
+                    }
+                }
+                // The last tiles' outputs, in the order the tiles ended.
+                for (int u = 0; u < kPStages; ++u)
+                    if (go) go = flush((it + u) % kPStages);
+                // Drain: no copy may still be landing in shared memory when the CTA exits.
+                if (nq > 0) mbar_wait(&bars->q_full, (nq - 1) & 1, nullptr, p.err, 0x73);
+                for (int u = max(0, it - kPStages); u < it; ++u)
+                    mbar_wait(&bars->kv_full[u % kPStages], (u / kPStages) & 1, nullptr, p.err, 0x73);
+            }
+        } else if (warp == kWarpMma) {
+            // ------------------------------------------------------------ MMA issuer
+            const uint32_t tS[2] = {tmem + C::kColS, tmem + C::kColS + BN};
+            const uint32_t tO[2] = {tmem + C::kColO, tmem + C::kColO + DV};
+            const uint64_t dq[2] = {sdesc_sw128(smem_u32(q1s), 16, 1024), sdesc_sw128(smem_u32(q2s), 16, 1024)};
+            const uint64_t dk0 = sdesc_sw128(smem_u32(stages), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(stages) + 2 * C::kKBytes, BN * 128, 1024);
+            constexpr uint64_t kStageStep = C::kStageBytes >> 4, kK2Step = C::kKBytes >> 4;
+            uint32_t J = 0;  // key tiles done over all query tiles (= ring stages consumed)
+            int k = 0, ti = tile_at(0);
+            bool ok = true;
+            if (ti >= 0) {
+                // Score tiles of the first query tile's first key tile.
+                ok = mbar_wait_warp(&bars->q_full, 0, abort_flag, p.err, 0x74) &&
+                     mbar_wait_warp(&bars->kv_full[0], 0, abort_flag, p.err, 0x75);
+                if (ok) {
+                    tc_fence_after();
+                    if (elect_one()) {
+                        issue_qk<D, F16>(tS[0], dq[0], dk0);
+                        umma_commit(&bars->s_full[0]);
+                        issue_qk<D, F16>(tS[1], dq[1], dk0 + kK2Step);
+                        umma_commit(&bars->s_full[1]);
+                        if (decode(ti).nkv == 1) umma_commit(&bars->q_empty);
+                    }
+                    __syncwarp();
+                }
+            }
+            while (ok && ti >= 0) {
+                const int nkv = decode(ti).nkv;
+                const int tn = tile_at(k + 1);
+                const int nkv_next = tn >= 0 ? decode(tn).nkv : 0;
+                for (int j = 0; ok && j < nkv; ++j, ++J) {
+                    const bool last = j + 1 == nkv;
+                    const bool more = !last || tn >= 0;  // a next score tile exists
+                    const bool new_q = last && tn >= 0;  // ... and it belongs to the next query tile
+                    // The next score tile is the last one of its query tile: its completion frees Q.
+                    const bool last_s = last ? nkv_next == 1 : j + 2 == nkv;
+                    const int s = (int)(J % kPStages), s1 = (int)((J + 1) % kPStages);
+                    const uint64_t dv = dv0 + s * kStageStep, dk1 = dk0 + s1 * kStageStep;
+                    for (int m = 0; m < 2; ++m) {
+                        if (!mbar_wait_warp(&bars->p_half[m], J & 1, abort_flag, p.err, 0x77 + m)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (elect_one()) issue_pv_half<DV, F16>(tO[m], tS[m], dv, 0, j > 0 ? 1u : 0u);
+                        __syncwarp();
+                        // The next Q and K/V tiles are checked while the softmax still works on
+                        // the second half of P, off the path from p_full to the MMAs.
+                        if (m == 0 && more) {
+                            if (new_q && !mbar_wait_warp(&bars->q_full, (k + 1) & 1, abort_flag, p.err, 0x79)) {
+                                ok = false;
+                                break;
+                            }
+                            if (!mbar_wait_warp(&bars->kv_full[s1], ((J + 1) / kPStages) & 1, abort_flag, p.err,
+                                                0x7a)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!mbar_wait_warp(&bars->p_full[m], J & 1, abort_flag, p.err, 0x7b + m)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (elect_one()) {
+                            issue_pv_half<DV, F16>(tO[m], tS[m], dv, 1, 1u);
+                            umma_commit(&bars->o_done[m]);
+                            if (m == 1) umma_commit(&bars->kv_empty[s]);
+                            if (more) {
+                                issue_qk<D, F16>(tS[m], dq[m], dk1 + m * kK2Step);
+                                umma_commit(&bars->s_full[m]);
+                                if (m == 1 && last_s) umma_commit(&bars->q_empty);
+                            }
+                        }
+                        __syncwarp();
+                    }
+                }
+                ++k;
+                ti = tn;
+            }
+            // Every MMA issued (also before an abort) must finish before TMEM is freed.
+            if (elect_one()) umma_commit(&bars->drain);
+            __syncwarp();
+            mbar_wait(&bars->drain, 0, nullptr, p.err, 0x7d);
+        }
+        tc_fence_before();
+        named_bar_sync(2, kThreads);
+        if (warp == kWarpMma) {
+            tc_fence_after();
+            tmem_dealloc(tmem, C::kTmemCols);
+        }
+    } else {
+        setmaxnreg_inc<kRegsSoftmax>();
+        // ------------------------------------------------------------ softmax (map g) and epilogue
+        const int g = warp >> 2;
+        const int lg = warp & 3;
+        const int r = lg * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
+        const uint32_t tS = lane_base + C::kColS + g * BN;
+        const uint32_t tO = lane_base + C::kColO + g * DV;
+        constexpr int kHalf = DV / 2;  // output columns handled by this group
+        const bool f16 = p.out_f16 != 0;
+        uint32_t J = 0;
+        bool ok = true;
+        // Every softmax thread walks the same tile list and takes every named barrier,
+        // also after a failed wait (then without waiting or computing).
+        for (int k = 0;; ++k) {
+            const int ti = tile_at(k);
+            if (ti < 0) break;
+            const QTile t = decode(ti);
+            const int q0 = t.q0, nkv = t.nkv;
+            const int qrow = q0 + r;
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; ok && j < nkv; ++j, ++J)
+                ok = softmax_tile<DV, F16>(p, g, &bars->s_full[g], &bars->o_done[g], &bars->p_half[g],
+                                           &bars->p_full[g], abort_flag, tS, tO, q0, qrow, j * BN, j == 0, J & 1u,
+                                           m_used, l);
+            // Epilogue: O1/l1 - lambda O2/l2, row RMSNorm, (1 - lambda_init), norm weight.
+            if (ok) {
+                ok = mbar_wait_warp(&bars->o_done[0], (J - 1) & 1u, abort_flag, p.err, 0x44) &&
+                     mbar_wait_warp(&bars->o_done[1], (J - 1) & 1u, abort_flag, p.err, 0x45);
+            }
+            tc_fence_after();
+            // Exchange slot X[g][r] is written by group g and read by the other group,
+            // which then reuses it for its own sum of squares.
+            const float own = (g == 0) ? 1.0f / l : p.lambda / l;
+            xch[g * BM + r] = own;
+            named_bar_sync(1, 256);
+            const float par = xch[(1 - g) * BM + r];
+            const float inv1 = g == 0 ? own : par, inv2 = g == 0 ? par : own;
+            // Two passes over O (sum of squares, then the scaled output), so that no
+            // output row is held in registers across the exchange.
+            float ss = 0.f;
+            if (ok) {
+#pragma unroll
+                for (int c = 0; c < kHalf / 32; ++c) {
+                    uint32_t o1[32], o2[32];
+                    tmem_ld32(lane_base + C::kColO + g * kHalf + c * 32, o1);
+                    tmem_ld32(lane_base + C::kColO + DV + g * kHalf + c * 32, o2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float x = __uint_as_float(o1[i]) * inv1 - __uint_as_float(o2[i]) * inv2;
+                        ss = fmaf(x, x, ss);
+                    }
+                }
+            }
+            xch[(1 - g) * BM + r] = ss;
+            named_bar_sync(1, 256);
+            // Stage this group's DV/2 columns as 128-byte-swizzled boxes of 128 rows in the
+            // stage that held the tile's last K/V tiles (idle since the last PV); the
+            // producer stores the tile from there.
+            uint8_t* stage = stages + (int)((J - 1) % kPStages) * C::kStageBytes;
+            if (ok) {
+                const float tot = ss + xch[g * BM + r];
+                const float rsc = (1.0f - p.lambda_init) / sqrtf(tot / (float)DV + p.eps);
+                const float* w = p.norm_w ? p.norm_w + g * kHalf : nullptr;
+#pragma unroll
+                for (int c = 0; c < kHalf / 32; ++c) {
+                    uint32_t o1[32], o2[32];
+                    tmem_ld32(lane_base + C::kColO + g * kHalf + c * 32, o1);
+                    tmem_ld32(lane_base + C::kColO + DV + g * kHalf + c * 32, o2);
+                    tmem_ld_wait();
+                    // 32 columns = half a box row: box (g DV/2 + 32 c) / 64, 16-byte chunks (c % 2) * 4 ..
+                    uint8_t* box = stage + ((g * kHalf + c * 32) / 64) * (BM * 128);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int i = q * 8 + e;
+                            const float x = __uint_as_float(o1[i]) * inv1 - __uint_as_float(o2[i]) * inv2;
+                            y[e] = x * rsc * (w ? w[c * 32 + i] : 1.f);
+                        }
+                        *reinterpret_cast<uint4*>(box + sw128_offset(r, (c & 1) * 4 + q)) =
+                            make_uint4(pack_16x2(y[0], y[1], f16), pack_16x2(y[2], y[3], f16),
+                                       pack_16x2(y[4], y[5], f16), pack_16x2(y[6], y[7], f16));
+                    }
+                }
+            }
+            // Both groups' reads of O precede this barrier; the next tile's first PV products
+            // (which overwrite O) follow it through the P hand-off.
+            tc_fence_before();
+            fence_proxy_async_shared();
+            named_bar_sync(1, 256);
+            if (threadIdx.x == 0) mbar_arrive(&bars->out_full[(J - 1) % kPStages]);
+        }
+        tc_fence_before();
+        named_bar_sync(2, kThreads);
+    }
+}
+
+template <int D, int DV, bool F16>
+cudaError_t launch_persist_t(const FwdParams& p, cudaStream_t stream) {
+    using C = PersistCfg<D, DV>;
+    auto k = fwd_persist_kernel<D, DV, F16>;
+    cudaError_t e = prepare_once<fwd_persist_kernel<D, DV, F16>>((int)C::kSmem, kRegsLaunch);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
+    const int total = ((p.N + BM - 1) / BM) * p.B * p.H;
+    k<<<min(total, sms), kThreads, C::kSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream) {
-    if (p.d == 64 && p.Dv == 128)
+    if (p.d == 64 && p.Dv == 128) {
+        // Short sequences: the persistent form (its saving per query tile outweighs its
+        // slower key-tile loop while a query tile has few key tiles; measured crossover
+        // near 16 key tiles on average, i.e. causal N = 4096).
+        const int n_tiles = (p.N + BM - 1) / BM;
+        const double mean_kv = p.causal ? 0.5 * (n_tiles + 1) : (double)n_tiles;
+        if ((p.out_bf16 || p.out_f16) && mean_kv <= kPersistMaxMeanKv)
+            return p.in_f16 ? launch_persist_t<64, 128, true>(p, stream) : launch_persist_t<64, 128, false>(p, stream);
         return p.in_f16 ? launch_t<64, 128, true, false>(p, stream) : launch_t<64, 128, false, false>(p, stream);
+    }
     return cudaErrorInvalidValue;
 }
 

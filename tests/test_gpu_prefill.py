@@ -105,6 +105,33 @@ def test_f16_output_is_the_rounded_f32_output(d, Dv, in_dtype):
     assert torch.equal(out16.cpu(), out32.cpu().half())
 
 
+@pytest.mark.parametrize("B,H,N,causal,out_dtype", [
+    (1, 1, 1, True, torch.bfloat16),      # one query tile, one key tile
+    (64, 16, 1, True, torch.float16),     # 1024 query tiles of one key tile each: ~7 per CTA
+    (2, 8, 513, True, torch.bfloat16),    # fewer query tiles than SMs, ragged last tile
+    (8, 16, 640, True, torch.float16),    # several query tiles per CTA, 1..5 key tiles each
+    (4, 16, 1000, False, torch.bfloat16), # non-causal, ragged
+    (1, 4, 2944, True, torch.bfloat16),   # largest causal N of the short-sequence (persistent) form
+    (1, 4, 3072, True, torch.bfloat16),   # smallest N of the per-tile form
+])
+def test_16bit_output_forms(B, H, N, causal, out_dtype):
+    """16-bit outputs of short sequences come from the persistent kernel (one CTA per SM
+    walking query tiles), fp32 outputs from the per-tile kernel; both compute the same fp32
+    values, so the 16-bit output is exactly the fp32 output rounded. Small cases also meet
+    the oracle."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    t = gi.prefill_inputs(w, B=B, H=H, N=N)
+    lam, lam_init = _lam(w)
+    nw = torch.linspace(0.5, 1.5, w.Dv).cuda() if N == 640 else None
+    out32 = _run(t, lam, lam_init, w.eps, causal=causal, norm_weight=nw)
+    out16 = _run(t, lam, lam_init, w.eps, causal=causal, norm_weight=nw, out_dtype=out_dtype)
+    assert torch.equal(out16.cpu(), out32.cpu().to(out_dtype))
+    if B * H * N <= 128 * 1024:
+        ref = orc.diffattn_fwd(*(t[k] for k in NAMES), lam, lam_init, w.eps, causal=causal,
+                               weight=None if nw is None else nw.cpu().numpy())
+        assert_bf16_out_parity(out16, ref, f"{out_dtype} out B{B} H{H} N{N}")
+
+
 def test_bf16_strided_views():
     """Q1/Q2 and K1/K2 as halves of one [B, N, H, 2d] buffer (the module's layout)."""
     w = gi.WORKLOADS["prefill_bf16"]
