@@ -424,25 +424,44 @@ def run_layer(args, da, gi, dev, stream, peaks, peak_kind):
 
 
 def run_backward(args, da, gi, dev, stream, peaks, peak_kind):
-    """The backward pass (diffattn_bwd) on the prefill workload, bf16 inputs, fp32 gradients."""
+    """The backward pass on the prefill workload, bf16 inputs, fp32 gradients: from the state the
+    training forward saved (diffattn_fwd_train + diffattn_bwd(saved=...)), and, beside it, the
+    backward that re-runs the forward itself (diffattn_bwd alone) and the two forwards' times."""
     w = gi.WORKLOADS["prefill_bf16"]
     x = {k: v.to(dev) for k, v in gi.prefill_inputs(w).items()}
     dy = gi.output_grad(w).to(dev)
     lv = gi.lambda_vectors(w)
     lam, lam_init = da.diffattn_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+    ops = (x["q1"], x["q2"], x["k1"], x["k2"], x["v"])
     ws = da.workspace(da.bwd_workspace_bytes(w.B, w.H, w.N, w.d, w.Dv), dev)
-    fn = lambda: da.diffattn_bwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], dy, lam, lam_init, w.eps,
-                                 want_dnorm_weight=True, ws=ws, stream=stream)
-    ms = time_device(fn, extra_reps(args), args.warmup, stream)
-    assert da.read_error(ws) == 0
+    out = torch.empty((w.B, w.N, w.H, w.Dv), dtype=torch.bfloat16, device=dev)
+    fws = da.workspace(256, dev)
+    saved = da.saved_state(w.B, w.H, w.N, w.Dv, dev)
+    train = lambda: da.diffattn_fwd_train(*ops, lam, lam_init, w.eps, out_dtype=torch.bfloat16, out=out,
+                                          saved=saved, ws=fws, stream=stream)
+    plain = lambda: da.diffattn_fwd(*ops, lam, lam_init, w.eps, out_dtype=torch.bfloat16, out=out, ws=fws,
+                                    stream=stream)
+    ms_train = time_device(train, extra_reps(args), args.warmup, stream)
+    ms_plain = time_device(plain, extra_reps(args), args.warmup, stream)
+    train()  # the saved state of these inputs
+    from_saved = lambda: da.diffattn_bwd(*ops, dy, lam, lam_init, w.eps, want_dnorm_weight=True, ws=ws,
+                                         stream=stream, saved=saved)
+    recompute = lambda: da.diffattn_bwd(*ops, dy, lam, lam_init, w.eps, want_dnorm_weight=True, ws=ws,
+                                        stream=stream)
+    ms = time_device(from_saved, extra_reps(args), args.warmup, stream)
+    ms_re = time_device(recompute, extra_reps(args), args.warmup, stream)
+    assert da.read_error(ws) == 0 and da.read_error(fws) == 0
     n_pairs = w.N * (w.N + 1) / 2
     # Chain-rule FLOPs per (b, h): per map S recomputed, dQ and dK (2 Np d each); dV and dA (2 Np Dv each).
     flops = w.B * w.H * (12 * n_pairs * w.d + 4 * n_pairs * w.Dv)
-    # Executed on the tensor cores: the forward re-run (4 Np d + 4 Np Dv), then the key-side kernel
-    # (S1, S2, dA, dV, dK1, dK2: 8 Np d + 4 Np Dv) and the query-side one (S1, S2, dA, dQ1, dQ2: 8 Np d + 2 Np Dv).
-    exec_flops = w.B * w.H * n_pairs * (20 * w.d + 10 * w.Dv)
+    # Executed on the tensor cores: the key-side kernel (S1, S2, dA, dV, dK1, dK2: 8 Np d + 4 Np Dv) and the
+    # query-side one (S1, S2, dA, dQ1, dQ2: 8 Np d + 2 Np Dv); re-running the forward adds 4 Np d + 4 Np Dv.
+    exec_flops = w.B * w.H * n_pairs * (16 * w.d + 6 * w.Dv)
+    exec_re = w.B * w.H * n_pairs * (20 * w.d + 10 * w.Dv)
     tf = flops / (ms * 1e-3) / 1e12
-    return {"workload": "backward of the prefill workload B4 H16 N2048 d64 Dv128 causal, bf16 in, fp32 gradients",
+    tf_re = flops / (ms_re * 1e-3) / 1e12
+    return {"workload": "backward of the prefill workload B4 H16 N2048 d64 Dv128 causal, bf16 in, fp32 gradients, "
+                        "from the training forward's saved state (O1, O2 and each map's row max and sum, fp32)",
             "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "flops_per_step": flops,
             "exec_tflops": exec_flops / (ms * 1e-3) / 1e12,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -450,7 +469,13 @@ def run_backward(args, da, gi, dev, stream, peaks, peak_kind):
                          "traffic_dominant_kernel": {
                              "kernel": "bwd_dkdv_kernel",
                              "bytes": profiled_traffic("bwd_dkdv_prefill_B4H16N2048", ["bwd_tcgen05.cu", "common.cuh"])}},
-            "gpu_launches_per_step": 4}
+            "gpu_launches_per_step": 4,
+            "recompute": {"note": "diffattn_bwd without saved state: the forward re-run as its first launch",
+                          "ms_per_step": ms_re, "value": tf_re, "frac": tf_re / peaks["bf16_tflops"],
+                          "exec_tflops": exec_re / (ms_re * 1e-3) / 1e12, "gpu_launches_per_step": 4},
+            "forward": {"note": "the same inputs' forward, bf16 out: diffattn_fwd_train (per-tile kernel, saves "
+                                f"{2 * w.B * w.H * w.N * w.Dv * 4 / 1e6:.0f} MB of state) against diffattn_fwd",
+                        "train_ms": ms_train, "plain_ms": ms_plain}}
 
 
 def run_decode(args, da, gi, dev, stream, peaks, peak_kind):

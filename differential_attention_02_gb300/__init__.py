@@ -27,7 +27,8 @@ EXPORTED = ("diffattn_status_string", "diffattn_lambda", "diffattn_fwd", "diffat
             "diffattn_bwd", "diffattn_bwd_workspace_size", "diffattn_lambda_bwd", "diffattn_decode_paged_fp8",
             "diffattn_kv_append_paged_fp8", "diffattn_decode_noalloc_read_error",
             "diffattn_selftest_timeout", "diffattn_gemm_residual", "diffattn_gemm_swiglu", "diffattn_fwd_host",
-            "diffattn_fwd_host_buffer_size")
+            "diffattn_fwd_host_buffer_size", "diffattn_train_saved_size", "diffattn_fwd_train",
+            "diffattn_bwd_saved")
 
 
 class DiffAttnError(RuntimeError):
@@ -109,6 +110,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.diffattn_bwd.argtypes = [Tensor4] * 5 + [vp, vp] + [i32] * 6 + [f32] * 3 + [i32] + [vp] * 7 + [vp, sz, vp]
     lib.diffattn_bwd_workspace_size.restype = i32
     lib.diffattn_bwd_workspace_size.argtypes = [i32] * 5 + [ctypes.POINTER(sz)]
+    lib.diffattn_train_saved_size.restype = i32
+    lib.diffattn_train_saved_size.argtypes = [i32] * 4 + [ctypes.POINTER(sz)]
+    lib.diffattn_fwd_train.restype = i32
+    lib.diffattn_fwd_train.argtypes = [Tensor4] * 5 + [vp, vp] + [i32] * 6 + [f32] * 3 + [i32, i32, vp, sz, vp, sz, vp]
+    lib.diffattn_bwd_saved.restype = i32
+    lib.diffattn_bwd_saved.argtypes = ([Tensor4] * 5 + [vp, vp] + [i32] * 6 + [f32] * 3 + [i32, vp, sz] + [vp] * 7 +
+                                       [vp, sz, vp])
     fpp = ctypes.POINTER(ctypes.c_float)
     lib.diffattn_lambda_bwd.restype = i32
     lib.diffattn_lambda_bwd.argtypes = [fpp] * 4 + [i32, f32] + [fpp] * 4
@@ -215,11 +223,54 @@ def diffattn_fwd(q1, q2, k1, k2, v, lam: float, lam_init: float, eps: float = 1e
     return out
 
 
+def train_saved_bytes(B, H, N, Dv) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().diffattn_train_saved_size(B, H, N, Dv, ctypes.byref(n)), "diffattn_train_saved_size")
+    return n.value
+
+
+def saved_state(B, H, N, Dv, device=None) -> torch.Tensor:
+    """A buffer of its own (not the cached workspace: the state must outlive other calls)
+    for diffattn_fwd_train's saved state: 256-byte aligned, train_saved_bytes() long."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    n = train_saved_bytes(B, H, N, Dv)
+    buf = torch.empty(n + 256, dtype=torch.uint8, device=dev)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + n]
+
+
+def diffattn_fwd_train(q1, q2, k1, k2, v, lam: float, lam_init: float, eps: float = 1e-5, norm_weight=None,
+                       causal: bool = True, out_dtype=torch.float32, out=None, saved=None, ws=None, stream=None):
+    """diffattn_fwd that also saves the state diffattn_bwd(..., saved=...) starts from (bf16/fp16,
+    d=64, Dv=128). Returns (out, saved); `saved` is a uint8 device buffer of train_saved_bytes()."""
+    B, H, N, d = q1.shape
+    Dv = v.shape[-1]
+    for t in (q1, q2, k1, k2, v):
+        if not t.is_cuda or t.dtype != q1.dtype:
+            raise ValueError("all operands must be CUDA tensors of one dtype")
+    dev = q1.device
+    if out is None:
+        out = torch.empty((B, N, H, Dv), dtype=out_dtype, device=dev)
+    if saved is None:
+        saved = saved_state(B, H, N, Dv, dev)
+    lib = load_library()
+    if ws is None:
+        ws = workspace(256, dev)
+    w = None if norm_weight is None else ctypes.c_void_p(norm_weight.data_ptr())
+    _check(lib.diffattn_fwd_train(_t4(q1), _t4(q2), _t4(k1), _t4(k2), _t4(v), ctypes.c_void_p(out.data_ptr()), w,
+                                  B, H, N, d, Dv, int(bool(causal)), float(lam), float(lam_init), float(eps),
+                                  _dtype_code(q1.dtype), _dtype_code(out.dtype), ctypes.c_void_p(saved.data_ptr()),
+                                  saved.numel(), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream)),
+           "diffattn_fwd_train")
+    return out, saved
+
+
 def diffattn_bwd(q1, q2, k1, k2, v, dy, lam: float, lam_init: float, eps: float = 1e-5, norm_weight=None,
-                 causal: bool = True, want_dnorm_weight: bool = False, ws=None, stream=None) -> dict:
+                 causal: bool = True, want_dnorm_weight: bool = False, ws=None, stream=None, saved=None) -> dict:
     """Backward of diffattn_fwd. Operands as for diffattn_fwd (one dtype: fp32, bf16 or fp16); dy
     [B,N,H,Dv] of that dtype. Returns dq1, dq2, dk1, dk2 [B,H,N,d] fp32, dv [B,H,N,Dv] fp32, dlam
-    (a 1-element fp32 device tensor) and dw ([Dv] fp32, or None)."""
+    (a 1-element fp32 device tensor) and dw ([Dv] fp32, or None). With `saved` (from
+    diffattn_fwd_train on the same inputs) it starts from that state (diffattn_bwd_saved)."""
     B, H, N, d = q1.shape
     Dv = v.shape[-1]
     for t in (q1, q2, k1, k2, v, dy):
@@ -238,11 +289,14 @@ def diffattn_bwd(q1, q2, k1, k2, v, dy, lam: float, lam_init: float, eps: float 
         _check(lib.diffattn_bwd_workspace_size(B, H, N, d, Dv, ctypes.byref(nbytes)), "diffattn_bwd_workspace_size")
         ws = workspace(nbytes.value, dev)
     ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
-    _check(lib.diffattn_bwd(_t4(q1), _t4(q2), _t4(k1), _t4(k2), _t4(v), ptr(dy), ptr(norm_weight), B, H, N, d, Dv,
-                            int(bool(causal)), float(lam), float(lam_init), float(eps), _dtype_code(q1.dtype),
-                            ptr(g["dq1"]), ptr(g["dq2"]), ptr(g["dk1"]), ptr(g["dk2"]), ptr(g["dv"]), ptr(g["dlam"]),
-                            ptr(g["dw"]), ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream)),
-           "diffattn_bwd")
+    head = (_t4(q1), _t4(q2), _t4(k1), _t4(k2), _t4(v), ptr(dy), ptr(norm_weight), B, H, N, d, Dv,
+            int(bool(causal)), float(lam), float(lam_init), float(eps), _dtype_code(q1.dtype))
+    grads = (ptr(g["dq1"]), ptr(g["dq2"]), ptr(g["dk1"]), ptr(g["dk2"]), ptr(g["dv"]), ptr(g["dlam"]), ptr(g["dw"]))
+    tail = (ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream))
+    if saved is None:
+        _check(lib.diffattn_bwd(*head, *grads, *tail), "diffattn_bwd")
+    else:
+        _check(lib.diffattn_bwd_saved(*head, ptr(saved), saved.numel(), *grads, *tail), "diffattn_bwd_saved")
     return g
 
 

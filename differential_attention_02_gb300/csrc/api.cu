@@ -16,6 +16,7 @@
 using namespace da;
 
 namespace {
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // ---------------------------------------------------------------- helpers
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -188,10 +189,15 @@ diffattn_status diffattn_fwd_workspace_size(int B, int H, int N, int d, int Dv, 
     return DIFFATTN_OK;
 }
 
-diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
-                             diffattn_tensor v, void* out, const float* norm_weight, int B, int H, int N, int d,
-                             int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype,
-                             int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// diffattn_fwd, and with o_save/ml_save set the training forward (tensor-core path,
+// d=64/Dv=128; the caller has checked that).
+diffattn_status fwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                         diffattn_tensor v, void* out, const float* norm_weight, int B, int H, int N, int d, int Dv,
+                         int causal, float lambda, float lambda_init, float eps, int in_dtype, int out_dtype,
+                         void* workspace, size_t workspace_bytes, void* stream, float* o_save, float* ml_save) {
     if (B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
     if ((in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16 && in_dtype != DIFFATTN_F16) ||
         (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16 && out_dtype != DIFFATTN_F16) ||
@@ -253,9 +259,64 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
     p.err = err_word(workspace);
+    if (o_save != nullptr) {
+        p.o_save = o_save;
+        p.ml_save = ml_save;
+        if (!encode_out_3d(&p.tm_osave, o_save, Dv, N, 2 * B * H, 4, kFwdBM)) return DIFFATTN_ERR_INVALID_ARG;
+        return cuda_status(launch_fwd_train(p, st));
+    }
     // (64, 128): both maps share one CTA; (128, 256): the accumulators of both
     // maps do not fit one CTA's tensor memory, so a CTA pair splits the maps.
     return cuda_status(d == 64 ? launch_fwd_bf16(p, st) : launch_fwd_pair_bf16(p, st));
+}
+
+// The training forward's saved state: O1, O2 (fp32 [2][B, H, N, Dv]), then the
+// per-row max and sum of both maps (fp32 [B, H, N, 4]), each part 256-byte aligned.
+struct SavedLayout {
+    size_t o, ml, total;
+};
+SavedLayout saved_layout(int B, int H, int N, int Dv) {
+    const size_t rows = (size_t)B * H * N;
+    SavedLayout l;
+    l.o = 0;
+    l.ml = round256(2 * rows * Dv * sizeof(float));
+    l.total = l.ml + round256(rows * 4 * sizeof(float));
+    return l;
+}
+bool saved_ok(const void* saved, size_t bytes, int B, int H, int N, int Dv) {
+    return saved != nullptr && !(reinterpret_cast<uintptr_t>(saved) & 255u) && bytes >= saved_layout(B, H, N, Dv).total;
+}
+}  // namespace
+
+extern "C" {
+
+diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                             diffattn_tensor v, void* out, const float* norm_weight, int B, int H, int N, int d,
+                             int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype,
+                             int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_impl(q1, q2, k1, k2, v, out, norm_weight, B, H, N, d, Dv, causal, lambda, lambda_init, eps, in_dtype,
+                    out_dtype, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+diffattn_status diffattn_train_saved_size(int B, int H, int N, int Dv, size_t* bytes) {
+    if (!bytes || B < 0 || H < 0 || N < 0 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    *bytes = saved_layout(B, H, N, Dv).total;
+    return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_fwd_train(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                                   diffattn_tensor v, void* out, const float* norm_weight, int B, int H, int N, int d,
+                                   int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype,
+                                   int out_dtype, void* saved, size_t saved_bytes, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    if (in_dtype == DIFFATTN_F32) return DIFFATTN_ERR_UNSUPPORTED;
+    if (B > 0 && H > 0 && N > 0 && !(d == 64 && Dv == 128)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (B > 0 && H > 0 && N > 0 && !saved_ok(saved, saved_bytes, B, H, N, Dv)) return DIFFATTN_ERR_INVALID_ARG;
+    uint8_t* sv = static_cast<uint8_t*>(saved);
+    const SavedLayout sl = saved_layout(B < 0 ? 0 : B, H < 0 ? 0 : H, N < 0 ? 0 : N, Dv < 1 ? 1 : Dv);
+    return fwd_impl(q1, q2, k1, k2, v, out, norm_weight, B, H, N, d, Dv, causal, lambda, lambda_init, eps, in_dtype,
+                    out_dtype, workspace, workspace_bytes, stream, reinterpret_cast<float*>(sv + sl.o),
+                    reinterpret_cast<float*>(sv + sl.ml));
 }
 
 diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int Dv, int num_splits, size_t* bytes) {
@@ -332,7 +393,6 @@ diffattn_status diffattn_decode(const void* q1, const void* q2, diffattn_tensor 
 }
 
 namespace {
-size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Byte offsets of the backward's workspace regions after the control block.
 struct BwdLayout {
@@ -357,11 +417,16 @@ diffattn_status diffattn_bwd_workspace_size(int B, int H, int N, int d, int Dv, 
     return DIFFATTN_OK;
 }
 
-diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
-                             diffattn_tensor v, const void* dy, const float* norm_weight, int B, int H, int N, int d,
-                             int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype, float* dq1,
-                             float* dq2, float* dk1, float* dk2, float* dv, float* dlambda, float* dnorm_weight,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// diffattn_bwd, and with `saved` set the backward from a training forward's saved
+// state (tensor-core path only; the caller has checked the saved buffer).
+diffattn_status bwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                         diffattn_tensor v, const void* dy, const float* norm_weight, int B, int H, int N, int d, int Dv,
+                         int causal, float lambda, float lambda_init, float eps, int in_dtype, float* dq1, float* dq2,
+                         float* dk1, float* dk2, float* dv, float* dlambda, float* dnorm_weight, void* workspace,
+                         size_t workspace_bytes, void* stream, const void* saved) {
     if (B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
     if (in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16 && in_dtype != DIFFATTN_F16)
         return DIFFATTN_ERR_INVALID_ARG;
@@ -390,6 +455,7 @@ diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     p.part_w = reinterpret_cast<float*>(ws + lay.part_w);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int dt = in_dtype == DIFFATTN_F32 ? 0 : in_dtype == DIFFATTN_BF16 ? 1 : 2;
+    if (saved != nullptr && !bwd_tc_supported(d, Dv, dt)) return DIFFATTN_ERR_UNSUPPORTED;
     if (bwd_tc_supported(d, Dv, dt)) {
         // Tensor-core path: the forward re-run with the preparation epilogue (dO in
         // the operand type, per-row statistics, dlambda and gain partials), the
@@ -433,7 +499,17 @@ diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
         t.scale_log2 = f.scale_log2;
         t.scale = (float)(1.0 / sqrt((double)d));
         t.err = err_word(workspace);
-        cudaError_t e = launch_bwd_prep(f, st);
+        cudaError_t e;
+        if (saved != nullptr) {
+            // The forward's state was saved: only the per-row preparation remains.
+            const SavedLayout sl = saved_layout(B, H, N, Dv);
+            uint8_t* sv = static_cast<uint8_t*>(const_cast<void*>(saved));
+            f.o_save = reinterpret_cast<float*>(sv + sl.o);
+            f.ml_save = reinterpret_cast<float*>(sv + sl.ml);
+            e = launch_bwd_prep_saved(f, st);
+        } else {
+            e = launch_bwd_prep(f, st);
+        }
         if (e == cudaSuccess) e = launch_bwd_tc(t, st);
         if (e == cudaSuccess) e = launch_bwd_reduce(p, (int64_t)((N + kFwdBM - 1) / kFwdBM) * B * H, st);
         return cuda_status(e);
@@ -455,6 +531,34 @@ diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
     p.in_dtype = dt;
     p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
     return cuda_status(launch_bwd_simt(p, st));
+}
+}  // namespace
+
+extern "C" {
+
+diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                             diffattn_tensor v, const void* dy, const float* norm_weight, int B, int H, int N, int d,
+                             int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype, float* dq1,
+                             float* dq2, float* dk1, float* dk2, float* dv, float* dlambda, float* dnorm_weight,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(q1, q2, k1, k2, v, dy, norm_weight, B, H, N, d, Dv, causal, lambda, lambda_init, eps, in_dtype,
+                    dq1, dq2, dk1, dk2, dv, dlambda, dnorm_weight, workspace, workspace_bytes, stream, nullptr);
+}
+
+diffattn_status diffattn_bwd_saved(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                                   diffattn_tensor v, const void* dy, const float* norm_weight, int B, int H, int N,
+                                   int d, int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype,
+                                   const void* saved, size_t saved_bytes, float* dq1, float* dq2, float* dk1,
+                                   float* dk2, float* dv, float* dlambda, float* dnorm_weight, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    if (in_dtype == DIFFATTN_F32) return DIFFATTN_ERR_UNSUPPORTED;
+    if (B > 0 && H > 0 && N > 0) {
+        if (!(d == 64 && Dv == 128)) return DIFFATTN_ERR_UNSUPPORTED;
+        if (!saved_ok(saved, saved_bytes, B, H, N, Dv)) return DIFFATTN_ERR_INVALID_ARG;
+    }
+    return bwd_impl(q1, q2, k1, k2, v, dy, norm_weight, B, H, N, d, Dv, causal, lambda, lambda_init, eps, in_dtype,
+                    dq1, dq2, dk1, dk2, dv, dlambda, dnorm_weight, workspace, workspace_bytes, stream,
+                    saved);
 }
 
 diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2, int d,

@@ -401,7 +401,15 @@ __device__ __forceinline__ void prep_epilogue(const FwdParams& p, bool ok, int g
     }
 }
 
-template <int D, int DV, bool F16, bool PREP>
+// What the per-tile kernel's epilogue does: store the output (plain), derive the
+// backward's inputs instead (prep), or store the output and save the state the
+// backward starts from (save: the unnormalised O1, O2 and each map's max and sum).
+constexpr int kModePlain = 0, kModePrep = 1, kModeSave = 2;
+// Save mode stages O1, O2 (8 boxes of 16 KB) in the K/V ring after the output's
+// staging (at most 64 KB, fp32 output).
+constexpr int kSaveStageOff = 64 * 1024;
+
+template <int D, int DV, bool F16, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D, DV>;
     extern __shared__ uint8_t smem_raw[];
@@ -491,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 // into the stage the ring frees next, so they land during the last tiles' work
                 // (the epilogue reads them; out-of-range rows read zeros).
                 bool dy_loaded = false;
-                if constexpr (PREP) {
+                if constexpr (MODE == kModePrep) {
                     const int s = nkv % kKvStages;
                     if (j == nkv &&
                         mbar_wait(&bars->kv_empty[s], ((nkv / kKvStages) & 1) ^ 1, abort_flag, p.err, 0x3e)) {
@@ -686,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         }
         tc_fence_after();
         named_bar_sync(1, 256);  // both groups past their last PV: the Q1 tile is free
-        if constexpr (PREP) {
+        if constexpr (MODE == kModePrep) {
             // The exchange slots take 8 x BM floats of the Q1 tile; the gain-gradient
             // terms [BM][DV + 1] take the idle K/V ring.
             // dy is in stage nkv % 3 (the producer's last load); the gain-gradient terms take the
@@ -714,6 +722,21 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 tmem_ld32(lane_base + C::kColO + g * kHalf + c * 32, o1);
                 tmem_ld32(lane_base + C::kColO + DV + g * kHalf + c * 32, o2);
                 tmem_ld_wait();
+                if constexpr (MODE == kModeSave) {
+                    // This group's half of both unnormalised accumulators, as they are in TMEM,
+                    // staged for TMA stores behind the output's staging in the idle K/V ring:
+                    // boxes of [128 rows][32 fp32], map m's box j at (4 m + j) * 16 KB.
+                    static_assert(kSaveStageOff + 8 * BM * 128 <= kKvStages * C::kStageBytes, "O staging fits");
+                    uint8_t* sb = smem + C::kOffStages + kSaveStageOff;
+                    const int j = (g * kHalf + c * 32) / 32;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        *reinterpret_cast<uint4*>(sb + j * (BM * 128) + sw128_offset(r, i)) =
+                            make_uint4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
+                        *reinterpret_cast<uint4*>(sb + (4 + j) * (BM * 128) + sw128_offset(r, i)) =
+                            make_uint4(o2[4 * i], o2[4 * i + 1], o2[4 * i + 2], o2[4 * i + 3]);
+                    }
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float x = __uint_as_float(o1[i]) * inv1 - __uint_as_float(o2[i]) * inv2;
@@ -721,6 +744,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                     ss = fmaf(x, x, ss);
                 }
             }
+        }
+        if constexpr (MODE == kModeSave) {
+            // This map's running max (scaled-score units) and sum for the row.
+            if (ok && qrow < p.N)
+                *reinterpret_cast<float2*>(p.ml_save + (((int64_t)b * p.H + h) * p.N + qrow) * 4 + 2 * g) =
+                    make_float2(m_used, l);
         }
         epi[(2 + g) * BM + r] = ss;
         named_bar_sync(1, 256);
@@ -775,6 +804,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
             const int bw = p.out_bf16 || p.out_f16 ? 64 : 32;  // elements per 128-byte box row
             index_ok(q0 < p.N, p.err, 0x92);
             for (int i = 0; i < DV / bw; ++i) tma_store_3d(&p.tm_out, stage + i * (BM * 128), h * DV + i * bw, q0, b);
+            if constexpr (MODE == kModeSave) {
+                // O1 and O2 of the tile: rows [q0, q0 + 128) of head (b, h) in maps 0 and 1 of the
+                // [2 B H][N][Dv] view; rows past N are clipped.
+                static_assert(DV == 128, "four 32-column boxes per map");
+                for (int m = 0; m < 2; ++m)
+                    for (int jb = 0; jb < 4; ++jb)
+                        tma_store_3d(&p.tm_osave, stage + kSaveStageOff + (4 * m + jb) * (BM * 128), jb * 32, q0,
+                                     (m * p.B + b) * p.H + h);
+            }
             tma_store_commit();
             tma_store_wait_read();
         }
@@ -783,12 +821,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     }
 }
 
-template <int D, int DV, bool F16, bool PREP>
+template <int D, int DV, bool F16, int MODE>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
     using C = FwdCfg<D, DV>;
-    auto k = fwd_bf16_kernel<D, DV, F16, PREP>;
+    auto k = fwd_bf16_kernel<D, DV, F16, MODE>;
     // The register split assumes the compiled per-thread count (see kRegsLaunch).
-    cudaError_t e = prepare_once<fwd_bf16_kernel<D, DV, F16, PREP>>((int)C::kSmem, kRegsLaunch);
+    cudaError_t e = prepare_once<fwd_bf16_kernel<D, DV, F16, MODE>>((int)C::kSmem, kRegsLaunch);
     if (e != cudaSuccess) return e;
     const int n_tiles = (p.N + BM - 1) / BM;
     k<<<n_tiles * p.B * p.H, kThreads, C::kSmem, stream>>>(p);
@@ -1190,6 +1228,156 @@ cudaError_t launch_persist_t(const FwdParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Backward preparation from the state a training forward saved, on the CUDA
+// cores: per query row, the quantities prep_epilogue derives in the forward
+// (dO rounded to the operand type, L1, L2, D1, D2, and the row's dlambda and
+// gain-gradient terms), from O1, O2 and each map's max and sum instead of TMEM.
+// HBM-bound (~1.3 KB per row): one warp per row, four columns per lane, warp
+// butterflies for the row sums; one CTA (8 warps) per 128-row query tile, whose
+// rows its warps take in a fixed order, so the per-CTA partials of dlambda and
+// of the gain's gradient are indexed and summed like the forward's.
+constexpr int kSavedThreads = 256;
+
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(kSavedThreads) bwd_prep_saved_kernel(const __grid_constant__ FwdParams p) {
+    constexpr int DV = 128, kWarps = kSavedThreads / 32;
+    using T16x2 = typename std::conditional<F16, __half2, __nv_bfloat162>::type;
+    __shared__ float wsum[kWarps][DV];
+    __shared__ float lsum[kWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = (p.N + BM - 1) / BM;
+    const int BH = p.B * p.H;
+    const int qt = n_tiles - 1 - (int)(blockIdx.x / BH);  // the forward's CTA order
+    const int bh = blockIdx.x % BH;
+    const int b = bh / p.H, h = bh % p.H;
+    const int q0 = qt * BM;
+    const float lam = p.lambda, cs = 1.0f - p.lambda_init;
+    const int c0 = 4 * lane;
+    const float4 w = p.norm_w ? *reinterpret_cast<const float4*>(p.norm_w + c0) : make_float4(1.f, 1.f, 1.f, 1.f);
+    const int64_t map_stride = (int64_t)BH * p.N * DV;
+    float dw[4] = {0.f, 0.f, 0.f, 0.f}, dl = 0.f;
+    // The warp's rows, in order; each row's operands are loaded one row ahead.
+    const int rbeg = q0 + warp * (BM / kWarps), rend = min(rbeg + BM / kWarps, p.N);
+    struct RowIn {
+        float4 ml, o1, o2;  // max1, sum1, max2, sum2; this lane's columns of O1, O2
+        uint2 dy;
+    };
+    auto load_row = [&](int qrow) {
+        const int64_t row = ((int64_t)b * p.H + h) * p.N + qrow;
+        RowIn in;
+        in.ml = *reinterpret_cast<const float4*>(p.ml_save + row * 4);
+        in.o1 = *reinterpret_cast<const float4*>(p.o_save + row * DV + c0);
+        in.o2 = *reinterpret_cast<const float4*>(p.o_save + map_stride + row * DV + c0);
+        in.dy = *reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.dy) +
+                                                ((((int64_t)b * p.N + qrow) * p.H + h) * DV + c0) * 2);
+        return in;
+    };
+    RowIn next{};
+    if (rbeg < rend) next = load_row(rbeg);
+    for (int qrow = rbeg; qrow < rend; ++qrow) {  // warp-uniform bounds
+        const int64_t row = ((int64_t)b * p.H + h) * p.N + qrow;
+        const RowIn cur = next;
+        if (qrow + 1 < rend) next = load_row(qrow + 1);
+        const float4 ml = cur.ml, o1 = cur.o1, o2 = cur.o2;
+        const uint2 dyr = cur.dy;
+        const float i1 = 1.0f / ml.y, i2 = 1.0f / ml.w;
+        const float a1[4] = {o1.x * i1, o1.y * i1, o1.z * i1, o1.w * i1};
+        const float a2[4] = {o2.x * i2, o2.y * i2, o2.z * i2, o2.w * i2};
+        float dyv[4];
+        if constexpr (F16) {
+            const float2 u = __half22float2(*reinterpret_cast<const __half2*>(&dyr.x));
+            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&dyr.y));
+            dyv[0] = u.x; dyv[1] = u.y; dyv[2] = v.x; dyv[3] = v.y;
+        } else {
+            dyv[0] = bf16lo_to_f32(dyr.x); dyv[1] = bf16hi_to_f32(dyr.x);
+            dyv[2] = bf16lo_to_f32(dyr.y); dyv[3] = bf16hi_to_f32(dyr.y);
+        }
+        const float wv[4] = {w.x, w.y, w.z, w.w};
+        float x[4], ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[k] = a1[k] - lam * a2[k];
+            ss = fmaf(x[k], x[k], ss);
+        }
+        const float ir = 1.0f / sqrtf(warp_allsum(ss) / (float)DV + p.eps);
+        float n[4], gg[4], gn = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            n[k] = x[k] * ir;
+            gg[k] = dyv[k] * wv[k] * cs;
+            gn = fmaf(gg[k], n[k], gn);
+        }
+        gn = warp_allsum(gn) / (float)DV;
+        float d[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) d[k] = (gg[k] - n[k] * gn) * ir;
+        // dO in the operand type; D1, D2 from the rounded dO the gradient products use (so
+        // that sum_j P_ij (dA_ij - D_i) stays zero for every row), dlambda from the unrounded one.
+        T16x2 lo, hi;
+        float r[4];
+        if constexpr (F16) {
+            lo = __floats2half2_rn(d[0], d[1]);
+            hi = __floats2half2_rn(d[2], d[3]);
+            const float2 u = __half22float2(lo), v = __half22float2(hi);
+            r[0] = u.x; r[1] = u.y; r[2] = v.x; r[3] = v.y;
+        } else {
+            lo = __floats2bfloat162_rn(d[0], d[1]);
+            hi = __floats2bfloat162_rn(d[2], d[3]);
+            const float2 u = __bfloat1622float2(lo), v = __bfloat1622float2(hi);
+            r[0] = u.x; r[1] = u.y; r[2] = v.x; r[3] = v.y;
+        }
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.d_o) + (row * DV + c0) * 2) = packed;
+        float x1 = 0.f, x2 = 0.f, x2e = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x1 = fmaf(r[k], a1[k], x1);
+            x2 = fmaf(r[k], a2[k], x2);
+            x2e = fmaf(d[k], a2[k], x2e);
+            dw[k] = fmaf(dyv[k] * n[k], cs, dw[k]);
+        }
+        x1 = warp_allsum(x1);
+        x2 = warp_allsum(x2);
+        x2e = warp_allsum(x2e);
+        if (lane == 0)
+            *reinterpret_cast<float4*>(p.stats + row * 4) =
+                make_float4(ml.x + __log2f(ml.y), ml.z + __log2f(ml.w), x1, -lam * x2);
+        dl -= x2e;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) wsum[warp][c0 + k] = dw[k];
+    if (lane == 0) lsum[warp] = dl;
+    __syncthreads();
+    if (threadIdx.x < DV) {
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < kWarps; ++k) acc += wsum[k][threadIdx.x];
+        p.part_w[(int64_t)blockIdx.x * DV + threadIdx.x] = acc;
+    }
+    if (threadIdx.x == 0) {
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < kWarps; ++k) acc += lsum[k];
+        p.part_lam[blockIdx.x] = acc;
+    }
+}
+
+template <bool F16>
+cudaError_t launch_prep_saved_t(const FwdParams& p, cudaStream_t stream) {
+    const int n_tiles = (p.N + BM - 1) / BM;
+    bwd_prep_saved_kernel<F16><<<n_tiles * p.B * p.H, kSavedThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream) {
@@ -1201,14 +1389,26 @@ cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream) {
         const double mean_kv = p.causal ? 0.5 * (n_tiles + 1) : (double)n_tiles;
         if ((p.out_bf16 || p.out_f16) && mean_kv <= kPersistMaxMeanKv)
             return p.in_f16 ? launch_persist_t<64, 128, true>(p, stream) : launch_persist_t<64, 128, false>(p, stream);
-        return p.in_f16 ? launch_t<64, 128, true, false>(p, stream) : launch_t<64, 128, false, false>(p, stream);
+        return p.in_f16 ? launch_t<64, 128, true, kModePlain>(p, stream) : launch_t<64, 128, false, kModePlain>(p, stream);
     }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_train(const FwdParams& p, cudaStream_t stream) {
+    if (p.d == 64 && p.Dv == 128 && p.o_save && p.ml_save)
+        return p.in_f16 ? launch_t<64, 128, true, kModeSave>(p, stream) : launch_t<64, 128, false, kModeSave>(p, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_prep_saved(const FwdParams& p, cudaStream_t stream) {
+    if (p.d == 64 && p.Dv == 128 && p.dy && p.d_o && p.stats && p.part_lam && p.part_w && p.o_save && p.ml_save)
+        return p.in_f16 ? launch_prep_saved_t<true>(p, stream) : launch_prep_saved_t<false>(p, stream);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_prep(const FwdParams& p, cudaStream_t stream) {
     if (p.d == 64 && p.Dv == 128 && p.dy && p.d_o && p.stats && p.part_lam && p.part_w)
-        return p.in_f16 ? launch_t<64, 128, true, true>(p, stream) : launch_t<64, 128, false, true>(p, stream);
+        return p.in_f16 ? launch_t<64, 128, true, kModePrep>(p, stream) : launch_t<64, 128, false, kModePrep>(p, stream);
     return cudaErrorInvalidValue;
 }
 

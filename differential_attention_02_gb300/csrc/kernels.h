@@ -171,9 +171,16 @@ struct FwdParams {
     float* stats = nullptr;        // [B, H, N, 4]: log2 sum-exp of map 1, of map 2 (scaled-score units), D1, D2
     float* part_lam = nullptr;     // [grid] per-CTA partial of dlambda
     float* part_w = nullptr;       // [grid][Dv] per-CTA partial of the gain's gradient
+    // Training forward (launch_fwd_train) writes, besides the output, the state the
+    // backward starts from; launch_bwd_prep_saved reads it instead of re-running the forward.
+    float* o_save = nullptr;       // [2][B, H, N, Dv]: the unnormalised accumulators O1, O2 (fp32)
+    CUtensorMap tm_osave;          // 3-D map over o_save [2 B H][N][Dv] fp32, boxes of 32 x 128 rows
+    float* ml_save = nullptr;      // [B, H, N, 4]: running max of map 1 (scaled-score units), its sum, max 2, sum 2
 };
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);       // both maps in one CTA
+cudaError_t launch_fwd_train(const FwdParams& p, cudaStream_t stream);      // d=64: forward + saved state
 cudaError_t launch_bwd_prep(const FwdParams& p, cudaStream_t stream);       // d=64: forward + backward inputs
+cudaError_t launch_bwd_prep_saved(const FwdParams& p, cudaStream_t stream); // d=64: backward inputs from the saved state
 cudaError_t launch_fwd_pair_bf16(const FwdParams& p, cudaStream_t stream);  // one map per CTA of a pair
 constexpr int kFwdBM = 128;
 constexpr int kFwdBN = 128;

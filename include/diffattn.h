@@ -367,6 +367,46 @@ diffattn_status diffattn_bwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
 diffattn_status diffattn_bwd_workspace_size(int B, int H, int N, int d, int Dv, size_t* bytes);
 
 /*
+ * Training pair: a forward that also saves the state the backward starts from,
+ * and the backward that starts from it instead of re-running the forward.
+ *
+ * diffattn_fwd_train — diffattn_fwd (same arguments, same output, bit for bit)
+ * that also writes into `saved` each map's unnormalised accumulator
+ * O_m = sum_j exp2(S_m log2(e)/sqrt(d) - max_m) V_j (f32 [2][B, H, N, Dv]) and,
+ * per row, each map's running max (in log2(e)/sqrt(d) score units) and sum
+ * (f32 [B, H, N, 4]: max1, sum1, max2, sum2): the forward's TMEM state after its
+ * last PV products. Tensor-core path only: bf16 or f16 with (d, Dv) = (64, 128)
+ * (else DIFFATTN_ERR_UNSUPPORTED); it always runs the per-tile kernel.
+ * saved: device, diffattn_train_saved_size() bytes, 256-byte aligned, owned by
+ *   the caller; the contents are meant only for diffattn_bwd_saved with the same
+ *   q1..v, norm_weight, shapes, causal, lambda, lambda_init, eps and in_dtype.
+ *
+ * diffattn_bwd_saved — diffattn_bwd (same arguments and outputs) from `saved`:
+ * its preparation (one CUDA-core pass over the rows, bandwidth-bound) reads O_m
+ * and the row statistics instead of recomputing the scores, softmaxes and PV
+ * products, then the same key-side, query-side and reduction kernels run. The
+ * gradients agree with diffattn_bwd's to rounding: the per-row sums (the norm, D1,
+ * D2) are added in another fp32 order, so an element of dO can round the other
+ * way. Deterministic. Same support as diffattn_fwd_train; workspace as for
+ * diffattn_bwd.
+ */
+diffattn_status diffattn_train_saved_size(int B, int H, int N, int Dv, size_t* bytes);
+diffattn_status diffattn_fwd_train(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                                   diffattn_tensor v, void* out, const float* norm_weight,
+                                   int B, int H, int N, int d, int Dv, int causal,
+                                   float lambda, float lambda_init, float eps, int in_dtype, int out_dtype,
+                                   void* saved, size_t saved_bytes,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+diffattn_status diffattn_bwd_saved(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
+                                   diffattn_tensor v, const void* dy, const float* norm_weight,
+                                   int B, int H, int N, int d, int Dv, int causal,
+                                   float lambda, float lambda_init, float eps, int in_dtype,
+                                   const void* saved, size_t saved_bytes,
+                                   float* dq1, float* dq2, float* dk1, float* dk2, float* dv,
+                                   float* dlambda, float* dnorm_weight,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * diffattn_lambda_bwd — on the host, the gradients of
  *   lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init
  * with respect to the four vectors, given dlambda:

@@ -358,6 +358,55 @@ def test_bwd_argument_validation(lib):
     assert _bwd(lib, ws=0x40010) == da.ERR_WORKSPACE
 
 
+def test_training_pair_argument_validation(lib):
+    """diffattn_fwd_train / diffattn_bwd_saved: the saved-state size and the checks that
+    run before anything is launched."""
+    n = ctypes.c_size_t()
+    assert lib.diffattn_train_saved_size(1, 2, 16, 128, ctypes.byref(n)) == da.OK
+    rows = 2 * 16
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert n.value == r256(2 * rows * 128 * 4) + r256(rows * 16)
+    assert lib.diffattn_train_saved_size(1, -2, 16, 128, ctypes.byref(n)) == da.ERR_INVALID_ARG
+    assert lib.diffattn_train_saved_size(1, 2, 16, 128, None) == da.ERR_INVALID_ARG
+    nbytes = n.value
+
+    def train(**kw):
+        a = dict(q1=_tensor(), q2=_tensor(), k1=_tensor(), k2=_tensor(), v=_tensor(sn=128), out=0x20000, w=None,
+                 B=1, H=2, N=16, d=64, Dv=128, causal=1, lam=0.5, lam_init=0.2, eps=1e-5, ind=da.BF16, outd=da.BF16,
+                 saved=0x50000, savedb=nbytes, ws=0x40000, wsb=256, stream=None)
+        a.update(kw)
+        vp = lambda x: None if x is None else ctypes.c_void_p(x)
+        return lib.diffattn_fwd_train(a["q1"], a["q2"], a["k1"], a["k2"], a["v"], vp(a["out"]), vp(a["w"]), a["B"],
+                                      a["H"], a["N"], a["d"], a["Dv"], a["causal"], a["lam"], a["lam_init"], a["eps"],
+                                      a["ind"], a["outd"], vp(a["saved"]), a["savedb"], vp(a["ws"]), a["wsb"],
+                                      a["stream"])
+
+    def bwd(**kw):
+        a = dict(q1=_tensor(), q2=_tensor(), k1=_tensor(), k2=_tensor(), v=_tensor(sn=128), dy=0x20000, w=None,
+                 B=1, H=2, N=16, d=64, Dv=128, causal=1, lam=0.5, lam_init=0.2, eps=1e-5, ind=da.BF16,
+                 saved=0x50000, savedb=nbytes, dq1=0x30000, dq2=0x30000, dk1=0x30000, dk2=0x30000, dv=0x30000,
+                 dlam=0x30000, dw=None, ws=0x40000, wsb=1 << 30, stream=None)
+        a.update(kw)
+        vp = lambda x: None if x is None else ctypes.c_void_p(x)
+        return lib.diffattn_bwd_saved(a["q1"], a["q2"], a["k1"], a["k2"], a["v"], vp(a["dy"]), vp(a["w"]), a["B"],
+                                      a["H"], a["N"], a["d"], a["Dv"], a["causal"], a["lam"], a["lam_init"], a["eps"],
+                                      a["ind"], vp(a["saved"]), a["savedb"], vp(a["dq1"]), vp(a["dq2"]), vp(a["dk1"]),
+                                      vp(a["dk2"]), vp(a["dv"]), vp(a["dlam"]), vp(a["dw"]), vp(a["ws"]), a["wsb"],
+                                      a["stream"])
+
+    for call in (train, bwd):
+        assert call(B=0) == da.OK and call(N=0) == da.OK                    # nothing to do
+        assert call(ind=da.F32) == da.ERR_UNSUPPORTED                       # tensor-core path only
+        assert call(d=128, q1=_tensor(sn=128), q2=_tensor(sn=128), k1=_tensor(sn=128),
+                    k2=_tensor(sn=128), Dv=256, v=_tensor(sn=256)) == da.ERR_UNSUPPORTED
+        assert call(saved=None) == da.ERR_INVALID_ARG
+        assert call(saved=0x50010) == da.ERR_INVALID_ARG                    # not 256-byte aligned
+        assert call(savedb=nbytes - 1) == da.ERR_INVALID_ARG
+        assert call(lam=float("nan")) == da.ERR_INVALID_ARG
+    assert train(out=0x20004) == da.ERR_INVALID_ARG
+    assert bwd(dy=None) == da.ERR_INVALID_ARG
+
+
 def test_host_lambda_backward_matches_oracle(lib):
     r = np.random.default_rng(3)
     vecs = [(0.2 * r.standard_normal(64)).astype(np.float32) for _ in range(4)]

@@ -208,3 +208,81 @@ def test_backward_prefill_workload_sampled_heads():
     bounds = _bounds(w.d, w.Dv, t["q1"].dtype)
     _check(g, ref, "prefill workload", heads=heads, bounds=bounds)
     _check_sums(g, ref, bounds, t, dy, lam, lam_init, eps=w.eps)
+
+
+@pytest.mark.parametrize("B,H,N,causal,dtype,weight", [
+    (1, 1, 1, True, torch.bfloat16, False),
+    (1, 3, 130, True, torch.bfloat16, True),
+    (2, 2, 300, False, torch.float16, False),
+    (1, 2, 513, True, torch.float16, True),
+])
+def test_training_pair(B, H, N, causal, dtype, weight):
+    """diffattn_fwd_train returns diffattn_fwd's output bit for bit. The backward from its saved
+    state meets the oracle with the tensor-core path's bars and agrees with the recomputing
+    backward to 1e-3 relative RMS per gradient (bf16; 2e-4 fp16): the same operands and
+    products, only the fp32 order of the per-row sums differs (and with it, rarely, which way
+    an element of dO rounds to the operand type)."""
+    g0 = torch.Generator().manual_seed(B * 100 + N)
+    t = {k: torch.randn(B, H, N, 128 if k == "v" else 64, generator=g0).to(dtype) for k in NAMES}
+    dy = torch.randn(B, N, H, 128, generator=g0).to(dtype)
+    dev = {k: v.cuda() for k, v in t.items()}
+    nw = torch.linspace(0.5, 1.5, 128) if weight else None
+    nwd = None if nw is None else nw.cuda()
+    lam, lam_init = 0.58, 0.35
+    saved = None
+    for out_dtype in (torch.float32, dtype):
+        ref = da.diffattn_fwd(*(dev[k] for k in NAMES), lam, lam_init, norm_weight=nwd, causal=causal,
+                              out_dtype=out_dtype)
+        out, saved = da.diffattn_fwd_train(*(dev[k] for k in NAMES), lam, lam_init, norm_weight=nwd, causal=causal,
+                                           out_dtype=out_dtype, saved=saved)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"training forward output, {out_dtype}"
+    kw = dict(norm_weight=nwd, causal=causal, want_dnorm_weight=True)
+    a = da.diffattn_bwd(*(dev[k] for k in NAMES), dy.cuda(), lam, lam_init, **kw)
+    a = {k: v.clone() for k, v in a.items()}
+    ws = da.workspace(da.bwd_workspace_bytes(B, H, N, 64, 128))
+    g = da.diffattn_bwd(*(dev[k] for k in NAMES), dy.cuda(), lam, lam_init, saved=saved, ws=ws, **kw)
+    torch.cuda.synchronize()
+    assert da.read_error(ws) == 0
+    ref = orc.diffattn_bwd(*(t[k] for k in NAMES), dy, lam, lam_init, 1e-5, causal=causal,
+                           weight=None if nw is None else nw.numpy())
+    bounds = _bounds(64, 128, dtype)
+    _check(g, ref, f"from saved state B{B} H{H} N{N}", bounds=bounds)
+    _check_sums(g, ref, bounds, t, dy, lam, lam_init, causal=causal, weight=None if nw is None else nw.numpy())
+    tol = 1e-3 if dtype == torch.bfloat16 else 2e-4
+    for k in GRADS + ("dw",):
+        x, y = g[k].double(), a[k].double()
+        rr = float((x - y).norm() / y.norm().clamp_min(1e-30))
+        assert rr <= tol or float((x - y).abs().max()) <= 1e-6, f"{k}: saved vs recompute rel-RMS {rr:.2e}"
+
+
+def test_training_forward_saved_state_against_the_definition():
+    """The saved state pinned to the definition, independently of the backward: per map,
+    O_m / sum_m = softmax_m V (the map's own attention output, float64), and
+    max_m + log2(sum_m) = log2 sum_j exp2(S_ij log2(e) / sqrt(d)) (the row's log-sum-exp in
+    base 2 of the scaled scores). P enters the PV product rounded to bf16, so the first is
+    held to the forward's bf16 bar; the second only sees fp32 sums and exp2: 1e-4 absolute."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    B, H, N = 1, 2, 300
+    t = gi.prefill_inputs(w, B=B, H=H, N=N)
+    _, saved = da.diffattn_fwd_train(*(t[k].cuda() for k in NAMES), 0.5, 0.3, w.eps)
+    torch.cuda.synchronize()
+    rows = B * H * N
+    obytes = 2 * rows * w.Dv * 4
+    o = saved[:obytes].view(torch.float32).view(2, B, H, N, w.Dv).double().cpu().numpy()
+    off = (obytes + 255) // 256 * 256
+    ml = saved[off:off + rows * 16].view(torch.float32).view(B, H, N, 4).double().cpu().numpy()
+    allowed = orc.causal_allowed(np.arange(N), N)
+    for h in range(H):
+        v = t["v"][0, h].double().numpy()
+        for m, (qn, kn) in enumerate((("q1", "k1"), ("q2", "k2"))):
+            s = t[qn][0, h].double().numpy() @ t[kn][0, h].double().numpy().T / np.sqrt(w.d)
+            ref_a = orc.masked_softmax_rows(s, allowed) @ v
+            got_a = o[m, 0, h] / ml[0, h, :, 2 * m + 1][:, None]
+            rr = np.linalg.norm(got_a - ref_a) / np.linalg.norm(ref_a)
+            assert rr <= 3e-3, f"head {h} map {m + 1}: O/sum rel-RMS {rr:.2e}"
+            x = np.where(allowed, s, -np.inf) * np.log2(np.e)
+            mx = x.max(axis=1)
+            ref_l = mx + np.log2(np.exp2(x - mx[:, None]).sum(axis=1))
+            got_l = ml[0, h, :, 2 * m] + np.log2(ml[0, h, :, 2 * m + 1])
+            assert np.abs(got_l - ref_l).max() <= 1e-4, f"head {h} map {m + 1}: log-sum-exp"
