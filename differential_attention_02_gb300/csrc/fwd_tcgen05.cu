@@ -1236,7 +1236,8 @@ cudaError_t launch_persist_t(const FwdParams& p, cudaStream_t stream) {
 // HBM-bound (~1.3 KB per row): one warp per row, four columns per lane, warp
 // butterflies for the row sums; one CTA (8 warps) per 128-row query tile, whose
 // rows its warps take in a fixed order, so the per-CTA partials of dlambda and
-// of the gain's gradient are indexed and summed like the forward's.
+// of the gain's gradient are indexed and summed like the forward's. At most 64
+// registers, so four CTAs share an SM (45 us vs 48 us at three).
 constexpr int kSavedThreads = 256;
 
 __device__ __forceinline__ float warp_allsum(float v) {
@@ -1246,7 +1247,7 @@ __device__ __forceinline__ float warp_allsum(float v) {
 }
 
 template <bool F16>
-__global__ void __launch_bounds__(kSavedThreads) bwd_prep_saved_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kSavedThreads, 4) bwd_prep_saved_kernel(const __grid_constant__ FwdParams p) {
     constexpr int DV = 128, kWarps = kSavedThreads / 32;
     using T16x2 = typename std::conditional<F16, __half2, __nv_bfloat162>::type;
     __shared__ float wsum[kWarps][DV];
