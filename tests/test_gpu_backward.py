@@ -286,3 +286,25 @@ def test_training_forward_saved_state_against_the_definition():
             ref_l = mx + np.log2(np.exp2(x - mx[:, None]).sum(axis=1))
             got_l = ml[0, h, :, 2 * m] + np.log2(ml[0, h, :, 2 * m + 1])
             assert np.abs(got_l - ref_l).max() <= 1e-4, f"head {h} map {m + 1}: log-sum-exp"
+
+
+def test_training_pair_prefill_workload_sampled_heads():
+    """The B=4, H=16, N=2048 prefill workload through the training pair: every gradient of
+    three heads against the oracle, and dlambda, dw over all 64 heads."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    t = gi.prefill_inputs(w)
+    dy = gi.output_grad(w)
+    lv = gi.lambda_vectors(w)
+    lam, lam_init = orc.reparam_lambda(lv["lq1"], lv["lk1"], lv["lq2"], lv["lk2"], w.layer)
+    dev = {k: v.cuda() for k, v in t.items()}
+    _, saved = da.diffattn_fwd_train(*(dev[k] for k in NAMES), lam, lam_init, w.eps, out_dtype=torch.bfloat16)
+    ws = da.workspace(da.bwd_workspace_bytes(w.B, w.H, w.N, w.d, w.Dv))
+    g = da.diffattn_bwd(*(dev[k] for k in NAMES), dy.cuda(), lam, lam_init, w.eps, want_dnorm_weight=True, ws=ws,
+                        saved=saved)
+    torch.cuda.synchronize()
+    assert da.read_error(ws) == 0
+    heads = [(0, 0), (1, 7), (3, 15)]
+    ref = orc.diffattn_bwd(*(t[k] for k in NAMES), dy, lam, lam_init, w.eps)
+    bounds = _bounds(w.d, w.Dv, t["q1"].dtype)
+    _check(g, ref, "prefill workload from the saved state", heads=heads, bounds=bounds)
+    _check_sums(g, ref, bounds, t, dy, lam, lam_init, eps=w.eps)

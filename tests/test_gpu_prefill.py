@@ -115,12 +115,23 @@ def test_f16_output_is_the_rounded_f32_output(d, Dv, in_dtype):
     (1, 4, 3072, True, torch.bfloat16),   # smallest N of the per-tile form
 ])
 def test_16bit_output_forms(B, H, N, causal, out_dtype):
+    _check_16bit_output_forms(B, H, N, causal, out_dtype, torch.bfloat16)
+
+
+@pytest.mark.parametrize("B,H,N,causal", [(4, 16, 300, True), (2, 8, 1000, False)])
+def test_16bit_output_forms_fp16_operands(B, H, N, causal):
+    """fp16 operands through the persistent kernel (fp16 output) against the per-tile kernel's
+    fp32 output, and the oracle."""
+    _check_16bit_output_forms(B, H, N, causal, torch.float16, torch.float16)
+
+
+def _check_16bit_output_forms(B, H, N, causal, out_dtype, in_dtype):
     """16-bit outputs of short sequences come from the persistent kernel (one CTA per SM
     walking query tiles), fp32 outputs from the per-tile kernel; both compute the same fp32
     values, so the 16-bit output is exactly the fp32 output rounded. Small cases also meet
     the oracle."""
     w = gi.WORKLOADS["prefill_bf16"]
-    t = gi.prefill_inputs(w, B=B, H=H, N=N)
+    t = {k: v.to(in_dtype) for k, v in gi.prefill_inputs(w, B=B, H=H, N=N).items()}
     lam, lam_init = _lam(w)
     nw = torch.linspace(0.5, 1.5, w.Dv).cuda() if N == 640 else None
     out32 = _run(t, lam, lam_init, w.eps, causal=causal, norm_weight=nw)
