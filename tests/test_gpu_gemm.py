@@ -17,7 +17,11 @@ def _lib():
     da.load_library()
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 128), (200, 264, 72), (1, 8, 8), (1000, 2048, 2048)])
+# More tiles than SMs, so the persistent CTAs take a second round: (2500, 2048): 160 tiles of
+# 128 x 256 with ragged last rows; (2304, 2112): 162 tiles, the last tile column partial;
+# (3968, 2048): 248 tiles.
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 128), (200, 264, 72), (1, 8, 8), (1000, 2048, 2048),
+                                   (2500, 2048, 512), (2304, 2112, 256), (3968, 2048, 256)])
 def test_gemm_against_float64(M, N, K):
     g = torch.Generator().manual_seed(M + N + K)
     a = torch.randn(M, K, generator=g).to(torch.bfloat16)
@@ -65,10 +69,12 @@ def _fp32_accum_bar(ref, K):
 
 
 @pytest.mark.parametrize("M,N,K,r_dtype", [(200, 512, 72, torch.float32), (1, 256, 8, torch.bfloat16),
-                                           (1000, 2048, 512, torch.float16), (384, 768, 2048, torch.float32)])
+                                           (1000, 2048, 512, torch.float16), (384, 768, 2048, torch.float32),
+                                           (2500, 2048, 256, torch.float16)])
 def test_gemm_residual_against_float64(M, N, K, r_dtype):
     """C = A W + R (fp32), its 16-bit copy C * gain (fp16 and bf16) and the per-256-column row
-    sums of C^2, each against float64 on the same inputs."""
+    sums of C^2, each against float64 on the same inputs (the last case has more tiles than
+    SMs)."""
     g = torch.Generator().manual_seed(M + 7 * N + K)
     a = torch.randn(M, K, generator=g).half()
     w = (torch.randn(K, N, generator=g) / K ** 0.5).half()
