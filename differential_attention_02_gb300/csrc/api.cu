@@ -422,6 +422,31 @@ diffattn_status diffattn_bwd_workspace_size(int B, int H, int N, int d, int Dv, 
 namespace {
 // diffattn_bwd, and with `saved` set the backward from a training forward's saved
 // state (tensor-core path only; the caller has checked the saved buffer).
+// One non-blocking side stream and a fork/join event pair per device, made on first
+// use and kept for the life of the process. The mutex orders concurrent callers'
+// fork, launches and join on the shared stream.
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream() {
+    static std::mutex init_mu;
+    static SideStream sides[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(init_mu);
+    SideStream& s = sides[dev];
+    if (s.stream == nullptr) {
+        if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    }
+    return &s;
+}
+
 diffattn_status bwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
                          diffattn_tensor v, const void* dy, const float* norm_weight, int B, int H, int N, int d, int Dv,
                          int causal, float lambda, float lambda_init, float eps, int in_dtype, float* dq1, float* dq2,
@@ -510,8 +535,21 @@ diffattn_status bwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor
         } else {
             e = launch_bwd_prep(f, st);
         }
-        if (e == cudaSuccess) e = launch_bwd_tc(t, st);
-        if (e == cudaSuccess) e = launch_bwd_reduce(p, (int64_t)((N + kFwdBM - 1) / kFwdBM) * B * H, st);
+        if (e != cudaSuccess) return cuda_status(e);
+        // The key-side kernel stays on the caller's stream; the query-side kernel and
+        // the reduction (both need only the preparation) go to a side stream forked
+        // after the preparation and joined back before return, so their tails overlap.
+        SideStream* side = side_stream();
+        if (side == nullptr) return DIFFATTN_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(side->mu);
+        if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess)
+            return cuda_status(e);
+        e = launch_bwd_tc(t, st, side->stream);
+        if (e == cudaSuccess) e = launch_bwd_reduce(p, (int64_t)((N + kFwdBM - 1) / kFwdBM) * B * H, side->stream);
+        const cudaError_t rj = cudaEventRecord(side->join, side->stream);
+        const cudaError_t wj = cudaStreamWaitEvent(st, side->join, 0);
+        if (e == cudaSuccess) e = rj != cudaSuccess ? rj : wj;
         return cuda_status(e);
     }
     p.q1 = q1.ptr; p.q2 = q2.ptr; p.k1 = k1.ptr; p.k2 = k2.ptr; p.v = v.ptr;

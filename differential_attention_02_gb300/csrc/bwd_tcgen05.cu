@@ -27,8 +27,6 @@
 
 #include <type_traits>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "kernels.h"
 
@@ -650,7 +648,7 @@ cudaError_t setup(K kernel, size_t smem) {
 
 bool bwd_tc_supported(int d, int Dv, int in_dtype) { return d == kD && Dv == kDV && (in_dtype == 1 || in_dtype == 2); }
 
-cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream) {
+cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t key_stream, cudaStream_t query_stream) {
     if (p.d != kD || p.Dv != kDV) return cudaErrorInvalidValue;
     const bool f16 = p.in_f16 != 0;
     cudaError_t e;
@@ -665,37 +663,14 @@ cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream) {
     }
     const int n_tiles = (p.N + BM - 1) / BM;
     const int grid = n_tiles * p.B * p.H;
-    // The key side and the query side read only the preparation's outputs: the query side
-    // runs on a library stream forked from `stream` (event) and joined back (event), so each
-    // kernel's last partial wave overlaps the other's work (backward step 0.443 -> 0.436 ms).
-    // The fork/join is a plain event pattern, so the sequence can also be captured into a
-    // graph. A mutex serialises the enqueue, since the side stream and events are shared.
-    static std::mutex mu;
-    static cudaStream_t side[64];
-    static cudaEvent_t fork[64], join[64];
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (side[dev] == nullptr) {
-        if ((e = cudaStreamCreateWithFlags(&side[dev], cudaStreamNonBlocking)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&fork[dev], cudaEventDisableTiming)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&join[dev], cudaEventDisableTiming)) != cudaSuccess)
-            return e;
-    }
-    if ((e = cudaEventRecord(fork[dev], stream)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(side[dev], fork[dev], 0)) != cudaSuccess)
-        return e;
     if (f16) {
-        bwd_dkdv_kernel<true><<<grid, kThreads, dkdv::kSmem, stream>>>(p);
-        bwd_dq_kernel<true><<<grid, kThreads, dq::kSmem, side[dev]>>>(p);
+        bwd_dkdv_kernel<true><<<grid, kThreads, dkdv::kSmem, key_stream>>>(p);
+        bwd_dq_kernel<true><<<grid, kThreads, dq::kSmem, query_stream>>>(p);
     } else {
-        bwd_dkdv_kernel<false><<<grid, kThreads, dkdv::kSmem, stream>>>(p);
-        bwd_dq_kernel<false><<<grid, kThreads, dq::kSmem, side[dev]>>>(p);
+        bwd_dkdv_kernel<false><<<grid, kThreads, dkdv::kSmem, key_stream>>>(p);
+        bwd_dq_kernel<false><<<grid, kThreads, dq::kSmem, query_stream>>>(p);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(join[dev], side[dev])) != cudaSuccess) return e;
-    return cudaStreamWaitEvent(stream, join[dev], 0);
+    return cudaGetLastError();
 }
 
 }  // namespace da

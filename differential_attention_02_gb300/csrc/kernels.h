@@ -61,7 +61,7 @@ struct BwdTcParams {
     int32_t* err;
 };
 bool bwd_tc_supported(int d, int Dv, int in_dtype);  // in_dtype 1 bf16, 2 fp16
-cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t key_stream, cudaStream_t query_stream);  // key side, query side
 
 // bf16 split-KV decode (+ merge).
 struct DecodeParams {

@@ -350,6 +350,11 @@ diffattn_status diffattn_kv_append_paged_fp8(const void* k1_new, const void* k2_
  *   otherwise (f32 inputs, other widths): fp32 arithmetic on the CUDA cores.
  * Results do not depend on scheduling (no atomics): every gradient row is
  * written by one CTA and the partial sums are added in a fixed order.
+ * Streams (tensor-core path): the query-side kernel and the reduction run on a
+ * side stream the library owns (one per device, created on first use), forked
+ * from `stream` after the preparation and joined back into it before the call
+ * returns, so work enqueued on `stream` afterwards sees every output. Concurrent
+ * calls from several host threads are serialised around the shared side stream.
  * B, H or N equal to 0: DIFFATTN_OK.
  * workspace: diffattn_bwd_workspace_size() bytes, 256-byte aligned.
  */
