@@ -391,6 +391,31 @@ __device__ __forceinline__ void mma_kmajor_mn(uint32_t d_tmem, uint64_t a_desc, 
                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// 16 lanes x 256 bits, four times along the columns: thread t gets lanes t/4 and t/4 + 8 of
+// the addressed 16, columns 2(t%4) and 2(t%4)+1 of each 8-column block (registers
+// 4i + {0, 1} from lane t/4, 4i + {2, 3} from lane t/4 + 8, block i).
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Shared-space load and store by 32-bit shared address (ld.shared / st.shared rather than
+// generic accesses through a pointer whose address space the compiler cannot see).
+__device__ __forceinline__ float4 lds_f4(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+
 template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdTcParams p) {
     using namespace dkdv;
@@ -529,61 +554,83 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     // ---------------------------------------------------------------- elementwise
     setmaxnreg_inc<kRegsMathKV>();
     const int g = warp >> 2, lg = warp & 3;
-    const int r = lg * 32 + lane;  // key row within the tile
+    const int r = lg * 32 + lane;  // key row of this thread in the epilogue
     const int key = k0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
     const float sl2 = p.scale_log2, lam = p.lambda;
     constexpr int kHQ = kSQ / 2;  // queries per group and step
-    // This thread's row of each result tile: 128 bytes, 16-byte chunk c at c ^ (r % 8).
-    uint8_t* prow = smem + kOffP + r * 128;
+    // In the step loop a warp reads its 32 lanes x 32 query columns with the 16x256b shape:
+    // thread (tr, tc) = (lane / 4, lane % 4) holds key rows lg*32 + 16h + 8a + tr (h, a in
+    // {0, 1}) and the group's query columns 8i + 2tc + e (i in 0..3, e in {0, 1}), register
+    // 4i + 2a + e of the load at lane offset 16h. It needs the statistics of 8 queries, where
+    // a thread holding a whole key row would need all 32 (they are broadcast reads).
+    const int tr = lane >> 2, tc = lane & 3;
+    // Result tiles: row R at R*128 bytes, 16-byte chunk c at c ^ (R % 8); R % 8 = tr here.
+    const uint32_t pbase = smem_u32(smem + kOffP) + (uint32_t)((lg * 32 + tr) * 128 + tc * 4);
     bool ok = true;
     for (int t = 0; ok && t < nsteps; ++t) {
         const int s = t % kStages;
         ok = mbar_wait_warp(&bars->s_full, t & 1, abort_flag, p.err, 0xF0);
         if (!ok) break;
         tc_fence_after();
-        uint32_t s1[kHQ], s2[kHQ], a[kHQ];
-        tmem_ld32(lane_base + kColS1 + g * kHQ, s1);
-        tmem_ld32(lane_base + kColS2 + g * kHQ, s2);
-        tmem_ld32(lane_base + kColA + g * kHQ, a);
+        uint32_t s1[2][16], s2[2][16], ga[2][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t lb = lane_base + ((uint32_t)(16 * h) << 16) + g * kHQ;
+            tmem_ld_16x256b_x4(lb + kColS1, s1[h]);
+            tmem_ld_16x256b_x4(lb + kColS2, s2[h]);
+            tmem_ld_16x256b_x4(lb + kColA, ga[h]);
+        }
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free);
 
-        const float4* stats = reinterpret_cast<const float4*>(stages + s * kStageBytes + 2 * kQBytes + kOBytes);
+        // L1, L2, D1, D2 of the thread's 8 queries
+        const uint32_t stats = smem_u32(stages + s * kStageBytes + 2 * kQBytes + kOBytes) + (g * kHQ + 2 * tc) * 16;
+        float4 st[4][2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) st[i][e] = lds_f4(stats + (8 * i + e) * 16);
         const int qbase = qs0 + t * kSQ + g * kHQ;  // first query of this group's columns
-        // Every (query, key) pair of the group visible: no masks (warp-uniform).
-        const bool full = (!p.causal || qbase >= k0 + BM - 1) && qbase + kHQ <= p.N;
-        uint32_t pa[kHQ / 2], p1[kHQ / 2], p2[kHQ / 2];
+        // Every (query, key) pair of the warp visible: no masks (warp-uniform).
+        const bool full = (!p.causal || qbase >= k0 + lg * 32 + 31) && qbase + kHQ <= p.N;
+        uint32_t pa[2][2][4], p1[2][2][4], p2[2][2][4];
         auto elementwise = [&](auto masked) {
 #pragma unroll
-            for (int i = 0; i < kHQ; i += 2) {
-                float va[2], v1[2], v2[2];
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int q = qbase + i + k;
-                    const float4 st = stats[g * kHQ + i + k];  // L1, L2, D1, D2 of query q (broadcast read)
-                    float e1 = fast_exp2(fmaf(__uint_as_float(s1[i + k]), sl2, -st.x));
-                    float e2 = fast_exp2(fmaf(__uint_as_float(s2[i + k]), sl2, -st.y));
-                    const float da = __uint_as_float(a[i + k]);
-                    float d1 = da - st.z, d2 = fmaf(-lam, da, -st.w);
-                    if constexpr (decltype(masked)::value) {
-                        // a query past N reads another row's statistics: every result is zeroed
-                        const bool vis = q < p.N && (!p.causal || key <= q);
-                        e1 = vis ? e1 : 0.f;
-                        e2 = vis ? e2 : 0.f;
-                        d1 = vis ? d1 : 0.f;
-                        d2 = vis ? d2 : 0.f;
+                for (int ar = 0; ar < 2; ++ar)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float va[2], v1[2], v2[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int reg = 4 * i + 2 * ar + e;
+                            const float4 q4 = st[i][e];
+                            float e1 = fast_exp2(fmaf(__uint_as_float(s1[h][reg]), sl2, -q4.x));
+                            float e2 = fast_exp2(fmaf(__uint_as_float(s2[h][reg]), sl2, -q4.y));
+                            const float da = __uint_as_float(ga[h][reg]);
+                            float d1 = da - q4.z, d2 = fmaf(-lam, da, -q4.w);
+                            if constexpr (decltype(masked)::value) {
+                                // a query past N reads another row's statistics: every result is zeroed
+                                const int q = qbase + 8 * i + 2 * tc + e;
+                                const int kr = k0 + lg * 32 + 16 * h + 8 * ar + tr;
+                                const bool vis = q < p.N && (!p.causal || kr <= q);
+                                e1 = vis ? e1 : 0.f;
+                                e2 = vis ? e2 : 0.f;
+                                d1 = vis ? d1 : 0.f;
+                                d2 = vis ? d2 : 0.f;
+                            }
+                            va[e] = fmaf(-lam, e2, e1);
+                            v1[e] = e1 * d1;
+                            v2[e] = e2 * d2;
+                        }
+                        pa[h][ar][i] = pack_p<F16>(va[0], va[1]);
+                        p1[h][ar][i] = pack_p<F16>(v1[0], v1[1]);
+                        p2[h][ar][i] = pack_p<F16>(v2[0], v2[1]);
                     }
-                    va[k] = fmaf(-lam, e2, e1);
-                    v1[k] = e1 * d1;
-                    v2[k] = e2 * d2;
-                }
-                pa[i / 2] = pack_p<F16>(va[0], va[1]);
-                p1[i / 2] = pack_p<F16>(v1[0], v1[1]);
-                p2[i / 2] = pack_p<F16>(v2[0], v2[1]);
-            }
         };
         if (full) elementwise(std::false_type{});
         else elementwise(std::true_type{});
@@ -591,16 +638,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         // the previous step's products have read the tiles this step overwrites
         if (t > 0) ok = mbar_wait_warp(&bars->p_empty, (t - 1) & 1, abort_flag, p.err, 0xF2);
         if (!ok) break;
+        // Per store instruction the warp writes 8 rows x 16 bytes into 8 distinct chunk
+        // positions ((4g + i) ^ tr): one wavefront, no bank conflict.
 #pragma unroll
-        for (int j = 0; j < kHQ / 8; ++j) {
-            const int c = g * (kHQ / 8) + j;  // 16-byte chunk: queries 8c .. 8c+7 of the step
-            const uint32_t off = (uint32_t)((c ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(prow + off) = make_uint4(pa[4 * j], pa[4 * j + 1], pa[4 * j + 2], pa[4 * j + 3]);
-            *reinterpret_cast<uint4*>(prow + kPBytes + off) =
-                make_uint4(p1[4 * j], p1[4 * j + 1], p1[4 * j + 2], p1[4 * j + 3]);
-            *reinterpret_cast<uint4*>(prow + 2 * kPBytes + off) =
-                make_uint4(p2[4 * j], p2[4 * j + 1], p2[4 * j + 2], p2[4 * j + 3]);
-        }
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int ar = 0; ar < 2; ++ar)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t off = (uint32_t)((16 * h + 8 * ar) * 128 + (((4 * g + i) ^ tr) << 4));
+                    sts_u32(pbase + off, pa[h][ar][i]);
+                    sts_u32(pbase + kPBytes + off, p1[h][ar][i]);
+                    sts_u32(pbase + 2 * kPBytes + off, p2[h][ar][i]);
+                }
         fence_proxy_async_shared();  // the tensor core reads these through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
