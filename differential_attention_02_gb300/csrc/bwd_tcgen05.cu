@@ -356,6 +356,7 @@ constexpr int kStageBytes = 2 * kQBytes + kOBytes + 1024;  // + stats, padded to
 constexpr int kOffK1 = 0, kOffK2 = kKBytes, kOffV = 2 * kKBytes, kOffP = 2 * kKBytes + kVBytes;
 constexpr int kOffStages = kOffP + 3 * kPBytes;
 constexpr int kOffBar = kOffStages + kStages * kStageBytes;
+constexpr int kEpiBox = 32 * 4 * BM;          // epilogue staging box: 32 fp32 columns x 128 rows, 16 KB
 constexpr size_t kSmem = 1024 + (size_t)kOffBar + 256;
 static_assert(kSmem <= 232448, "shared memory budget");
 static_assert(kOffP % 1024 == 0 && kOffStages % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled tiles");
@@ -414,6 +415,9 @@ __device__ __forceinline__ float4 lds_f4(uint32_t saddr) {
 }
 __device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 template <bool F16>
@@ -656,14 +660,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&bars->p_full);
     }
     // ---------------------------------------------------------------- epilogue: dV, dK rows
+    // The rows are staged in the idle result tiles and ring (every product that read them has
+    // completed at acc_done) as 128-byte-swizzled boxes of 32 fp32 columns x 128 rows (dV
+    // boxes 0..3, dK1 4..5, dK2 6..7) and written by TMA stores, which clip rows past N.
+    // Group 0 stages dV columns 0..63 and dK1, group 1 dV columns 64..127 and dK2.
     if (ok && nsteps > 0) ok = mbar_wait_warp(&bars->acc_done, 0, abort_flag, p.err, 0xF1);
     tc_fence_after();
-    const int64_t row = ((int64_t)b * p.H + h) * p.N + key;
-    const bool store = ok && key < p.N;
+    static_assert(kOffP + 8 * kEpiBox <= kOffBar, "staging fits below the barriers");
     {
-        // group 0: dV columns 0..63 and dK1; group 1: dV columns 64..127 and dK2.
-        float* dvrow = p.dv + row * kDV + g * 64;
-        float* dkrow = (g ? p.dk2 : p.dk1) + row * kD;
+        const uint32_t stage0 = smem_u32(smem + kOffP) + (uint32_t)(r * 128);
+        const float scale = p.scale;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             uint32_t v[32], k[32];
@@ -672,18 +678,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 tmem_ld32(lane_base + (g ? kColK2 : kColK1) + c * 32, k);
                 tmem_ld_wait();
             }
-            if (store) {
+            const uint32_t bv = stage0 + (uint32_t)((2 * g + c) * kEpiBox);
+            const uint32_t bk = stage0 + (uint32_t)((4 + 2 * g + c) * kEpiBox);
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    *reinterpret_cast<float4*>(dvrow + c * 32 + i) =
-                        make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                                    __uint_as_float(v[i + 3]));
-                    *reinterpret_cast<float4*>(dkrow + c * 32 + i) =
-                        make_float4(__uint_as_float(k[i]) * p.scale, __uint_as_float(k[i + 1]) * p.scale,
-                                    __uint_as_float(k[i + 2]) * p.scale, __uint_as_float(k[i + 3]) * p.scale);
-                }
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t off = (uint32_t)((j ^ (r & 7)) << 4);
+                sts_v4(bv + off, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                sts_v4(bk + off, __float_as_uint(__uint_as_float(k[4 * j]) * scale),
+                       __float_as_uint(__uint_as_float(k[4 * j + 1]) * scale),
+                       __float_as_uint(__uint_as_float(k[4 * j + 2]) * scale),
+                       __float_as_uint(__uint_as_float(k[4 * j + 3]) * scale));
             }
         }
+    }
+    fence_proxy_async_shared();  // the TMA stores read the boxes through the async proxy
+    named_bar_sync(3, 256);
+    if (threadIdx.x == 0 && ok && *abort_flag == 0 && k0 < p.N) {
+        uint8_t* box = smem + kOffP;
+        for (int x = 0; x < 4; ++x) tma_store_3d(&p.tm_dv, box + x * kEpiBox, x * 32, k0, bh);
+        for (int x = 0; x < 2; ++x) tma_store_3d(&p.tm_dk1, box + (4 + x) * kEpiBox, x * 32, k0, bh);
+        for (int x = 0; x < 2; ++x) tma_store_3d(&p.tm_dk2, box + (6 + x) * kEpiBox, x * 32, k0, bh);
+        tma_store_commit();
+        tma_store_wait_read();  // the boxes stay valid until the copies have read them
     }
     tc_fence_before();
     named_bar_sync(2, kThreads);
