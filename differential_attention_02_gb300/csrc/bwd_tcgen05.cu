@@ -73,6 +73,34 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uin
 // warp 9 issues the MMAs. Per key tile j the issue order is
 //   dA(j), S1(j), S2(j)  ...  dQ1 += dS1(j) K1(j), dA(j+1), S1(j+1), dQ2 += dS2(j) K2(j), S2(j+1)
 // so one group's elementwise work overlaps the other group's products.
+// 16 lanes x 256 bits, four times along the columns: thread t gets lanes t/4 and t/4 + 8 of
+// the addressed 16, columns 2(t%4) and 2(t%4)+1 of each 8-column block (registers
+// 4i + {0, 1} from lane t/4, 4i + {2, 3} from lane t/4 + 8, block i).
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Shared-space load and store by 32-bit shared address (ld.shared / st.shared rather than
+// generic accesses through a pointer whose address space the compiler cannot see).
+__device__ __forceinline__ float4 lds_f4(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 namespace dq {
 constexpr int kStages = 2;
 constexpr int kQBytes = BM * kD * 2;           // 16 KB
@@ -85,6 +113,8 @@ constexpr int kOffBar = kOffStages + kStages * kStageBytes;
 constexpr size_t kSmem = 1024 + (size_t)kOffBar + 256;
 static_assert(kSmem <= 232448, "shared memory budget");
 constexpr uint32_t kColS = 0, kColA = 256, kColQ = 384;
+constexpr int kEpiBox = 32 * 4 * BM;  // epilogue staging box: 32 fp32 columns x 128 rows, 16 KB
+static_assert(4 * kEpiBox <= kOffStages, "dQ1, dQ2 staging fits in the Q1, Q2, dO tiles");
 
 struct Bars {
     uint64_t q_full;
@@ -305,26 +335,38 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         if (lane == 0) mbar_arrive(&bars->ds_full[g]);
     }
     // ---------------------------------------------------------------- epilogue: dQ_g rows
+    // Staged in the idle Q1/Q2/dO tiles (every product that read them has completed at
+    // dq_done) as 128-byte-swizzled boxes of 32 fp32 columns x 128 rows (dQ1 boxes 0, 1;
+    // dQ2 boxes 2, 3) and written by TMA stores, which clip rows past N.
     if (ok) ok = mbar_wait_warp(&bars->dq_done, 0, abort_flag, p.err, 0xD2);
     tc_fence_after();
-    // TMEM is read by whole warps (ok is the same in every lane); only the stores
-    // depend on the row.
-    if (ok) {
+    {
+        const int r = lg * 32 + lane;
+        const uint32_t stage0 = smem_u32(smem) + (uint32_t)(r * 128);
         const float scale = p.scale;  // 1 / sqrt(d)
-        float* dst = (g ? p.dq2 : p.dq1) + (((int64_t)b * p.H + h) * p.N + qrow) * kD;
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
             uint32_t v[32];
-            tmem_ld32(lane_base + kColQ + g * kD + c * 32, v);
-            tmem_ld_wait();
-            if (qrow < p.N) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4*>(dst + c * 32 + i) =
-                        make_float4(__uint_as_float(v[i]) * scale, __uint_as_float(v[i + 1]) * scale,
-                                    __uint_as_float(v[i + 2]) * scale, __uint_as_float(v[i + 3]) * scale);
+            if (ok) {  // TMEM is read by whole warps (ok is the same in every lane)
+                tmem_ld32(lane_base + kColQ + g * kD + c * 32, v);
+                tmem_ld_wait();
             }
+            const uint32_t bx = stage0 + (uint32_t)((2 * g + c) * kEpiBox);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                sts_v4(bx + (uint32_t)((j ^ (r & 7)) << 4), __float_as_uint(__uint_as_float(v[4 * j]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * j + 1]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * j + 2]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * j + 3]) * scale));
         }
+    }
+    fence_proxy_async_shared();  // the TMA stores read the boxes through the async proxy
+    named_bar_sync(3, 256);
+    if (threadIdx.x == 0 && ok && *abort_flag == 0) {
+        for (int x = 0; x < 2; ++x) tma_store_3d(&p.tm_dq1, smem + x * kEpiBox, x * 32, q0, bh);
+        for (int x = 0; x < 2; ++x) tma_store_3d(&p.tm_dq2, smem + (2 + x) * kEpiBox, x * 32, q0, bh);
+        tma_store_commit();
+        tma_store_wait_read();  // the boxes stay valid until the copies have read them
     }
     tc_fence_before();
     named_bar_sync(2, kThreads);
@@ -390,34 +432,6 @@ __device__ __forceinline__ void mma_kmajor_mn(uint32_t d_tmem, uint64_t a_desc, 
     for (int kk = 0; kk < KSTEPS; ++kk)
         umma_ss(d_tmem, a_desc + (uint64_t)(kk * 2), b_desc + (uint64_t)(kk * 128), idesc,
                 (accumulate || kk > 0) ? 1u : 0u);
-}
-
-// 16 lanes x 256 bits, four times along the columns: thread t gets lanes t/4 and t/4 + 8 of
-// the addressed 16, columns 2(t%4) and 2(t%4)+1 of each 8-column block (registers
-// 4i + {0, 1} from lane t/4, 4i + {2, 3} from lane t/4 + 8, block i).
-__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t* r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
-
-// Shared-space load and store by 32-bit shared address (ld.shared / st.shared rather than
-// generic accesses through a pointer whose address space the compiler cannot see).
-__device__ __forceinline__ float4 lds_f4(uint32_t saddr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void sts_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 template <bool F16>
