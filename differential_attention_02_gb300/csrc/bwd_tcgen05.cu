@@ -21,8 +21,9 @@
 //
 // Both kernels keep S, dA and the gradient accumulators in TMEM. The products
 // whose left operand is elementwise data (dS or A, rounded to the operand type)
-// read it from TMEM in bwd_dq, like the forward's P.V, and from shared memory in
-// bwd_dkdv, where that frees the score columns for the next step's products.
+// read it from TMEM in bwd_dq, like the forward's P.V (written over the score
+// columns), and in bwd_dkdv from columns of its own (A, dS1) or shared memory (dS2),
+// so that the score columns are free for the next step's products.
 #include <math.h>
 
 #include <type_traits>
@@ -94,6 +95,14 @@ __device__ __forceinline__ float4 lds_f4(uint32_t saddr) {
                  : "memory");
     return v;
 }
+// 16 lanes x 128 bits, four times along the columns: register 2i + a goes to lane t/4 + 8a
+// of the addressed 16, column 4i + t%4.
+__device__ __forceinline__ void tmem_st_16x128b_x4(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
 }
@@ -376,10 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 // bwd_dkdv: one CTA per 128-key tile of one (b, h); query steps of 64 rows.
 // ============================================================================
 // TMEM (keys = lanes): S1^T [0,64), S2^T [64,128), dA^T [128,192) for one step's
-// 64 queries; dV [192,320), dK1 [320,384), dK2 [384,448). The elementwise warps
-// write A^T = P1 - lambda P2, dS1^T and dS2^T (operand type) to shared memory as
-// K-major 128-byte-swizzled tiles, the left operands of
-//   dV += A^T dO,  dK1 += dS1^T Q1,  dK2 += dS2^T Q2.
+// 64 queries; dV [192,320), dK1 [320,384), dK2 [384,448); A^T [448,480) and
+// dS1^T [480,512) as 16-bit pairs. The elementwise warps write A^T = P1 - lambda P2
+// and dS1^T (operand type) into those last columns and dS2^T to shared memory as a
+// K-major 128-byte-swizzled tile: the left operands of
+//   dV += A^T dO,  dK1 += dS1^T Q1  (A from TMEM),  dK2 += dS2^T Q2  (A from smem).
+// Shared memory bandwidth bounds this kernel (the tensor core's operand reads, the
+// TMA fills and the elementwise traffic), so what can live in TMEM does.
 // The score columns are free as soon as the elementwise warps have loaded them,
 // so the products of step t+1's scores run while step t's elementwise work does:
 //   S/dA(0) ... [loads of S/dA(t)] S/dA(t+1) [elementwise t, stores] dV/dK(t) ...
@@ -387,22 +399,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 // key row).
 namespace dkdv {
 constexpr int kSQ = 64;                        // queries per step
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kKBytes = BM * kD * 2;           // K tile, 16 KB
 constexpr int kVBytes = BM * kDV * 2;          // V tile, 32 KB
 constexpr int kQBytes = kSQ * kD * 2;          // Q step, 8 KB
 constexpr int kOBytes = kSQ * kDV * 2;         // dO step, 16 KB
 constexpr int kSBytes = kSQ * 16;              // stats of the step, 1 KB
-constexpr int kPBytes = BM * kSQ * 2;          // one elementwise result tile, 16 KB
+constexpr int kPBytes = BM * kSQ * 2;          // the dS2^T result tile, 16 KB
 constexpr int kStageBytes = 2 * kQBytes + kOBytes + 1024;  // + stats, padded to keep tiles 1024-aligned
 constexpr int kOffK1 = 0, kOffK2 = kKBytes, kOffV = 2 * kKBytes, kOffP = 2 * kKBytes + kVBytes;
-constexpr int kOffStages = kOffP + 3 * kPBytes;
+constexpr int kOffStages = kOffP + kPBytes;
 constexpr int kOffBar = kOffStages + kStages * kStageBytes;
 constexpr int kEpiBox = 32 * 4 * BM;          // epilogue staging box: 32 fp32 columns x 128 rows, 16 KB
 constexpr size_t kSmem = 1024 + (size_t)kOffBar + 256;
 static_assert(kSmem <= 232448, "shared memory budget");
 static_assert(kOffP % 1024 == 0 && kOffStages % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled tiles");
 constexpr uint32_t kColS1 = 0, kColS2 = 64, kColA = 128, kColV = 192, kColK1 = 320, kColK2 = 384;
+// A^T and dS1^T of the step as 16-bit pairs (the left operands of the dV and dK1 products)
+constexpr uint32_t kColPA = 448, kColP1 = 480;
 // Register split: the MMA warp's loop (two waits and two groups of products per step) needs
 // more than 56 registers; the elementwise warps need far fewer than 216.
 constexpr int kRegsMathKV = 216, kRegsOtherKV = 72;
@@ -413,7 +427,7 @@ struct Bars {
     uint64_t q_full[kStages], q_empty[kStages];
     uint64_t s_full;      // S1^T, S2^T, dA^T of the step in TMEM
     uint64_t s_free;      // every elementwise warp has loaded them (8 warps)
-    uint64_t p_full;      // A^T, dS1^T, dS2^T of the step in shared memory (8 warps)
+    uint64_t p_full;      // A^T, dS1^T of the step in TMEM and dS2^T in shared memory (8 warps)
     uint64_t p_empty;     // the products that read them completed
     uint64_t acc_done;    // the last products completed
     uint64_t drain;
@@ -508,11 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             // field's 2^14 limit for shared memory): one base plus constant offsets.
             const uint64_t dk1 = sdesc_sw128(smem_u32(smem), 16, 1024);
             const uint64_t dk2 = dk1 + (kOffK2 >> 4), dv = dk1 + (kOffV >> 4);
-            const uint64_t dpa = dk1 + (kOffP >> 4);                                // A^T, K-major
+            const uint64_t dp2 = dk1 + (kOffP >> 4);                                // dS2^T, K-major
             const uint64_t dst0 = dk1 + (kOffStages >> 4);                          // K-major step tiles
             const uint64_t dsn0 = sdesc_sw128(smem_u32(stages), kSQ * 128, 1024);   // MN-major step tiles
             constexpr uint64_t kStep = kStageBytes >> 4, kQ2 = kQBytes >> 4, kO = (2 * kQBytes) >> 4;
-            constexpr uint64_t kP = kPBytes >> 4;
             constexpr uint32_t id_s = idesc_kind_f16(BM, kSQ, 0, 0, F16);    // S^T, dA^T: 128 x 64
             constexpr uint32_t id_v = idesc_kind_f16(BM, kDV, 0, 1, F16);    // dV: 128 x 128, B MN-major
             constexpr uint32_t id_k = idesc_kind_f16(BM, kD, 0, 1, F16);     // dK: 128 x 64, B MN-major
@@ -547,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 if (!ok) break;
                 tc_fence_after();
                 if (lead) {
-                    mma_kmajor_mn<kSQ / 16>(tmem + kColV, dpa, dsn0 + st + kO, id_v, t > 0);
-                    mma_kmajor_mn<kSQ / 16>(tmem + kColK1, dpa + kP, dsn0 + st, id_k, t > 0);
-                    mma_kmajor_mn<kSQ / 16>(tmem + kColK2, dpa + 2 * kP, dsn0 + st + kQ2, id_k, t > 0);
+                    mma_tmem_a<kSQ / 16>(tmem + kColV, tmem + kColPA, dsn0 + st + kO, id_v, t > 0);
+                    mma_tmem_a<kSQ / 16>(tmem + kColK1, tmem + kColP1, dsn0 + st, id_k, t > 0);
+                    mma_kmajor_mn<kSQ / 16>(tmem + kColK2, dp2, dsn0 + st + kQ2, id_k, t > 0);
                     umma_commit(&bars->q_empty[s]);
                     umma_commit(&bars->p_empty);
                     if (!more) umma_commit(&bars->acc_done);
@@ -573,7 +586,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     setmaxnreg_inc<kRegsMathKV>();
     const int g = warp >> 2, lg = warp & 3;
     const int r = lg * 32 + lane;  // key row of this thread in the epilogue
-    const int key = k0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
     const float sl2 = p.scale_log2, lam = p.lambda;
     constexpr int kHQ = kSQ / 2;  // queries per group and step
@@ -656,8 +668,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         // the previous step's products have read the tiles this step overwrites
         if (t > 0) ok = mbar_wait_warp(&bars->p_empty, (t - 1) & 1, abort_flag, p.err, 0xF2);
         if (!ok) break;
-        // Per store instruction the warp writes 8 rows x 16 bytes into 8 distinct chunk
-        // positions ((4g + i) ^ tr): one wavefront, no bank conflict.
+        // A^T and dS1^T go to TMEM with the 16x128b shape: register 2i + a of the store at
+        // lane offset 16h is lane 16h + 8a + tr, column 4i + tc of the group's 16 (queries
+        // 8i + 2tc, +1 as one pair), which is exactly where this thread's pair belongs.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t lb = lane_base + ((uint32_t)(16 * h) << 16) + g * (kHQ / 2);
+            const uint32_t ra[8] = {pa[h][0][0], pa[h][1][0], pa[h][0][1], pa[h][1][1],
+                                    pa[h][0][2], pa[h][1][2], pa[h][0][3], pa[h][1][3]};
+            const uint32_t r1[8] = {p1[h][0][0], p1[h][1][0], p1[h][0][1], p1[h][1][1],
+                                    p1[h][0][2], p1[h][1][2], p1[h][0][3], p1[h][1][3]};
+            tmem_st_16x128b_x4(lb + kColPA, ra);
+            tmem_st_16x128b_x4(lb + kColP1, r1);
+        }
+        // dS2^T to shared memory: per store instruction the warp writes 8 rows x 16 bytes
+        // into 8 distinct chunk positions ((4g + i) ^ tr): one wavefront, no bank conflict.
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -665,11 +690,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t off = (uint32_t)((16 * h + 8 * ar) * 128 + (((4 * g + i) ^ tr) << 4));
-                    sts_u32(pbase + off, pa[h][ar][i]);
-                    sts_u32(pbase + kPBytes + off, p1[h][ar][i]);
-                    sts_u32(pbase + 2 * kPBytes + off, p2[h][ar][i]);
+                    sts_u32(pbase + off, p2[h][ar][i]);
                 }
-        fence_proxy_async_shared();  // the tensor core reads these through the async proxy
+        tmem_st_wait();
+        fence_proxy_async_shared();  // the tensor core reads the tile through the async proxy
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
     }
