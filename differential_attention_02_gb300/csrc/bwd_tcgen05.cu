@@ -73,7 +73,10 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uin
 // Warps 0..3 compute dS1 and warps 4..7 dS2 for row 32*(w%4)+lane; warp 8 loads,
 // warp 9 issues the MMAs. Per key tile j the issue order is
 //   dA(j), S1(j), S2(j)  ...  dQ1 += dS1(j) K1(j), dA(j+1), S1(j+1), dQ2 += dS2(j) K2(j), S2(j+1)
-// so one group's elementwise work overlaps the other group's products.
+// so one group's elementwise work overlaps the other group's products; each dQ_m
+// product runs in two halves of 64 keys, the first while the group computes the
+// second half's dS_m.
+
 // 16 lanes x 256 bits, four times along the columns: thread t gets lanes t/4 and t/4 + 8 of
 // the addressed 16, columns 2(t%4) and 2(t%4)+1 of each 8-column block (registers
 // 4i + {0, 1} from lane t/4, 4i + {2, 3} from lane t/4 + 8, block i).
@@ -129,7 +132,8 @@ struct Bars {
     uint64_t q_full;
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2];   // S_m(j) and dA(j) in TMEM
-    uint64_t ds_full[2];  // dS_m(j) in TMEM (4 warps each)
+    uint64_t ds_half[2];  // dS_m(j) of keys 0..63 in TMEM (4 warps each)
+    uint64_t ds_full[2];  // dS_m(j) of keys 64..127 too
     uint64_t da_free;     // every elementwise warp has read dA(j) (8 warps)
     uint64_t dq_done;     // the last dQ products completed
     uint64_t drain;
@@ -162,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(&bars->s_full[g], 1);
+            mbar_init(&bars->ds_half[g], 4);
             mbar_init(&bars->ds_full[g], 4);
         }
         mbar_init(&bars->da_free, 8);
@@ -243,7 +248,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 const int s = j % kStages, s1 = (j + 1) % kStages;
                 const bool more = j + 1 < nkv;
                 const uint64_t st = (uint64_t)s * kStep;
+                // Each map's dQ_m += dS_m K_m in two halves of four K-steps: keys 0..63 as soon
+                // as the group has written them (ds_half), while it computes keys 64..127.
+                constexpr uint64_t kHalfB = (uint64_t)(BM / 2 / 16) * 128;  // 4 K-steps of B
                 // map 1: dQ1 += dS1 K1, then dA(j+1) and S1(j+1)
+                if (!(ok = mbar_wait_warp(&bars->ds_half[0], j & 1, abort_flag, p.err, 0xCC))) break;
+                tc_fence_after();
+                if (lead) mma_tmem_a<BM / 32>(tQ1, tS1, dkn0 + st, id_q, j > 0);
+                __syncwarp();
                 ok = mbar_wait_warp(&bars->ds_full[0], j & 1, abort_flag, p.err, 0xC7);
                 if (ok && more)
                     ok = mbar_wait_warp(&bars->kv_full[s1], ((j + 1) / kStages) & 1, abort_flag, p.err, 0xC8) &&
@@ -251,15 +263,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 if (lead) {
-                    mma_tmem_a<BM / 16>(tQ1, tS1, dkn0 + st, id_q, j > 0);
+                    mma_tmem_a<BM / 32>(tQ1, tS1 + BM / 4, dkn0 + st + kHalfB, id_q, true);
                     if (more) issue_scores(s1, false);
                 }
                 __syncwarp();
                 // map 2: dQ2 += dS2 K2, release the stage, then S2(j+1)
+                if (!(ok = mbar_wait_warp(&bars->ds_half[1], j & 1, abort_flag, p.err, 0xCD))) break;
+                tc_fence_after();
+                if (lead) mma_tmem_a<BM / 32>(tQ2, tS2, dkn0 + st + kK2, id_q, j > 0);
+                __syncwarp();
                 if (!(ok = mbar_wait_warp(&bars->ds_full[1], j & 1, abort_flag, p.err, 0xCA))) break;
                 tc_fence_after();
                 if (lead) {
-                    mma_tmem_a<BM / 16>(tQ2, tS2, dkn0 + st + kK2, id_q, j > 0);
+                    mma_tmem_a<BM / 32>(tQ2, tS2 + BM / 4, dkn0 + st + kK2 + kHalfB, id_q, true);
                     umma_commit(&bars->kv_empty[s]);
                     if (more) issue_scores(s1, true);
                     else umma_commit(&bars->dq_done);
@@ -337,11 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             if (need_mask) elementwise(std::true_type{});
             else elementwise(std::false_type{});
             tmem_st32(tS + hf * 32, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(hf == 0 ? &bars->ds_half[g] : &bars->ds_full[g]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->ds_full[g]);
     }
     // ---------------------------------------------------------------- epilogue: dQ_g rows
     // Staged in the idle Q1/Q2/dO tiles (every product that read them has completed at
