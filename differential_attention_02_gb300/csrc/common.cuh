@@ -98,22 +98,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// As mbar_try_wait, but the thread may sleep up to `hint_ns` waiting for the
-// phase (it wakes as soon as the phase completes), so waiting threads stop
-// taking issue slots from the warps doing the work on the same sub-partition.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-constexpr uint32_t kSleepHintNs = 1000000;  // 1 ms per attempt; the total stays bounded below
+constexpr uint32_t kSleepHintNs = 1000000;  // suspend hint of the cluster waits: 1 ms per attempt, bounded below
 
 // Waits for the phase of `bar` with the given parity to complete.
 // Gives up when *abort becomes non-zero (another role of the CTA failed) or
@@ -124,8 +109,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
+        // try_wait without a suspend-time hint: the hardware still suspends the thread
+        // for a short while, and wakes it sooner than with a long hint (about 1% on the
+        // prefill and backward kernels, whose critical paths are chains of these waits).
         for (int i = 0; i < 8; ++i)
-            if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+            if (mbar_try_wait(bar, parity)) return true;
         if (abort != nullptr && *abort) return false;
         // Time bound, with an iteration cap as a backstop should the timer not advance.
         if (globaltimer_ns() - t0 > kWaitTimeoutNs || it > kWaitMaxIters) {
