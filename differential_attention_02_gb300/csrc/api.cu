@@ -515,10 +515,7 @@ diffattn_status bwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor
             !encode_4d(&t.tm_q1s, q1, d, N, H, B, 64, 64, sw, tdt) ||
             !encode_4d(&t.tm_q2s, q2, d, N, H, B, 64, 64, sw, tdt) ||
             !encode_4d(&t.tm_dos, dot, Dv, N, H, B, 64, 64, sw, tdt) ||
-            !encode_stats_2d(&t.tm_stats, stats, (int64_t)B * H * N) ||
-            !encode_out_3d(&t.tm_dv, dv, Dv, N, B * H, 4, 128) || !encode_out_3d(&t.tm_dk1, dk1, d, N, B * H, 4, 128) ||
-            !encode_out_3d(&t.tm_dk2, dk2, d, N, B * H, 4, 128) || !encode_out_3d(&t.tm_dq1, dq1, d, N, B * H, 4, 128) ||
-            !encode_out_3d(&t.tm_dq2, dq2, d, N, B * H, 4, 128))
+            !encode_stats_2d(&t.tm_stats, stats, (int64_t)B * H * N))
             return DIFFATTN_ERR_INVALID_ARG;
         t.stats = stats;
         t.dq1 = dq1; t.dq2 = dq2; t.dk1 = dk1; t.dk2 = dk2; t.dv = dv;

@@ -109,9 +109,6 @@ __device__ __forceinline__ void tmem_st_16x128b_x4(uint32_t taddr, const uint32_
 __device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void sts_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 namespace dq {
 constexpr int kStages = 2;
@@ -125,8 +122,6 @@ constexpr int kOffBar = kOffStages + kStages * kStageBytes;
 constexpr size_t kSmem = 1024 + (size_t)kOffBar + 256;
 static_assert(kSmem <= 232448, "shared memory budget");
 constexpr uint32_t kColS = 0, kColA = 256, kColQ = 384;
-constexpr int kEpiBox = 32 * 4 * BM;  // epilogue staging box: 32 fp32 columns x 128 rows, 16 KB
-static_assert(4 * kEpiBox <= kOffStages, "dQ1, dQ2 staging fits in the Q1, Q2, dO tiles");
 
 struct Bars {
     uint64_t q_full;
@@ -360,38 +355,38 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         }
     }
     // ---------------------------------------------------------------- epilogue: dQ_g rows
-    // Staged in the idle Q1/Q2/dO tiles (every product that read them has completed at
-    // dq_done) as 128-byte-swizzled boxes of 32 fp32 columns x 128 rows (dQ1 boxes 0, 1;
-    // dQ2 boxes 2, 3) and written by TMA stores, which clip rows past N.
+    // Read from TMEM with the 16x256b shape and stored straight from registers: per
+    // instruction a warp writes 8 rows x 32 contiguous bytes (whole 32-byte sectors).
     if (ok) ok = mbar_wait_warp(&bars->dq_done, 0, abort_flag, p.err, 0xD2);
     tc_fence_after();
     {
-        const int r = lg * 32 + lane;
-        const uint32_t stage0 = smem_u32(smem) + (uint32_t)(r * 128);
         const float scale = p.scale;  // 1 / sqrt(d)
+        const int tr = lane >> 2, tc = lane & 3;
+        float* dst = (g ? p.dq2 : p.dq1) + ((int64_t)b * p.H + h) * p.N * kD;
 #pragma unroll
         for (int c = 0; c < kD / 32; ++c) {
-            uint32_t v[32];
+            uint32_t v[2][16];
             if (ok) {  // TMEM is read by whole warps (ok is the same in every lane)
-                tmem_ld32(lane_base + kColQ + g * kD + c * 32, v);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+                    tmem_ld_16x256b_x4(lane_base + ((uint32_t)(16 * hh) << 16) + kColQ + g * kD + c * 32, v[hh]);
                 tmem_ld_wait();
             }
-            const uint32_t bx = stage0 + (uint32_t)((2 * g + c) * kEpiBox);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                sts_v4(bx + (uint32_t)((j ^ (r & 7)) << 4), __float_as_uint(__uint_as_float(v[4 * j]) * scale),
-                       __float_as_uint(__uint_as_float(v[4 * j + 1]) * scale),
-                       __float_as_uint(__uint_as_float(v[4 * j + 2]) * scale),
-                       __float_as_uint(__uint_as_float(v[4 * j + 3]) * scale));
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int ar = 0; ar < 2; ++ar) {
+                    const int qr = q0 + lg * 32 + 16 * hh + 8 * ar + tr;
+                    if (!ok || qr >= p.N) continue;
+                    float* row = dst + (int64_t)qr * kD + c * 32 + 2 * tc;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rg = 4 * i + 2 * ar;
+                        *reinterpret_cast<float2*>(row + 8 * i) =
+                            make_float2(__uint_as_float(v[hh][rg]) * scale, __uint_as_float(v[hh][rg + 1]) * scale);
+                    }
+                }
         }
-    }
-    fence_proxy_async_shared();  // the TMA stores read the boxes through the async proxy
-    named_bar_sync(3, 256);
-    if (threadIdx.x == 0 && ok && *abort_flag == 0) {
-        for (int x = 0; x < 2; ++x) tma_store_3d(&p.tm_dq1, smem + x * kEpiBox, x * 32, q0, bh);
-        for (int x = 0; x < 2; ++x) tma_store_3d(&p.tm_dq2, smem + (2 + x) * kEpiBox, x * 32, q0, bh);
-        tma_store_commit();
-        tma_store_wait_read();  // the boxes stay valid until the copies have read them
     }
     tc_fence_before();
     named_bar_sync(2, kThreads);
@@ -426,7 +421,6 @@ constexpr int kStageBytes = 2 * kQBytes + kOBytes + 1024;  // + stats, padded to
 constexpr int kOffK1 = 0, kOffK2 = kKBytes, kOffV = 2 * kKBytes, kOffP = 2 * kKBytes + kVBytes;
 constexpr int kOffStages = kOffP + kPBytes;
 constexpr int kOffBar = kOffStages + kStages * kStageBytes;
-constexpr int kEpiBox = 32 * 4 * BM;          // epilogue staging box: 32 fp32 columns x 128 rows, 16 KB
 constexpr size_t kSmem = 1024 + (size_t)kOffBar + 256;
 static_assert(kSmem <= 232448, "shared memory budget");
 static_assert(kOffP % 1024 == 0 && kOffStages % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled tiles");
@@ -715,46 +709,46 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&bars->p_full);
     }
     // ---------------------------------------------------------------- epilogue: dV, dK rows
-    // The rows are staged in the idle result tiles and ring (every product that read them has
-    // completed at acc_done) as 128-byte-swizzled boxes of 32 fp32 columns x 128 rows (dV
-    // boxes 0..3, dK1 4..5, dK2 6..7) and written by TMA stores, which clip rows past N.
-    // Group 0 stages dV columns 0..63 and dK1, group 1 dV columns 64..127 and dK2.
+    // Group 0 writes dV columns 0..63 and dK1, group 1 dV columns 64..127 and dK2, read from
+    // TMEM with the 16x256b shape and stored straight from registers: per instruction a warp
+    // writes 8 rows x 32 contiguous bytes, whole 32-byte sectors (faster than staging the
+    // rows for TMA stores, whose drain the CTA has to wait for before it exits).
     if (ok && nsteps > 0) ok = mbar_wait_warp(&bars->acc_done, 0, abort_flag, p.err, 0xF1);
     tc_fence_after();
-    static_assert(kOffP + 8 * kEpiBox <= kOffBar, "staging fits below the barriers");
     {
-        const uint32_t stage0 = smem_u32(smem + kOffP) + (uint32_t)(r * 128);
         const float scale = p.scale;
+        const int64_t row0 = ((int64_t)b * p.H + h) * p.N;
+        float* dkbase = g ? p.dk2 : p.dk1;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            uint32_t v[32], k[32];
+            uint32_t v[2][16], k[2][16];
             if (ok) {
-                tmem_ld32(lane_base + kColV + g * 64 + c * 32, v);
-                tmem_ld32(lane_base + (g ? kColK2 : kColK1) + c * 32, k);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t lb = lane_base + ((uint32_t)(16 * hh) << 16) + c * 32;
+                    tmem_ld_16x256b_x4(lb + kColV + g * 64, v[hh]);
+                    tmem_ld_16x256b_x4(lb + (g ? kColK2 : kColK1), k[hh]);
+                }
                 tmem_ld_wait();
             }
-            const uint32_t bv = stage0 + (uint32_t)((2 * g + c) * kEpiBox);
-            const uint32_t bk = stage0 + (uint32_t)((4 + 2 * g + c) * kEpiBox);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t off = (uint32_t)((j ^ (r & 7)) << 4);
-                sts_v4(bv + off, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                sts_v4(bk + off, __float_as_uint(__uint_as_float(k[4 * j]) * scale),
-                       __float_as_uint(__uint_as_float(k[4 * j + 1]) * scale),
-                       __float_as_uint(__uint_as_float(k[4 * j + 2]) * scale),
-                       __float_as_uint(__uint_as_float(k[4 * j + 3]) * scale));
-            }
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int ar = 0; ar < 2; ++ar) {
+                    const int key = k0 + lg * 32 + 16 * hh + 8 * ar + tr;
+                    if (!ok || key >= p.N) continue;
+                    float* dvr = p.dv + (row0 + key) * kDV + g * 64 + c * 32 + 2 * tc;
+                    float* dkr = dkbase + (row0 + key) * kD + c * 32 + 2 * tc;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rg = 4 * i + 2 * ar;
+                        *reinterpret_cast<float2*>(dvr + 8 * i) =
+                            make_float2(__uint_as_float(v[hh][rg]), __uint_as_float(v[hh][rg + 1]));
+                        *reinterpret_cast<float2*>(dkr + 8 * i) =
+                            make_float2(__uint_as_float(k[hh][rg]) * scale, __uint_as_float(k[hh][rg + 1]) * scale);
+                    }
+                }
         }
-    }
-    fence_proxy_async_shared();  // the TMA stores read the boxes through the async proxy
-    named_bar_sync(3, 256);
-    if (threadIdx.x == 0 && ok && *abort_flag == 0 && k0 < p.N) {
-        uint8_t* box = smem + kOffP;
-        for (int x = 0; x < 4; ++x) tma_store_3d(&p.tm_dv, box + x * kEpiBox, x * 32, k0, bh);
-        for (int x = 0; x < 2; ++x) tma_store_3d(&p.tm_dk1, box + (4 + x) * kEpiBox, x * 32, k0, bh);
-        for (int x = 0; x < 2; ++x) tma_store_3d(&p.tm_dk2, box + (6 + x) * kEpiBox, x * 32, k0, bh);
-        tma_store_commit();
-        tma_store_wait_read();  // the boxes stay valid until the copies have read them
     }
     tc_fence_before();
     named_bar_sync(2, kThreads);

@@ -54,7 +54,6 @@ struct BwdTcParams {
     CUtensorMap tm_do;                             // dO [B, H, N, Dv], boxes of 64 x 128 rows
     CUtensorMap tm_q1s, tm_q2s, tm_dos;            // the same tensors in boxes of 64 x 64 rows (query steps)
     CUtensorMap tm_stats;                          // 2-D map over the stats [B*H*N][4] fp32, boxes of 4 x 64
-    CUtensorMap tm_dv, tm_dk1, tm_dk2, tm_dq1, tm_dq2;  // 3-D maps over the fp32 gradients [B*H, N, width], boxes of 32 x 128
     const float* stats;                            // [B, H, N, 4]: L1, L2, D1, D2
     float *dq1, *dq2, *dk1, *dk2, *dv;             // fp32 gradients, contiguous
     int B, H, N, d, Dv, causal, in_f16;
