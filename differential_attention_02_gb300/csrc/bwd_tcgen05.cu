@@ -595,7 +595,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     // ---------------------------------------------------------------- elementwise
     setmaxnreg_inc<kRegsMathKV>();
     const int g = warp >> 2, lg = warp & 3;
-    const int r = lg * 32 + lane;  // key row of this thread in the epilogue
     const uint32_t lane_base = tmem + ((uint32_t)(lg * 32) << 16);
     const float sl2 = p.scale_log2, lam = p.lambda;
     constexpr int kHQ = kSQ / 2;  // queries per group and step
