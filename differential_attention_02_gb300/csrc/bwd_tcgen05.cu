@@ -509,6 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 for (int x = 0; x < kDV / 64; ++x)
                     tma_load_4d(smem + kOffV + x * BM * 128, &p.tm_v, &bars->kv_full, x * 64, k0, h, b);
                 const int row0 = (b * p.H + h) * p.N;  // first row of (b, h) in the stats matrix
+                // dO and the statistics come from the preparation kernel launched before this one
+                asm volatile("griddepcontrol.wait;" ::: "memory");
                 int t = 0;
                 for (; t < nsteps; ++t) {
                     const int s = t % kStages, q = qs0 + t * kSQ;
@@ -777,11 +779,24 @@ cudaError_t launch_bwd_tc(const BwdTcParams& p, cudaStream_t key_stream, cudaStr
     }
     const int n_tiles = (p.N + BM - 1) / BM;
     const int grid = n_tiles * p.B * p.H;
+    // The key side follows the preparation in its stream as a programmatic dependent launch:
+    // its CTAs may start while the preparation's last CTAs run, and its producer waits for
+    // the preparation (griddepcontrol.wait) before loading dO and the statistics.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = dkdv::kSmem;
+    cfg.stream = key_stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (f16) {
-        bwd_dkdv_kernel<true><<<grid, kThreads, dkdv::kSmem, key_stream>>>(p);
+        if ((e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<true>, p)) != cudaSuccess) return e;
         bwd_dq_kernel<true><<<grid, kThreads, dq::kSmem, query_stream>>>(p);
     } else {
-        bwd_dkdv_kernel<false><<<grid, kThreads, dkdv::kSmem, key_stream>>>(p);
+        if ((e = cudaLaunchKernelEx(&cfg, bwd_dkdv_kernel<false>, p)) != cudaSuccess) return e;
         bwd_dq_kernel<false><<<grid, kThreads, dq::kSmem, query_stream>>>(p);
     }
     return cudaGetLastError();

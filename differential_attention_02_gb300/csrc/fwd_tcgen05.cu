@@ -417,6 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
     float* epi = reinterpret_cast<float*>(smem + C::kOffEpi);  // [4][BM]: 1/l1, lambda/l2, ss1, ss2
     volatile int* abort_flag = &bars->abort;
+    // As the backward's preparation: the key-side kernel that follows may start its setup
+    // and K/V loads once every CTA of this grid has started (it waits for this grid before
+    // reading dO and the statistics).
+    if constexpr (MODE == kModePrep) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = (p.N + BM - 1) / BM;
@@ -1248,6 +1252,9 @@ __device__ __forceinline__ float warp_allsum(float v) {
 
 template <bool F16>
 __global__ void __launch_bounds__(kSavedThreads, 4) bwd_prep_saved_kernel(const __grid_constant__ FwdParams p) {
+    // the key-side kernel that follows may start its setup and K/V loads once every CTA of
+    // this grid has started (it waits for this grid before reading dO and the statistics)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int DV = 128, kWarps = kSavedThreads / 32;
     using T16x2 = typename std::conditional<F16, __half2, __nv_bfloat162>::type;
     __shared__ float wsum[kWarps][DV];
