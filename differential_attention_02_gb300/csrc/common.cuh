@@ -307,6 +307,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
+// Programmatic dependent launch (kernels started with launch_pdl). pdl_trigger lets the
+// next kernel in the stream start its CTAs once every CTA of this grid has triggered or
+// exited (so no CTA of this grid is still waiting for resources); pdl_wait blocks until
+// the previous kernel in the stream has completed and its writes are visible (it returns
+// at once without a programmatic predecessor). A kernel calls pdl_wait in every thread
+// before it reads what an earlier kernel wrote and before it can exit, which keeps
+// completion transitive along a chain of such launches.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `count` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -168,6 +168,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // The setup above may overlap the previous kernel's tail (the projection GEMM that wrote
+    // Q, K and V).
+    pdl_trigger();
+    pdl_wait();
     const uint32_t tmem = bars->tmem_base;
     uint8_t* qs = smem + C::kOffQ;
     uint8_t* ks = smem + C::kOffK;
@@ -504,8 +508,7 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t stream) {
     cudaError_t e = prepare_once<fwd_pair_kernel<D, DV, F16>>((int)C::kSmem);
     if (e != cudaSuccess) return e;
     const int n_tiles = (p.N + BM - 1) / BM;
-    k<<<2 * n_tiles * p.B * p.H, kThreads, C::kSmem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(2 * n_tiles * p.B * p.H), dim3(kThreads), C::kSmem, stream, p);
 }
 
 }  // namespace

@@ -88,6 +88,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_kernel(const __grid_con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // The setup above may overlap the previous kernel's tail; A (and R, the gain, the row
+    // sums) may be that kernel's output.
+    pdl_trigger();
+    pdl_wait();
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
@@ -383,8 +387,7 @@ cudaError_t launch_gemm_bf16(const GemmParams& p, cudaStream_t stream) {
     int sms = 0;
     if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
     const int tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
-    gemm_bf16_kernel<<<tiles < sms ? tiles : sms, kThreads, kSmem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_bf16_kernel, dim3(tiles < sms ? tiles : sms), dim3(kThreads), kSmem, stream, p);
 }
 
 }  // namespace da

@@ -212,6 +212,24 @@ cudaError_t prepare_once(int smem_bytes, int want_regs = 0) {
     return cudaSuccess;
 }
 
+// Launches `kernel` as a programmatic dependent of the previous kernel in `stream`: its CTAs
+// may start (and run their setup up to pdl_wait) while that kernel's last CTAs finish.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Number of SMs of the current device (queried once per device).
 inline cudaError_t device_sm_count(int* sms) {
     static std::atomic<int> cache[64];

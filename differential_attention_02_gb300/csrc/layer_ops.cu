@@ -46,6 +46,8 @@ __device__ __forceinline__ void load_y8(const AddNormParams& p, int64_t off, flo
 }
 
 __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(const __grid_constant__ AddNormParams p) {
+    pdl_trigger();
+    pdl_wait();  // y and z may be the previous kernel's output
     __shared__ float red[kNormThreads / 32];
     const int64_t base = (int64_t)blockIdx.x * p.N;
     const int n8 = p.N / 8;
@@ -110,8 +112,7 @@ __global__ void swiglu_kernel(const __half* __restrict__ gu, uint16_t* __restric
 }  // namespace
 
 cudaError_t launch_add_rmsnorm(const AddNormParams& p, cudaStream_t stream) {
-    add_rmsnorm_kernel<<<p.M, kNormThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(add_rmsnorm_kernel, dim3(p.M), dim3(kNormThreads), 0, stream, p);
 }
 
 cudaError_t launch_swiglu(const void* gate_up, void* h, int h_f16, int64_t M, int H, cudaStream_t stream) {
