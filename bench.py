@@ -461,7 +461,8 @@ def run_backward(args, da, gi, dev, stream, peaks, peak_kind):
     tf = flops / (ms * 1e-3) / 1e12
     tf_re = flops / (ms_re * 1e-3) / 1e12
     return {"workload": "backward of the prefill workload B4 H16 N2048 d64 Dv128 causal, bf16 in, fp32 gradients, "
-                        "from the training forward's saved state (O1, O2 and each map's row max and sum, fp32)",
+                        "from the training forward's saved state (x = O1/l1 - lambda O2/l2 in fp32, O2/l2 in the operand "
+                        "type, each map's row log-sum-exp)",
             "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "flops_per_step": flops,
             "exec_tflops": exec_flops / (ms * 1e-3) / 1e12,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -474,7 +475,7 @@ def run_backward(args, da, gi, dev, stream, peaks, peak_kind):
                           "ms_per_step": ms_re, "value": tf_re, "frac": tf_re / peaks["bf16_tflops"],
                           "exec_tflops": exec_re / (ms_re * 1e-3) / 1e12, "gpu_launches_per_step": 4},
             "forward": {"note": "the same inputs' forward, bf16 out: diffattn_fwd_train (per-tile kernel, saves "
-                                f"{2 * w.B * w.H * w.N * w.Dv * 4 / 1e6:.0f} MB of state) against diffattn_fwd",
+                                f"{da.train_saved_bytes(w.B, w.H, w.N, w.Dv) / 1e6:.0f} MB of state) against diffattn_fwd",
                         "train_ms": ms_train, "plain_ms": ms_plain}}
 
 

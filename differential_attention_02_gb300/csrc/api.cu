@@ -192,12 +192,28 @@ diffattn_status diffattn_fwd_workspace_size(int B, int H, int N, int d, int Dv, 
 }  // extern "C"
 
 namespace {
-// diffattn_fwd, and with o_save/ml_save set the training forward (tensor-core path,
+struct SavedLayout {
+    size_t x, a2, lse, total;  // x (fp32), O2/l2 (16-bit), L1 and L2 per row (fp32)
+};
+SavedLayout saved_layout(int B, int H, int N, int Dv) {
+    const size_t rows = (size_t)B * H * N;
+    SavedLayout l;
+    l.x = 0;
+    l.a2 = round256(rows * Dv * sizeof(float));
+    l.lse = l.a2 + round256(rows * Dv * sizeof(uint16_t));
+    l.total = l.lse + round256(rows * 2 * sizeof(float));
+    return l;
+}
+bool saved_ok(const void* saved, size_t bytes, int B, int H, int N, int Dv) {
+    return saved != nullptr && !(reinterpret_cast<uintptr_t>(saved) & 255u) && bytes >= saved_layout(B, H, N, Dv).total;
+}
+
+// diffattn_fwd, and with `saved` set the training forward (tensor-core path,
 // d=64/Dv=128; the caller has checked that).
 diffattn_status fwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor k1, diffattn_tensor k2,
                          diffattn_tensor v, void* out, const float* norm_weight, int B, int H, int N, int d, int Dv,
                          int causal, float lambda, float lambda_init, float eps, int in_dtype, int out_dtype,
-                         void* workspace, size_t workspace_bytes, void* stream, float* o_save, float* ml_save) {
+                         void* workspace, size_t workspace_bytes, void* stream, void* saved) {
     if (B < 0 || H < 0 || N < 0 || d < 1 || Dv < 1) return DIFFATTN_ERR_INVALID_ARG;
     if ((in_dtype != DIFFATTN_F32 && in_dtype != DIFFATTN_BF16 && in_dtype != DIFFATTN_F16) ||
         (out_dtype != DIFFATTN_F32 && out_dtype != DIFFATTN_BF16 && out_dtype != DIFFATTN_F16) ||
@@ -259,10 +275,15 @@ diffattn_status fwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor
     p.lambda = lambda; p.lambda_init = lambda_init; p.eps = eps;
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
     p.err = err_word(workspace);
-    if (o_save != nullptr) {
-        p.o_save = o_save;
-        p.ml_save = ml_save;
-        if (!encode_out_3d(&p.tm_osave, o_save, Dv, N, 2 * B * H, 4, kFwdBM)) return DIFFATTN_ERR_INVALID_ARG;
+    if (saved != nullptr) {
+        const SavedLayout sl = saved_layout(B, H, N, Dv);
+        uint8_t* sv = static_cast<uint8_t*>(saved);
+        p.x_save = reinterpret_cast<float*>(sv + sl.x);
+        p.a2_save = sv + sl.a2;
+        p.lse_save = reinterpret_cast<float*>(sv + sl.lse);
+        if (!encode_out_3d(&p.tm_xsave, p.x_save, Dv, N, B * H, 4, kFwdBM) ||
+            !encode_out_3d(&p.tm_a2save, p.a2_save, Dv, N, B * H, 2, kFwdBM))
+            return DIFFATTN_ERR_INVALID_ARG;
         return cuda_status(launch_fwd_train(p, st));
     }
     // (64, 128): both maps share one CTA; (128, 256): the accumulators of both
@@ -272,20 +293,6 @@ diffattn_status fwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor
 
 // The training forward's saved state: O1, O2 (fp32 [2][B, H, N, Dv]), then the
 // per-row max and sum of both maps (fp32 [B, H, N, 4]), each part 256-byte aligned.
-struct SavedLayout {
-    size_t o, ml, total;
-};
-SavedLayout saved_layout(int B, int H, int N, int Dv) {
-    const size_t rows = (size_t)B * H * N;
-    SavedLayout l;
-    l.o = 0;
-    l.ml = round256(2 * rows * Dv * sizeof(float));
-    l.total = l.ml + round256(rows * 4 * sizeof(float));
-    return l;
-}
-bool saved_ok(const void* saved, size_t bytes, int B, int H, int N, int Dv) {
-    return saved != nullptr && !(reinterpret_cast<uintptr_t>(saved) & 255u) && bytes >= saved_layout(B, H, N, Dv).total;
-}
 }  // namespace
 
 extern "C" {
@@ -295,7 +302,7 @@ diffattn_status diffattn_fwd(diffattn_tensor q1, diffattn_tensor q2, diffattn_te
                              int Dv, int causal, float lambda, float lambda_init, float eps, int in_dtype,
                              int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
     return fwd_impl(q1, q2, k1, k2, v, out, norm_weight, B, H, N, d, Dv, causal, lambda, lambda_init, eps, in_dtype,
-                    out_dtype, workspace, workspace_bytes, stream, nullptr, nullptr);
+                    out_dtype, workspace, workspace_bytes, stream, nullptr);
 }
 
 diffattn_status diffattn_train_saved_size(int B, int H, int N, int Dv, size_t* bytes) {
@@ -312,11 +319,8 @@ diffattn_status diffattn_fwd_train(diffattn_tensor q1, diffattn_tensor q2, diffa
     if (in_dtype == DIFFATTN_F32) return DIFFATTN_ERR_UNSUPPORTED;
     if (B > 0 && H > 0 && N > 0 && !(d == 64 && Dv == 128)) return DIFFATTN_ERR_UNSUPPORTED;
     if (B > 0 && H > 0 && N > 0 && !saved_ok(saved, saved_bytes, B, H, N, Dv)) return DIFFATTN_ERR_INVALID_ARG;
-    uint8_t* sv = static_cast<uint8_t*>(saved);
-    const SavedLayout sl = saved_layout(B < 0 ? 0 : B, H < 0 ? 0 : H, N < 0 ? 0 : N, Dv < 1 ? 1 : Dv);
     return fwd_impl(q1, q2, k1, k2, v, out, norm_weight, B, H, N, d, Dv, causal, lambda, lambda_init, eps, in_dtype,
-                    out_dtype, workspace, workspace_bytes, stream, reinterpret_cast<float*>(sv + sl.o),
-                    reinterpret_cast<float*>(sv + sl.ml));
+                    out_dtype, workspace, workspace_bytes, stream, saved);
 }
 
 diffattn_status diffattn_decode_workspace_size(int B, int H, int L, int d, int Dv, int num_splits, size_t* bytes) {
@@ -529,8 +533,9 @@ diffattn_status bwd_impl(diffattn_tensor q1, diffattn_tensor q2, diffattn_tensor
             // The forward's state was saved: only the per-row preparation remains.
             const SavedLayout sl = saved_layout(B, H, N, Dv);
             uint8_t* sv = static_cast<uint8_t*>(const_cast<void*>(saved));
-            f.o_save = reinterpret_cast<float*>(sv + sl.o);
-            f.ml_save = reinterpret_cast<float*>(sv + sl.ml);
+            f.x_save = reinterpret_cast<float*>(sv + sl.x);
+            f.a2_save = sv + sl.a2;
+            f.lse_save = reinterpret_cast<float*>(sv + sl.lse);
             e = launch_bwd_prep_saved(f, st);
         } else {
             e = launch_bwd_prep(f, st);

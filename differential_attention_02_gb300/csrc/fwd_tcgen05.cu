@@ -407,7 +407,8 @@ __device__ __forceinline__ void prep_epilogue(const FwdParams& p, bool ok, int g
 constexpr int kModePlain = 0, kModePrep = 1, kModeSave = 2;
 // Save mode stages O1, O2 (8 boxes of 16 KB) in the K/V ring after the output's
 // staging (at most 64 KB, fp32 output).
-constexpr int kSaveStageOff = 64 * 1024;
+constexpr int kSaveStageOff = 64 * 1024;                 // x boxes (4 x 16 KB) of the saved state
+constexpr int kSaveA2Off = kSaveStageOff + 4 * 128 * 128;  // O2/l2 boxes (2 x 16 KB)
 
 template <int D, int DV, bool F16, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ FwdParams p) {
@@ -726,34 +727,52 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
                 tmem_ld32(lane_base + C::kColO + g * kHalf + c * 32, o1);
                 tmem_ld32(lane_base + C::kColO + DV + g * kHalf + c * 32, o2);
                 tmem_ld_wait();
-                if constexpr (MODE == kModeSave) {
-                    // This group's half of both unnormalised accumulators, as they are in TMEM,
-                    // staged for TMA stores behind the output's staging in the idle K/V ring:
-                    // boxes of [128 rows][32 fp32], map m's box j at (4 m + j) * 16 KB.
-                    static_assert(kSaveStageOff + 8 * BM * 128 <= kKvStages * C::kStageBytes, "O staging fits");
-                    uint8_t* sb = smem + C::kOffStages + kSaveStageOff;
-                    const int j = (g * kHalf + c * 32) / 32;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        *reinterpret_cast<uint4*>(sb + j * (BM * 128) + sw128_offset(r, i)) =
-                            make_uint4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
-                        *reinterpret_cast<uint4*>(sb + (4 + j) * (BM * 128) + sw128_offset(r, i)) =
-                            make_uint4(o2[4 * i], o2[4 * i + 1], o2[4 * i + 2], o2[4 * i + 3]);
-                    }
-                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float x = __uint_as_float(o1[i]) * inv1 - __uint_as_float(o2[i]) * inv2;
                     oh[c * 32 + i] = x;
                     ss = fmaf(x, x, ss);
                 }
+                if constexpr (MODE == kModeSave) {
+                    // x = O1/l1 - lambda O2/l2 (the output before the norm, fp32), this group's
+                    // columns, staged for TMA stores behind the output's staging in the idle K/V
+                    // ring as boxes of [128 rows][32 fp32]: box j (columns 32 j..) at j * 16 KB.
+                    static_assert(kSaveA2Off + 2 * BM * 128 <= kKvStages * C::kStageBytes, "staging fits");
+                    uint8_t* box = smem + C::kOffStages + kSaveStageOff + (g * (kHalf / 32) + c) * (BM * 128);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(box + sw128_offset(r, i)) =
+                            make_float4(oh[c * 32 + 4 * i], oh[c * 32 + 4 * i + 1], oh[c * 32 + 4 * i + 2],
+                                        oh[c * 32 + 4 * i + 3]);
+                }
             }
         }
         if constexpr (MODE == kModeSave) {
-            // This map's running max (scaled-score units) and sum for the row.
-            if (ok && qrow < p.N)
-                *reinterpret_cast<float2*>(p.ml_save + (((int64_t)b * p.H + h) * p.N + qrow) * 4 + 2 * g) =
-                    make_float2(m_used, l);
+            // Map 2's own output O2 / l2 (its attention output), rounded to the operand type, by
+            // group 1 (which holds l2), staged behind the x boxes as boxes of [128 rows][64
+            // 16-bit values]; then the row's log-sum-exp of map g in base 2 of the scaled
+            // scores, L_g = max_g + log2(l_g).
+            if (ok && g == 1) {
+                const float inv = 1.0f / l;
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + C::kColO + DV + c * 32, o);
+                    tmem_ld_wait();
+                    uint8_t* box = smem + C::kOffStages + kSaveA2Off + (c / 2) * (BM * 128);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            pk[e] = pack_p<F16>(__uint_as_float(o[8 * i + 2 * e]) * inv,
+                                                __uint_as_float(o[8 * i + 2 * e + 1]) * inv);
+                        *reinterpret_cast<uint4*>(box + sw128_offset(r, (c % 2) * 4 + i)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            }
+            if (ok && qrow < p.N) p.lse_save[(((int64_t)b * p.H + h) * p.N + qrow) * 2 + g] = m_used + log2f(l);
         }
         epi[(2 + g) * BM + r] = ss;
         named_bar_sync(1, 256);
@@ -809,13 +828,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
             index_ok(q0 < p.N, p.err, 0x92);
             for (int i = 0; i < DV / bw; ++i) tma_store_3d(&p.tm_out, stage + i * (BM * 128), h * DV + i * bw, q0, b);
             if constexpr (MODE == kModeSave) {
-                // O1 and O2 of the tile: rows [q0, q0 + 128) of head (b, h) in maps 0 and 1 of the
-                // [2 B H][N][Dv] view; rows past N are clipped.
-                static_assert(DV == 128, "four 32-column boxes per map");
-                for (int m = 0; m < 2; ++m)
-                    for (int jb = 0; jb < 4; ++jb)
-                        tma_store_3d(&p.tm_osave, stage + kSaveStageOff + (4 * m + jb) * (BM * 128), jb * 32, q0,
-                                     (m * p.B + b) * p.H + h);
+                // x (fp32) and O2/l2 (16-bit) of the tile: rows [q0, q0 + 128) of head (b, h);
+                // rows past N are clipped.
+                static_assert(DV == 128, "four 32-column fp32 boxes, two 64-column 16-bit boxes");
+                for (int jb = 0; jb < 4; ++jb)
+                    tma_store_3d(&p.tm_xsave, stage + kSaveStageOff + jb * (BM * 128), jb * 32, q0, b * p.H + h);
+                for (int jb = 0; jb < 2; ++jb)
+                    tma_store_3d(&p.tm_a2save, stage + kSaveA2Off + jb * (BM * 128), jb * 64, q0, b * p.H + h);
             }
             tma_store_commit();
             tma_store_wait_read();
@@ -1269,20 +1288,21 @@ __global__ void __launch_bounds__(kSavedThreads, 4) bwd_prep_saved_kernel(const 
     const float lam = p.lambda, cs = 1.0f - p.lambda_init;
     const int c0 = 4 * lane;
     const float4 w = p.norm_w ? *reinterpret_cast<const float4*>(p.norm_w + c0) : make_float4(1.f, 1.f, 1.f, 1.f);
-    const int64_t map_stride = (int64_t)BH * p.N * DV;
     float dw[4] = {0.f, 0.f, 0.f, 0.f}, dl = 0.f;
     // The warp's rows, in order; each row's operands are loaded one row ahead.
     const int rbeg = q0 + warp * (BM / kWarps), rend = min(rbeg + BM / kWarps, p.N);
     struct RowIn {
-        float4 ml, o1, o2;  // max1, sum1, max2, sum2; this lane's columns of O1, O2
+        float2 lse;  // L1, L2
+        float4 x;    // this lane's four columns of x = O1/l1 - lambda O2/l2
+        uint2 a2;    // and of O2/l2 (16-bit)
         uint2 dy;
     };
     auto load_row = [&](int qrow) {
         const int64_t row = ((int64_t)b * p.H + h) * p.N + qrow;
         RowIn in;
-        in.ml = *reinterpret_cast<const float4*>(p.ml_save + row * 4);
-        in.o1 = *reinterpret_cast<const float4*>(p.o_save + row * DV + c0);
-        in.o2 = *reinterpret_cast<const float4*>(p.o_save + map_stride + row * DV + c0);
+        in.lse = *reinterpret_cast<const float2*>(p.lse_save + row * 2);
+        in.x = *reinterpret_cast<const float4*>(p.x_save + row * DV + c0);
+        in.a2 = *reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.a2_save) + (row * DV + c0) * 2);
         in.dy = *reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.dy) +
                                                 ((((int64_t)b * p.N + qrow) * p.H + h) * DV + c0) * 2);
         return in;
@@ -1293,25 +1313,30 @@ __global__ void __launch_bounds__(kSavedThreads, 4) bwd_prep_saved_kernel(const 
         const int64_t row = ((int64_t)b * p.H + h) * p.N + qrow;
         const RowIn cur = next;
         if (qrow + 1 < rend) next = load_row(qrow + 1);
-        const float4 ml = cur.ml, o1 = cur.o1, o2 = cur.o2;
-        const uint2 dyr = cur.dy;
-        const float i1 = 1.0f / ml.y, i2 = 1.0f / ml.w;
-        const float a1[4] = {o1.x * i1, o1.y * i1, o1.z * i1, o1.w * i1};
-        const float a2[4] = {o2.x * i2, o2.y * i2, o2.z * i2, o2.w * i2};
-        float dyv[4];
-        if constexpr (F16) {
-            const float2 u = __half22float2(*reinterpret_cast<const __half2*>(&dyr.x));
-            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&dyr.y));
-            dyv[0] = u.x; dyv[1] = u.y; dyv[2] = v.x; dyv[3] = v.y;
-        } else {
-            dyv[0] = bf16lo_to_f32(dyr.x); dyv[1] = bf16hi_to_f32(dyr.x);
-            dyv[2] = bf16lo_to_f32(dyr.y); dyv[3] = bf16hi_to_f32(dyr.y);
-        }
+        const float2 lse = cur.lse;
+        // four 16-bit values of the operand type as floats
+        auto unpack4 = [](uint2 u, float* o) {
+            if constexpr (F16) {
+                const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+                const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+                o[0] = a.x; o[1] = a.y; o[2] = c.x; o[3] = c.y;
+            } else {
+                o[0] = bf16lo_to_f32(u.x); o[1] = bf16hi_to_f32(u.x);
+                o[2] = bf16lo_to_f32(u.y); o[3] = bf16hi_to_f32(u.y);
+            }
+        };
+        float a2[4], dyv[4];
+        unpack4(cur.a2, a2);
+        unpack4(cur.dy, dyv);
+        const float xv[4] = {cur.x.x, cur.x.y, cur.x.z, cur.x.w};
+        float a1[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a1[k] = fmaf(lam, a2[k], xv[k]);  // O1/l1
         const float wv[4] = {w.x, w.y, w.z, w.w};
         float x[4], ss = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            x[k] = a1[k] - lam * a2[k];
+            x[k] = xv[k];  // the forward's own fp32 value
             ss = fmaf(x[k], x[k], ss);
         }
         const float ir = 1.0f / sqrtf(warp_allsum(ss) / (float)DV + p.eps);
@@ -1358,7 +1383,7 @@ __global__ void __launch_bounds__(kSavedThreads, 4) bwd_prep_saved_kernel(const 
         x2e = warp_allsum(x2e);
         if (lane == 0)
             *reinterpret_cast<float4*>(p.stats + row * 4) =
-                make_float4(ml.x + __log2f(ml.y), ml.z + __log2f(ml.w), x1, -lam * x2);
+                make_float4(lse.x, lse.y, x1, -lam * x2);
         dl -= x2e;
     }
 #pragma unroll
@@ -1403,13 +1428,13 @@ cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_fwd_train(const FwdParams& p, cudaStream_t stream) {
-    if (p.d == 64 && p.Dv == 128 && p.o_save && p.ml_save)
+    if (p.d == 64 && p.Dv == 128 && p.x_save && p.a2_save && p.lse_save)
         return p.in_f16 ? launch_t<64, 128, true, kModeSave>(p, stream) : launch_t<64, 128, false, kModeSave>(p, stream);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_prep_saved(const FwdParams& p, cudaStream_t stream) {
-    if (p.d == 64 && p.Dv == 128 && p.dy && p.d_o && p.stats && p.part_lam && p.part_w && p.o_save && p.ml_save)
+    if (p.d == 64 && p.Dv == 128 && p.dy && p.d_o && p.stats && p.part_lam && p.part_w && p.x_save && p.a2_save && p.lse_save)
         return p.in_f16 ? launch_prep_saved_t<true>(p, stream) : launch_prep_saved_t<false>(p, stream);
     return cudaErrorInvalidValue;
 }

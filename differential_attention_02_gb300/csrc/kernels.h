@@ -173,9 +173,11 @@ struct FwdParams {
     float* part_w = nullptr;       // [grid][Dv] per-CTA partial of the gain's gradient
     // Training forward (launch_fwd_train) writes, besides the output, the state the
     // backward starts from; launch_bwd_prep_saved reads it instead of re-running the forward.
-    float* o_save = nullptr;       // [2][B, H, N, Dv]: the unnormalised accumulators O1, O2 (fp32)
-    CUtensorMap tm_osave;          // 3-D map over o_save [2 B H][N][Dv] fp32, boxes of 32 x 128 rows
-    float* ml_save = nullptr;      // [B, H, N, 4]: running max of map 1 (scaled-score units), its sum, max 2, sum 2
+    float* x_save = nullptr;       // [B, H, N, Dv]: x = O1/l1 - lambda O2/l2, the output before the norm (fp32)
+    void* a2_save = nullptr;       // [B, H, N, Dv]: O2/l2, map 2's own output, in the operand type
+    CUtensorMap tm_xsave;          // 3-D map over x_save [B H][N][Dv] fp32, boxes of 32 x 128 rows
+    CUtensorMap tm_a2save;         // 3-D map over a2_save [B H][N][Dv] 16-bit, boxes of 64 x 128 rows
+    float* lse_save = nullptr;     // [B, H, N, 2]: L1, L2 = max + log2(sum) per map (base 2, scaled scores)
 };
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);       // both maps in one CTA
 cudaError_t launch_fwd_train(const FwdParams& p, cudaStream_t stream);      // d=64: forward + saved state

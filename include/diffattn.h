@@ -376,23 +376,26 @@ diffattn_status diffattn_bwd_workspace_size(int B, int H, int N, int d, int Dv, 
  * and the backward that starts from it instead of re-running the forward.
  *
  * diffattn_fwd_train — diffattn_fwd (same arguments, same output, bit for bit)
- * that also writes into `saved` each map's unnormalised accumulator
- * O_m = sum_j exp2(S_m log2(e)/sqrt(d) - max_m) V_j (f32 [2][B, H, N, Dv]) and,
- * per row, each map's running max (in log2(e)/sqrt(d) score units) and sum
- * (f32 [B, H, N, 4]: max1, sum1, max2, sum2): the forward's TMEM state after its
- * last PV products. Tensor-core path only: bf16 or f16 with (d, Dv) = (64, 128)
+ * that also writes into `saved` what the backward needs of the forward once its
+ * last PV products finished: per row, x = O1/l1 - lambda O2/l2, the output before
+ * the norm (f32 [B, H, N, Dv], the forward's own values); map 2's attention output
+ * O2/l2 = softmax_2 V rounded once to the operand type ([B, H, N, Dv], 16-bit; the
+ * backward forms O1/l1 = x + lambda O2/l2); and each map's log-sum-exp in base 2 of
+ * the scaled scores, L_m = max_m + log2(l_m) = log2 sum_j exp2(S_m log2(e)/sqrt(d))
+ * (f32 [B, H, N, 2]). Tensor-core path only: bf16 or f16 with (d, Dv) = (64, 128)
  * (else DIFFATTN_ERR_UNSUPPORTED); it always runs the per-tile kernel.
  * saved: device, diffattn_train_saved_size() bytes, 256-byte aligned, owned by
  *   the caller; the contents are meant only for diffattn_bwd_saved with the same
  *   q1..v, norm_weight, shapes, causal, lambda, lambda_init, eps and in_dtype.
  *
  * diffattn_bwd_saved — diffattn_bwd (same arguments and outputs) from `saved`:
- * its preparation (one CUDA-core pass over the rows, bandwidth-bound) reads O_m
- * and the row statistics instead of recomputing the scores, softmaxes and PV
- * products, then the same key-side, query-side and reduction kernels run. The
- * gradients agree with diffattn_bwd's to rounding: the per-row sums (the norm, D1,
- * D2) are added in another fp32 order, so an element of dO can round the other
- * way. Deterministic. Same support as diffattn_fwd_train; workspace as for
+ * its preparation (one CUDA-core pass over the rows, bandwidth-bound) reads x,
+ * O2/l2 and L_m instead of recomputing the scores, softmaxes and PV products, then
+ * the same key-side, query-side and reduction kernels run. The gradients agree with
+ * diffattn_bwd's to rounding: O2/l2 carries one rounding to the operand type (it
+ * enters D1 and D2 only; the norm's x is exact) and the per-row sums (the norm, D1,
+ * D2) are added in another fp32 order.
+ * Deterministic. Same support as diffattn_fwd_train; workspace as for
  * diffattn_bwd.
  */
 diffattn_status diffattn_train_saved_size(int B, int H, int N, int Dv, size_t* bytes);

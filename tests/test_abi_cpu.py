@@ -365,7 +365,7 @@ def test_training_pair_argument_validation(lib):
     assert lib.diffattn_train_saved_size(1, 2, 16, 128, ctypes.byref(n)) == da.OK
     rows = 2 * 16
     r256 = lambda x: (x + 255) // 256 * 256
-    assert n.value == r256(2 * rows * 128 * 4) + r256(rows * 16)
+    assert n.value == r256(rows * 128 * 4) + r256(rows * 128 * 2) + r256(rows * 8)  # x, O2/l2, L1 and L2
     assert lib.diffattn_train_saved_size(1, -2, 16, 128, ctypes.byref(n)) == da.ERR_INVALID_ARG
     assert lib.diffattn_train_saved_size(1, 2, 16, 128, None) == da.ERR_INVALID_ARG
     nbytes = n.value
