@@ -9,7 +9,8 @@
 //   y = O / sqrt(mean(O^2) + eps) * w * (1 - lambda_init).
 // The pages train the model but print no gradient; this is the chain rule of
 // that definition. The preparation pass (the forward kernel with another
-// epilogue, launch_bwd_prep) leaves per query row: dO (the gradient of O, in the
+// epilogue, launch_bwd_prep, or from a training forward's saved state,
+// launch_bwd_prep_saved) leaves per query row: dO (the gradient of O, in the
 // operand type), L_m (so that P_m = exp2(S_m log2(e)/sqrt(d) - L_m)),
 // D1 = dO . (P1 V) and D2 = -lambda dO . (P2 V). Then, with dA = dO V^T:
 //   dS1 = P1 (dA - D1),  dS2 = P2 (-lambda dA - D2)
@@ -17,7 +18,9 @@
 //   dK_m = dS_m^T Q_m / sqrt(d),  dV = A^T dO
 //                                  (kernel bwd_dkdv: one key tile per CTA)
 // Each gradient row is written by exactly one CTA, so there are no atomics and
-// the result does not depend on scheduling.
+// the result does not depend on scheduling. The key side follows the preparation
+// as a programmatic dependent launch (its setup and K/V loads overlap the
+// preparation's last wave); the query side runs beside it on a forked stream.
 //
 // Both kernels keep S, dA and the gradient accumulators in TMEM. The products
 // whose left operand is elementwise data (dS or A, rounded to the operand type)
