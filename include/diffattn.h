@@ -21,6 +21,11 @@
  *    never synchronises, except diffattn_read_error (documented there).
  *  - All pointers are device pointers unless stated otherwise. Work is
  *    enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *    Some kernels (the GEMMs, the wide-head attention, add+RMSNorm, the
+ *    backward's key side) are programmatic dependent launches: their CTAs may
+ *    start their setup while the previous kernel on the stream finishes, but
+ *    they read nothing and complete nothing before it has completed, so stream
+ *    order holds as for ordinary launches (also under CUDA-graph capture).
  *  - Every call returns a diffattn_status; nothing throws across the ABI.
  *    Shapes, dtypes, alignment and strides are checked on the host before any
  *    launch (DIFFATTN_ERR_INVALID_ARG); shape families without a kernel give
