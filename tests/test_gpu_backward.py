@@ -259,6 +259,32 @@ def test_training_pair(B, H, N, causal, dtype, weight):
         assert rr <= tol or float((x - y).abs().max()) <= 1e-6, f"{k}: saved vs recompute rel-RMS {rr:.2e}"
 
 
+@pytest.mark.parametrize("lam,dtype", [(0.0, torch.bfloat16), (-0.7, torch.float16), (2.2, torch.bfloat16)])
+def test_training_pair_lambda_values(lam, dtype):
+    """The saved state's O1/l1 is rebuilt as x + lambda O2/l2, so lambda enters the backward's
+    preparation directly: the training pair against the oracle at lambda = 0 (O2/l2 drops out;
+    dQ2 and dK2 are exactly zero), lambda < 0 and lambda > 1, with a gain."""
+    B, H, N = 1, 2, 200
+    g0 = torch.Generator().manual_seed(int(1000 * abs(lam)) + 7)
+    t = {k: torch.randn(B, H, N, 128 if k == "v" else 64, generator=g0).to(dtype) for k in NAMES}
+    dy = torch.randn(B, N, H, 128, generator=g0).to(dtype)
+    nw = torch.linspace(0.5, 1.5, 128)
+    dev = {k: v.cuda() for k, v in t.items()}
+    lam_init = 0.35
+    _, saved = da.diffattn_fwd_train(*(dev[k] for k in NAMES), lam, lam_init, norm_weight=nw.cuda())
+    ws = da.workspace(da.bwd_workspace_bytes(B, H, N, 64, 128))
+    g = da.diffattn_bwd(*(dev[k] for k in NAMES), dy.cuda(), lam, lam_init, norm_weight=nw.cuda(),
+                        want_dnorm_weight=True, ws=ws, saved=saved)
+    torch.cuda.synchronize()
+    assert da.read_error(ws) == 0
+    ref = orc.diffattn_bwd(*(t[k] for k in NAMES), dy, lam, lam_init, 1e-5, weight=nw.numpy())
+    bounds = _bounds(64, 128, dtype)
+    _check(g, ref, f"training pair lambda {lam}", bounds=bounds)
+    _check_sums(g, ref, bounds, t, dy, lam, lam_init, weight=nw.numpy())
+    if lam == 0.0:
+        assert float(g["dq2"].abs().max()) == 0.0 and float(g["dk2"].abs().max()) == 0.0
+
+
 def test_training_forward_saved_state_against_the_definition():
     """The saved state pinned to the definition, independently of the backward: with
     A_m = softmax_m V (each map's attention output, float64), x = A1 - lambda A2 (fp32),
