@@ -366,6 +366,11 @@ def test_training_pair_argument_validation(lib):
     rows = 2 * 16
     r256 = lambda x: (x + 255) // 256 * 256
     assert n.value == r256(rows * 128 * 4) + r256(rows * 128 * 2) + r256(rows * 8)  # x, O2/l2, L1 and L2
+    for B, H, N in ((1, 1, 1), (3, 5, 130), (4, 16, 2048), (2, 3, 16383)):
+        assert lib.diffattn_train_saved_size(B, H, N, 128, ctypes.byref(n)) == da.OK
+        r = B * H * N
+        assert n.value == r256(r * 128 * 4) + r256(r * 128 * 2) + r256(r * 8), (B, H, N)
+    assert lib.diffattn_train_saved_size(1, 2, 16, 128, ctypes.byref(n)) == da.OK
     assert lib.diffattn_train_saved_size(1, -2, 16, 128, ctypes.byref(n)) == da.ERR_INVALID_ARG
     assert lib.diffattn_train_saved_size(1, 2, 16, 128, None) == da.ERR_INVALID_ARG
     nbytes = n.value

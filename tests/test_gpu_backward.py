@@ -328,6 +328,42 @@ def test_training_forward_saved_state_against_the_definition():
                 assert np.abs(lse[0, h, :, m] - ref_l[m]).max() <= 1e-4, f"{in_dtype} head {h} map {m + 1}: L"
 
 
+def test_training_forward_saved_state_prefill_workload_sampled_heads():
+    """The saved state at the full B=4, H=16, N=2048 prefill workload, on three heads against
+    the definition (x, O2/l2 and L as in the test above, the same bars), and its size."""
+    w = gi.WORKLOADS["prefill_bf16"]
+    t = gi.prefill_inputs(w)
+    lam = 0.5
+    dev = {k: v.cuda() for k, v in t.items()}
+    _, saved = da.diffattn_fwd_train(*(dev[k] for k in NAMES), lam, 0.3, w.eps, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    rows = w.B * w.H * w.N
+    r256 = lambda n: (n + 255) // 256 * 256
+    xb, ab = rows * w.Dv * 4, rows * w.Dv * 2
+    assert saved.numel() == r256(xb) + r256(ab) + r256(rows * 8)
+    allowed = orc.causal_allowed(np.arange(w.N), w.N)
+    for b, h in ((0, 0), (1, 7), (3, 15)):
+        row0 = (b * w.H + h) * w.N
+        x = saved[row0 * w.Dv * 4:(row0 + w.N) * w.Dv * 4].view(torch.float32).view(w.N, w.Dv).double().cpu().numpy()
+        a2 = saved[r256(xb) + row0 * w.Dv * 2:r256(xb) + (row0 + w.N) * w.Dv * 2].view(torch.bfloat16)
+        a2 = a2.view(w.N, w.Dv).double().cpu().numpy()
+        off = r256(xb) + r256(ab)
+        lse = saved[off + row0 * 8:off + (row0 + w.N) * 8].view(torch.float32).view(w.N, 2).double().cpu().numpy()
+        v = t["v"][b, h].double().numpy()
+        ref_a, ref_l = [], []
+        for qn, kn in (("q1", "k1"), ("q2", "k2")):
+            sc = t[qn][b, h].double().numpy() @ t[kn][b, h].double().numpy().T / np.sqrt(w.d)
+            ref_a.append(orc.masked_softmax_rows(sc, allowed) @ v)
+            z = np.where(allowed, sc, -np.inf) * np.log2(np.e)
+            mx = z.max(axis=1)
+            ref_l.append(mx + np.log2(np.exp2(z - mx[:, None]).sum(axis=1)))
+        rel = lambda got, ref: np.linalg.norm(got - ref) / np.linalg.norm(ref)
+        assert rel(x, ref_a[0] - lam * ref_a[1]) <= 3e-3, (b, h)
+        assert rel(a2, ref_a[1]) <= 3e-3 + 2.0 ** -8 / np.sqrt(3), (b, h)
+        for m in range(2):
+            assert np.abs(lse[:, m] - ref_l[m]).max() <= 1e-4, (b, h, m)
+
+
 def test_training_pair_prefill_workload_sampled_heads():
     """The B=4, H=16, N=2048 prefill workload through the training pair: every gradient of
     three heads against the oracle, and dlambda, dw over all 64 heads."""
