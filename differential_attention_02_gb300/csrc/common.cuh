@@ -22,7 +22,10 @@ constexpr int32_t kErrWaitTimeout = 1;
 // Upper bound for one barrier wait. No legitimate wait in these kernels comes
 // within orders of magnitude of it; reaching it means a lost arrival.
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
-constexpr uint32_t kWaitMaxIters = 1u << 16;         // outer polling rounds of one wait
+// Outer polling rounds of one wait: a backstop should %globaltimer not advance. A failed
+// try_wait without a suspend hint can return within tens of nanoseconds, so the cap is set
+// for eight of them per round to outlast the 1 s time bound.
+constexpr uint32_t kWaitMaxIters = 1u << 23;
 
 __device__ __forceinline__ void report_error(int32_t* err, int32_t site, int32_t kind) {
     if (err != nullptr) atomicCAS(err, 0, (site << 8) | kind);
